@@ -1,0 +1,110 @@
+"""Seeded synthetic inputs for the block-quantized mat-vec workloads.
+
+This module holds shape tables and random-number generation only: no
+quantization, no dequantization and none of the mat-vec's arithmetic.  The
+oracle-side tests, the CUDA-side tests and ``bench.py`` all draw their fp32
+weights and activations here, so both sides see the same numbers.
+
+Recipe (model weights are not needed and not available; these stand in):
+
+* W is fp32, drawn as ``standard_normal(float32) * float32(0.02)`` in blocks of
+  4096 rows; block ``i`` of a matrix with seed ``s`` uses
+  ``Generator(PCG64(SeedSequence(s, spawn_key=(i,))))``, so any row can be
+  regenerated without drawing the whole matrix.
+* x is fp32 N(0, 1): one ``[4, n_in]`` draw from seed ``s + 1``; a call with
+  ``ntok = k`` uses rows ``0..k-1``, so token 0 of every ntok is the same vector.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+ROW_CHUNK = 4096
+W_STD = np.float32(0.02)
+MAX_NTOK = 4
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    fmt: str          # "q8_0" | "q4_0" | "affine4_g64" | "bf16"
+    n_out: int
+    n_in: int
+    seed: int
+    argmax: bool = False
+    note: str = ""
+
+
+# The five workload families of the mat-vec at ntok = 1..4 (shapes are n_out x n_in).
+WORKLOADS: dict[str, Workload] = {w.name: w for w in [
+    # config 0: the small square projection.
+    Workload("q8_0_2560x2560", "q8_0", 2560, 2560, 100, note="small case"),
+    # config 1: the dense projection set, n_in -> n_out = 2560->6144/10240/12288 and 6144->2560.
+    Workload("q8_0_6144x2560", "q8_0", 6144, 2560, 110),
+    Workload("q8_0_10240x2560", "q8_0", 10240, 2560, 111),
+    Workload("q8_0_12288x2560", "q8_0", 12288, 2560, 112),
+    Workload("q8_0_2560x6144", "q8_0", 2560, 6144, 113),
+    # config 2: the 8192x2560 format comparison, Q4_0 and BF16 from the same fp32 W.
+    Workload("q4_0_8192x2560", "q4_0", 8192, 2560, 120),
+    Workload("bf16_8192x2560", "bf16", 8192, 2560, 120),
+    # config 3: Q8_0 LM head with fused argmax; the drafted-vocab variant is a row prefix.
+    Workload("q8_0_head_248320x2560", "q8_0", 248320, 2560, 130, argmax=True),
+    Workload("q8_0_head_106299x2560", "q8_0", 106299, 2560, 130, argmax=True,
+             note="first 106299 rows of the 248320-row head"),
+    # config 4: affine 4-bit (group 64) drafter LM head with fused argmax.
+    Workload("affine4_head_248320x5120", "affine4_g64", 248320, 5120, 140, argmax=True),
+]}
+
+# The dense projection set timed as one step by bench.py.
+DENSE_SET = ["q8_0_6144x2560", "q8_0_10240x2560", "q8_0_12288x2560", "q8_0_2560x6144"]
+
+
+def _chunk_rng(seed: int, chunk: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(chunk,))))
+
+
+def weight_chunk(seed: int, n_out: int, n_in: int, chunk: int) -> np.ndarray:
+    """Rows ``[chunk*4096, min(n_out, (chunk+1)*4096))`` of the fp32 weight matrix."""
+    r0 = chunk * ROW_CHUNK
+    if r0 >= n_out or chunk < 0:
+        raise IndexError(f"chunk {chunk} outside a {n_out}-row matrix")
+    rows = min(ROW_CHUNK, n_out - r0)
+    z = _chunk_rng(seed, chunk).standard_normal((rows, n_in), dtype=np.float32)
+    return z * W_STD
+
+
+def iter_weight_chunks(seed: int, n_out: int, n_in: int):
+    """Yield ``(row0, W_chunk)`` over the whole matrix, 4096 rows at a time."""
+    for c in range((n_out + ROW_CHUNK - 1) // ROW_CHUNK):
+        yield c * ROW_CHUNK, weight_chunk(seed, n_out, n_in, c)
+
+
+def weights(seed: int, n_out: int, n_in: int) -> np.ndarray:
+    """The whole fp32 matrix (small shapes only)."""
+    return np.concatenate([w for _, w in iter_weight_chunks(seed, n_out, n_in)], axis=0)
+
+
+def weight_rows(seed: int, n_out: int, n_in: int, rows) -> np.ndarray:
+    """Selected rows of the fp32 matrix, regenerating only the 4096-row blocks they live in."""
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, n_in), dtype=np.float32)
+    for c in np.unique(rows // ROW_CHUNK):
+        blk = weight_chunk(seed, n_out, n_in, int(c))
+        sel = np.nonzero(rows // ROW_CHUNK == c)[0]
+        out[sel] = blk[rows[sel] - c * ROW_CHUNK]
+    return out
+
+
+def activations(seed: int, n_in: int, ntok: int) -> np.ndarray:
+    """x as fp32 ``[ntok, n_in]``: rows 0..ntok-1 of one ``[4, n_in]`` N(0,1) draw from ``seed + 1``."""
+    if not 1 <= ntok <= MAX_NTOK:
+        raise ValueError("ntok must be in 1..4")
+    g = np.random.Generator(np.random.PCG64(seed + 1))
+    return np.ascontiguousarray(g.standard_normal((MAX_NTOK, n_in), dtype=np.float32)[:ntok])
+
+
+def gaussian(seed: int, shape, scale: float = 1.0) -> np.ndarray:
+    """A generic seeded fp32 normal array for small test cases."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    return g.standard_normal(shape, dtype=np.float32) * np.float32(scale)
