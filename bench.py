@@ -1,0 +1,487 @@
+#!/usr/bin/env python
+"""Benchmark: effective weight GB/s of the block-quantized mat-vec (qgemv) on GB300.
+
+One step = one pass of the Q8_0 dense projection set (n_in -> n_out: 2560->6144,
+2560->10240, 2560->12288, 6144->2560) at ntok = 1, 2, 3 and 4: 16 kernel launches
+over 379 MB of distinct weights.  value = weight bytes / time (scales included,
+1e9 B per GB).  The launches of a step are replayed from a CUDA graph (the
+kernels are 2-20 us long; launching them one by one from Python would time the
+host).  Also reported, outside the timed region:
+
+* per_workload: every workload family x ntok (including the fused LM-head
+  argmax heads), median of 5 graph replays of 50 launches rotating over weight
+  copies totalling >= 4x L2;
+* e2e: the same step through the public API with host buffers, per call
+  (pinned x uploaded, y read back, host synchronized every step, no graph);
+* roofline of the dominant kernel, cpu_baseline (the fp64 oracle on the host).
+
+--impl reference times the CPU oracle instead (the only reference there is).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "effective weight GB/s and % of GB300 HBM peak, qgemv at ntok=1..4"
+WORKLOAD_NAME = ("Q8_0 dense projection set (n_in->n_out 2560->6144, 2560->10240, "
+                 "2560->12288, 6144->2560) at ntok=1,2,3,4")
+NTOKS = (1, 2, 3, 4)
+PEAK_FALLBACK_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-detail", action="store_true", help="skip the per-workload table")
+    p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--detail-only", default="", help="comma list of workload names for the table")
+    p.add_argument("--cpu-worker", default="", help=argparse.SUPPRESS)
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return PEAK_FALLBACK_GBS, "fallback"
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "block_quantized_token_format_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def algo_bytes(fmt, n_out, n_in, ntok, argmax=False):
+    b = workloads_bytes(fmt, n_out, n_in) + 4 * ntok * (n_in + n_out)
+    return b + (4 * ntok if argmax else 0)
+
+
+def workloads_bytes(fmt, n_out, n_in):
+    n = n_out * n_in
+    return {"q8_0": n // 32 * 34, "q4_0": n // 32 * 18, "affine4_g64": n // 2 + n // 64 * 4, "bf16": 2 * n}[fmt]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            if t0 - 0.05 <= ts <= t1 + 0.15:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def gen_packed(qg, w: workloads.Workload, threads: int = 16) -> np.ndarray:
+    """Device-layout bytes of a whole workload matrix, generated 4096 rows at a time."""
+    stride = qg.qg_row_stride(w.fmt, w.n_in)
+    out = np.empty(w.n_out * stride, dtype=np.uint8)
+    n_chunks = (w.n_out + workloads.ROW_CHUNK - 1) // workloads.ROW_CHUNK
+
+    def one(c):
+        Wc = workloads.weight_chunk(w.seed, w.n_out, w.n_in, c)
+        r0 = c * workloads.ROW_CHUNK
+        qg.qg_pack(w.fmt, Wc, out=out[r0 * stride:(r0 + Wc.shape[0]) * stride])
+
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(one, range(n_chunks)))
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+
+def cpu_worker(spec: str):
+    """Run inside a fresh process with BLAS pinned to one thread: time the oracle."""
+    import oracle
+    cfg = json.loads(spec)
+    names, steps, warm, frac = cfg["names"], cfg["steps"], cfg["warmup"], cfg["row_frac"]
+    data = []
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        rows = max(64, int(math.ceil(w.n_out * frac)))
+        W = workloads.weight_rows(w.seed, w.n_out, w.n_in, np.arange(rows))
+        data.append((w, rows, oracle.quantize(w.fmt, W), workloads.activations(w.seed, w.n_in, 4)))
+    per_step_bytes = sum(workloads_bytes(w.fmt, rows, w.n_in) for w, rows, _, _ in data) * len(NTOKS)
+
+    def step():
+        for ntok in NTOKS:
+            for w, rows, canon, x in data:
+                oracle.gemv(w.fmt, canon, rows, w.n_in, x[:ntok])
+
+    for _ in range(warm):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = time.perf_counter() - t0
+    print(json.dumps({"seconds": dt, "steps": steps, "bytes_per_step": per_step_bytes,
+                      "rows": {w.name: rows for w, rows, _, _ in data}}))
+
+
+def run_cpu_oracle(names, steps, warmup, row_frac):
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = "1"
+    spec = json.dumps({"names": names, "steps": steps, "warmup": warmup, "row_frac": row_frac})
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", spec],
+                       capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ----------------------------------------------------------------------------- GPU legs
+
+def main_gpu(args, rank, world, local_rank):
+    import torch
+    import block_quantized_token_format_gb300 as qg
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+    peak, peak_kind = peaks()
+    stream = torch.cuda.current_stream()
+
+    # --- the dense set: two sets of 16 distinct weight buffers (one per shape x ntok)
+    dense = [workloads.WORKLOADS[n] for n in workloads.DENSE_SET]
+    host = {w.name: gen_packed(qg, w) for w in dense}
+    bufs = {}
+    for s in range(2):
+        for w in dense:
+            base = torch.from_numpy(host[w.name]).to(dev)
+            for ntok in NTOKS:
+                bufs[(s, w.name, ntok)] = base if ntok == 1 else base.clone()
+    xs = {w.name: torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).to(dev) for w in dense}
+    ys = {(w.name, ntok): torch.empty((ntok, w.n_out), dtype=torch.float32, device=dev)
+          for w in dense for ntok in NTOKS}
+    step_bytes = sum(workloads_bytes(w.fmt, w.n_out, w.n_in) for w in dense) * len(NTOKS)
+    distinct = sum(b.numel() for b in bufs.values())
+
+    def launches(s, ntoks):
+        for ntok in ntoks:
+            for w in dense:
+                qg.qgemv(w.fmt, bufs[(s, w.name, ntok)], w.n_out, w.n_in, xs[w.name], ys[(w.name, ntok)], ntok)
+
+    for s in range(2):                                  # warm every kernel / cache occupancy before capture
+        launches(s, NTOKS)
+    torch.cuda.synchronize()
+    graphs = []
+    for s in range(2):
+        ga, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga, capture_error_mode="thread_local"):
+            launches(s, (1, 2, 3))
+        with torch.cuda.graph(gb, capture_error_mode="thread_local"):
+            launches(s, (4,))
+        graphs.append((ga, gb))
+    torch.cuda.synchronize()
+
+    K, Wm = args.steps, max(3, args.warmup)
+    for i in range(Wm):
+        ga, gb = graphs[i % 2]
+        ga.replay()
+        gb.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else (str(uuid) if uuid else str(local_rank))
+    with ClockSampler(gpu_id) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        start.record()
+        for i in range(K):
+            ga, gb = graphs[i % 2]
+            ga.replay()
+            ev[i][0].record()
+            gb.replay()
+            ev[i][1].record()
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+        t_wall1 = time.time()
+    clocks = clk.summary(t_wall0, t_wall1)
+    total_ms = start.elapsed_time(end)
+    dom_ms = sum(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    value = step_bytes * K * world / (total_ms * 1e-3) / 1e9
+
+    # --- roofline of the dominant kernel: the ntok=4 launches of the step (4 per step)
+    dom_bytes = sum(algo_bytes(w.fmt, w.n_out, w.n_in, 4) for w in dense)
+    achieved = dom_bytes * K / (dom_ms * 1e-3) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            td = json.load(f)
+        if td.get("csrc_hash") == csrc_hash():
+            traffic = td.get("traffic_bytes_per_launch")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": "qgemv_kernel<Q8_0, NTOK=4> over the dense set (4 launches per step)",
+                "algorithmic_bytes_per_launch": round(dom_bytes / 4), "peak_kind": peak_kind,
+                "ms_per_step_share": round(dom_ms / K / ms_per_step, 4)}
+
+    result = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+              "warmup": Wm, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
+              "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+              "config": {"workload": WORKLOAD_NAME, "formats": "Q8_0 weights, fp32 x and y, fp32 accumulation",
+                         "weight_bytes_per_step": step_bytes, "launches_per_step": 16,
+                         "l2": f"inputs larger than L2: each step reads {step_bytes / 1e6:.0f} MB of distinct "
+                               f"weights; two alternating sets ({distinct / 1e6:.0f} MB) vs L2 {l2 / 1e6:.0f} MB",
+                         "timing": "CUDA graph replay of the step's launches, CUDA events on the launch stream",
+                         "parallelism": "replicas" if world > 1 else "single GPU"},
+              "frac_of_peak": round(value / world / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
+              "frac_of_nominal_7900": round(value / world / 7900.0, 4),
+              "clocks": clocks, "gpu_launches": 16 * K, "roofline": roofline}
+
+    # --- e2e through the public API with host buffers (no graph), rank-local
+    pin_x = {w.name: torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).pin_memory() for w in dense}
+    pin_y = {k: torch.empty(v.shape, dtype=torch.float32).pin_memory() for k, v in ys.items()}
+    dx = {w.name: torch.empty((4, w.n_in), dtype=torch.float32, device=dev) for w in dense}
+    h2d = sum(v.numel() * 4 for v in pin_x.values())
+    d2h = sum(v.numel() * 4 for v in pin_y.values())
+
+    def e2e_step(s):
+        for w in dense:
+            dx[w.name].copy_(pin_x[w.name], non_blocking=True)
+        for ntok in NTOKS:
+            for w in dense:
+                qg.qgemv(w.fmt, bufs[(s, w.name, ntok)], w.n_out, w.n_in, dx[w.name], ys[(w.name, ntok)], ntok)
+        for k, v in ys.items():
+            pin_y[k].copy_(v, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(5):
+        e2e_step(i % 2)
+    n_e2e = max(50, min(2000, K // 10))
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        e2e_step(i % 2)
+    e2e_s = time.perf_counter() - t0
+    result["e2e"] = {"value": round(step_bytes * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                     "how": "python qgemv calls per launch (ctypes), pinned x uploaded and y read back, "
+                            "host synchronized every step; no CUDA graph"}
+
+    if rank == 0 and not args.no_detail:
+        result["per_workload"] = detail_table(args, qg, torch, dev, l2, peak)
+
+    if rank == 0 and not args.no_cpu:
+        try:
+            cores = 1
+            r = run_cpu_oracle(workloads.DENSE_SET, steps=1, warmup=0, row_frac=1.0)
+            result["cpu_baseline"] = {"value": round(r["bytes_per_step"] * r["steps"] / r["seconds"] / 1e9, 4),
+                                      "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                      "sample": "one full step of the workload (16 oracle calls: 4 shapes x ntok "
+                                                "1..4, all rows), numpy fp64, BLAS pinned to 1 thread",
+                                      "seconds": round(r["seconds"], 3),
+                                      "host_cores_available": len(os.sched_getaffinity(0))}
+        except Exception as e:  # noqa: BLE001
+            result["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                      "sample": f"failed: {e}"}
+    return result
+
+
+def detail_table(args, qg, torch, dev, l2, peak):
+    """Every workload x ntok: median of 5 replays of a 50-launch graph over rotating copies."""
+    names = [n for n in workloads.WORKLOADS] if not args.detail_only else args.detail_only.split(",")
+    table = {}
+    cache = {}
+    for name in names:
+        w = workloads.WORKLOADS[name]
+        src = name
+        if name == "q8_0_head_106299x2560":
+            src = "q8_0_head_248320x2560"
+        if src not in cache:
+            ws = workloads.WORKLOADS[src]
+            cache.clear()
+            torch.cuda.empty_cache()
+            cache[src] = torch.from_numpy(gen_packed(qg, ws)).to(dev)
+        base = cache[src]
+        wbytes = workloads_bytes(w.fmt, w.n_out, w.n_in)
+        copies = max(1, math.ceil(4 * l2 / base.numel()))
+        pool = [base] + [base.clone() for _ in range(copies - 1)]
+        x = torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).to(dev)
+        y = torch.empty((4, w.n_out), dtype=torch.float32, device=dev)
+        am = torch.empty(4, dtype=torch.int32, device=dev)
+        wsp = torch.zeros(qg.qgemv_argmax_workspace_bytes(w.n_out, 4), dtype=torch.uint8, device=dev)
+        row = {}
+        for ntok in NTOKS:
+            def call(i):
+                if w.argmax:
+                    qg.qgemv_argmax(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y, am, wsp, ntok)
+                else:
+                    qg.qgemv(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y, ntok)
+            n = 50
+            for i in range(copies + 2):
+                call(i)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                for i in range(n):
+                    call(i)
+            g.replay()
+            times = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                times.append(a.elapsed_time(b) / n * 1e3)
+            us = statistics.median(times)
+            gbs = wbytes / (us * 1e-6) / 1e9
+            row[str(ntok)] = {"us": round(us, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "tile": qg.qg_describe_tile(w.fmt, w.n_out, w.n_in, ntok)}
+            del g
+        table[name] = {"fmt": w.fmt, "n_out": w.n_out, "n_in": w.n_in, "weight_bytes": wbytes,
+                       "call": "qgemv_argmax" if w.argmax else "qgemv", "copies": copies, "ntok": row}
+        del pool
+    cache.clear()
+    torch.cuda.empty_cache()
+    return table
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    K, Wm = args.steps, max(3, args.warmup)
+    full_rows = sum(workloads.WORKLOADS[n].n_out for n in workloads.DENSE_SET)
+    # a full step of the oracle takes seconds; sample rows so the run ends within ~2 minutes
+    est_full_step_s = 6.0
+    frac = min(1.0, 120.0 / ((K + Wm) * est_full_step_s))
+    r = run_cpu_oracle(workloads.DENSE_SET, steps=K, warmup=Wm, row_frac=frac)
+    value = r["bytes_per_step"] * r["steps"] / r["seconds"] / 1e9
+    sample = (f"each step: the oracle on the first {frac:.4%} of each shape's rows (>= 64 rows), "
+              f"4 shapes x ntok 1..4, numpy fp64, BLAS pinned to 1 thread")
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": Wm, "ms_per_step": round(r["seconds"] / K * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD_NAME, "rows_sampled": r["rows"]},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------- entry
+
+def main():
+    args = parse_args()
+    if args.cpu_worker:
+        cpu_worker(args.cpu_worker)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.impl == "reference":
+        res = reference_arm(args, rank, world)
+    else:
+        res = main_gpu(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+"""Python binding of the block-quantized weight mat-vec library (GB300, sm_103a).
+
+A thin ctypes layer over ``_lib/libqgemv.so`` (C ABI in ``include/qgemv.h``):
+the functions carry the C names and only marshal arguments.  Device buffers
+are torch CUDA tensors (or raw device addresses); host buffers for the packer
+are numpy arrays.  Every step of the mat-vec runs in the library's CUDA
+kernels; if the library is missing, every call raises.
+
+    y[t, o] = sum_i dequant(W)[o, i] * x[t, i],  ntok = 1..4
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "QG_Q8_0", "QG_Q4_0", "QG_AFFINE4_G64", "QG_BF16", "FORMATS", "QGError", "load_library",
+    "qg_strerror", "qg_abi_version", "qg_canonical_bytes", "qg_packed_bytes", "qg_row_stride",
+    "qg_quantize", "qg_to_device_layout", "qg_pack", "qgemv", "qgemv_argmax_workspace_bytes",
+    "qgemv_argmax", "qg_set_tile_override", "qg_describe_tile", "weight_bytes",
+]
+
+QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
+FORMATS = {"q8_0": QG_Q8_0, "q4_0": QG_Q4_0, "affine4_g64": QG_AFFINE4_G64, "bf16": QG_BF16}
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqgemv.so")
+_lib = None
+
+
+class QGError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {qg_strerror(status)} (status {status})")
+
+
+def _fmt(fmt) -> int:
+    if isinstance(fmt, str):
+        return FORMATS[fmt]
+    return int(fmt)
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the shared library once (build it with ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or _LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing (run __graft_entry__.build())")
+    try:
+        import torch  # noqa: F401  (load torch's CUDA runtime first so one copy is shared)
+    except ImportError:
+        pass
+    lib = ctypes.CDLL(p)
+    i64, vp, sz, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    sig = {
+        "qg_strerror": (ctypes.c_char_p, [i32]),
+        "qg_abi_version": (i32, []),
+        "qg_canonical_bytes": (sz, [i32, i64, i64]),
+        "qg_packed_bytes": (sz, [i32, i64, i64]),
+        "qg_row_stride": (i64, [i32, i64]),
+        "qg_quantize": (i32, [i32, vp, i64, i64, vp]),
+        "qg_to_device_layout": (i32, [i32, vp, i64, i64, vp]),
+        "qg_pack": (i32, [i32, vp, i64, i64, vp]),
+        "qgemv": (i32, [i32, vp, i64, i64, vp, vp, i32, vp]),
+        "qgemv_argmax_workspace_bytes": (sz, [i64, i32]),
+        "qgemv_argmax": (i32, [i32, vp, i64, i64, vp, vp, vp, i32, vp, sz, vp]),
+        "qg_set_tile_override": (i32, [ctypes.c_char_p]),
+        "qg_describe_tile": (i32, [i32, i64, i64, i32, ctypes.c_char_p, sz]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> int | None:
+    """Device address of a torch tensor / raw int / None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr()
+    raise TypeError(f"expected a torch tensor or an address, got {type(t)}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise QGError(status, what)
+
+
+# ----------------------------------------------------------------------------- sizes
+
+def qg_strerror(status: int) -> str:
+    return load_library().qg_strerror(int(status)).decode()
+
+
+def qg_abi_version() -> int:
+    return load_library().qg_abi_version()
+
+
+def qg_canonical_bytes(fmt, n_out: int, n_in: int) -> int:
+    return load_library().qg_canonical_bytes(_fmt(fmt), n_out, n_in)
+
+
+weight_bytes = qg_canonical_bytes
+
+
+def qg_packed_bytes(fmt, n_out: int, n_in: int) -> int:
+    return load_library().qg_packed_bytes(_fmt(fmt), n_out, n_in)
+
+
+def qg_row_stride(fmt, n_in: int) -> int:
+    return load_library().qg_row_stride(_fmt(fmt), n_in)
+
+
+# ----------------------------------------------------------------------------- host packer
+
+def _f32_host(W) -> np.ndarray:
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    if W.ndim != 2:
+        raise ValueError("W must be [n_out, n_in]")
+    return W
+
+
+def qg_quantize(fmt, W) -> np.ndarray:
+    """fp32 ``[n_out, n_in]`` -> canonical bytes (uint8)."""
+    W = _f32_host(W)
+    n_out, n_in = W.shape
+    out = np.empty(max(1, qg_canonical_bytes(fmt, n_out, n_in)), dtype=np.uint8)
+    _check(load_library().qg_quantize(_fmt(fmt), W.ctypes.data, n_out, n_in, out.ctypes.data), "qg_quantize")
+    return out
+
+
+def qg_to_device_layout(fmt, canonical, n_out: int, n_in: int) -> np.ndarray:
+    src = np.ascontiguousarray(canonical, dtype=np.uint8)
+    if src.size != qg_canonical_bytes(fmt, n_out, n_in):
+        raise ValueError("canonical buffer has the wrong size")
+    out = np.empty(max(1, qg_packed_bytes(fmt, n_out, n_in)), dtype=np.uint8)
+    _check(load_library().qg_to_device_layout(_fmt(fmt), src.ctypes.data, n_out, n_in, out.ctypes.data),
+           "qg_to_device_layout")
+    return out
+
+
+def qg_pack(fmt, W, out: np.ndarray | None = None) -> np.ndarray:
+    """fp32 ``[n_out, n_in]`` -> device-layout bytes (uint8), optionally into ``out``."""
+    W = _f32_host(W)
+    n_out, n_in = W.shape
+    n = qg_packed_bytes(fmt, n_out, n_in)
+    if out is None:
+        out = np.empty(max(1, n), dtype=np.uint8)
+    if out.dtype != np.uint8 or not out.flags["C_CONTIGUOUS"] or out.size < n:
+        raise ValueError("out must be a contiguous uint8 array of qg_packed_bytes bytes")
+    _check(load_library().qg_pack(_fmt(fmt), W.ctypes.data, n_out, n_in, out.ctypes.data), "qg_pack")
+    return out
+
+
+# ----------------------------------------------------------------------------- the mat-vec
+
+def qgemv(fmt, W, n_out: int, n_in: int, x, y, ntok: int | None = None, stream=None) -> None:
+    """Enqueue ``y[t, o] = sum_i dequant(W)[o, i] * x[t, i]`` on ``stream`` (default: torch's current)."""
+    if ntok is None:
+        ntok = x.shape[0] if getattr(x, "dim", lambda: 1)() == 2 else 1
+    st = load_library().qgemv(_fmt(fmt), _ptr(W), n_out, n_in, _ptr(x), _ptr(y), int(ntok), _stream(stream))
+    _check(st, "qgemv")
+
+
+def qgemv_argmax_workspace_bytes(n_out: int, ntok: int) -> int:
+    return load_library().qgemv_argmax_workspace_bytes(n_out, ntok)
+
+
+def qgemv_argmax(fmt, W, n_out: int, n_in: int, x, y, argmax, workspace, ntok: int | None = None,
+                 workspace_bytes: int | None = None, stream=None) -> None:
+    """Enqueue the mat-vec fused with the per-token first-index argmax (y may be None)."""
+    if ntok is None:
+        ntok = x.shape[0] if getattr(x, "dim", lambda: 1)() == 2 else 1
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+    st = load_library().qgemv_argmax(_fmt(fmt), _ptr(W), n_out, n_in, _ptr(x), _ptr(y), _ptr(argmax),
+                                     int(ntok), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "qgemv_argmax")
+
+
+def qg_set_tile_override(spec: str | None) -> None:
+    _check(load_library().qg_set_tile_override(spec.encode() if spec else None), "qg_set_tile_override")
+
+
+def qg_describe_tile(fmt, n_out: int, n_in: int, ntok: int) -> str:
+    buf = ctypes.create_string_buffer(160)
+    _check(load_library().qg_describe_tile(_fmt(fmt), n_out, n_in, ntok, buf, len(buf)), "qg_describe_tile")
+    return buf.value.decode()

@@ -1,0 +1,261 @@
+// C ABI entry points of the mat-vec: validation, tile selection, launch.
+// The operation and every argument rule are documented in include/qgemv.h.
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "qgemv_kernels.cuh"
+#include "tile_select.h"
+
+namespace qg {
+
+const void* kernel_lookup_fmt0(int, int, int, bool);
+const void* kernel_lookup_fmt1(int, int, int, bool);
+const void* kernel_lookup_fmt2(int, int, int, bool);
+const void* kernel_lookup_fmt3(int, int, int, bool);
+
+const void* kernel_lookup(int fmt, int ntok, int rpw, int depth, bool argmax) {
+    switch (fmt) {
+        case 0: return kernel_lookup_fmt0(ntok, rpw, depth, argmax);
+        case 1: return kernel_lookup_fmt1(ntok, rpw, depth, argmax);
+        case 2: return kernel_lookup_fmt2(ntok, rpw, depth, argmax);
+        case 3: return kernel_lookup_fmt3(ntok, rpw, depth, argmax);
+        default: return nullptr;
+    }
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device constants, read once.
+struct DevInfo {
+    std::atomic<int> sms{0};
+    std::atomic<int> smem_optin{0};
+};
+DevInfo g_dev[kMaxDevices];
+
+// Tile override: QGEMV_TILE at first use, or qg_set_tile_override.
+std::mutex g_override_mu;
+TileOverride g_override;
+std::once_flag g_env_once;
+
+void read_env_override() {
+    std::call_once(g_env_once, [] {
+        const char* e = std::getenv("QGEMV_TILE");
+        TileOverride o;
+        if (e && parse_tile_spec(e, &o)) {
+            std::lock_guard<std::mutex> lk(g_override_mu);
+            g_override = o;
+        }
+    });
+}
+
+TileOverride current_override() {
+    read_env_override();
+    std::lock_guard<std::mutex> lk(g_override_mu);
+    return g_override;
+}
+
+// Occupancy, cached per (kernel, device, threads, smem bytes).  The first use of a
+// kernel on a device raises its dynamic shared memory limit to the device maximum.
+std::mutex g_occ_mu;
+std::map<std::tuple<const void*, int, size_t, int>, int> g_occ;
+std::map<std::pair<const void*, int>, bool> g_configured;
+
+qg_status device_info(int* dev, int* sms, int* smem_optin) {
+    if (cudaGetDevice(dev) != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
+    if (*dev < 0 || *dev >= kMaxDevices) return QG_EUNSUPPORTED;
+    DevInfo& d = g_dev[*dev];
+    int s = d.sms.load(std::memory_order_relaxed);
+    int m = d.smem_optin.load(std::memory_order_relaxed);
+    if (s == 0 || m == 0) {
+        if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&m, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev) != cudaSuccess) {
+            cudaGetLastError();
+            return QG_ECUDA;
+        }
+        d.sms.store(s, std::memory_order_relaxed);
+        d.smem_optin.store(m, std::memory_order_relaxed);
+    }
+    *sms = s;
+    *smem_optin = m;
+    return QG_OK;
+}
+
+// Blocks of `fn` resident per SM with `threads` threads and `smem` dynamic bytes (0 on error).
+int blocks_per_sm(const void* fn, int dev, int optin, int threads, size_t smem) {
+    auto key = std::make_tuple(fn, dev, smem, threads);
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+    auto ck = std::make_pair(fn, dev);
+    if (!g_configured[ck]) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess ||
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - int(fa.sharedSizeBytes)) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        g_configured[ck] = true;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    g_occ[key] = n;
+    return n;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Plan {
+    const void* fn = nullptr;
+    Tile tile;
+    int grid = 0;
+    int threads = 0;
+    size_t smem = 0;
+};
+
+// Everything up to the launch.  Checks that need no CUDA call come first.
+qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argmax, Plan* plan) {
+    int dev = 0, sms = 0, optin = 0;
+    qg_status st = device_info(&dev, &sms, &optin);
+    if (st != QG_OK) return st;
+    const size_t smem = smem_bytes(fmt, ntok, int(n_in));
+    if (smem + 1024 > size_t(optin)) return QG_EUNSUPPORTED;   // static smem of the argmax kernels fits in 1 KB
+
+    Tile t = apply_override(select_tile(fmt, n_out, n_in, ntok), current_override());
+    if (!rpw_ok(t.rpw) || !depth_ok(t.depth) || t.warps < 1 || t.warps > 8 || t.ctas < 1) return QG_EINVAL;
+    const void* fn = kernel_lookup(fmt, ntok, t.rpw, t.depth, argmax);
+    if (!fn) return QG_EUNSUPPORTED;
+    const int threads = 32 * t.warps;
+    const int occ = blocks_per_sm(fn, dev, optin, threads, smem);
+    if (occ < 1) return QG_EUNSUPPORTED;
+    const int64_t ngroups = (n_out + t.rpw - 1) / t.rpw;
+    const int64_t need = (ngroups + t.warps - 1) / t.warps;
+    int64_t grid = int64_t(sms) * std::min(t.ctas, occ);
+    if (need < grid) grid = need;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    if (grid < 1) grid = 1;
+    plan->fn = fn;
+    plan->tile = t;
+    plan->tile.ctas = std::min(t.ctas, occ);
+    plan->grid = int(grid);
+    plan->threads = threads;
+    plan->smem = smem;
+    return QG_OK;
+}
+
+qg_status check_common(int fmt, const void* W, int64_t n_out, int64_t n_in, const float* x, int ntok) {
+    if (!shape_valid(fmt, n_out, n_in)) return QG_EINVAL;
+    if (ntok < 1 || ntok > kMaxNtok) return QG_EINVAL;
+    if (!W || !x) return QG_EINVAL;
+    if (!aligned(W, 16) || !aligned(x, 16)) return QG_EALIGN;
+    return QG_OK;
+}
+
+qg_status launch(const Plan& p, const KernelArgs& args, void* stream) {
+    KernelArgs a = args;
+    void* params[] = {&a};
+    cudaError_t e = cudaLaunchKernel(p.fn, dim3(p.grid), dim3(p.threads), params, p.smem,
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
+    return QG_OK;
+}
+
+}  // namespace
+}  // namespace qg
+
+using namespace qg;
+
+extern "C" {
+
+const char* qg_strerror(qg_status s) {
+    switch (s) {
+        case QG_OK: return "ok";
+        case QG_EINVAL: return "invalid argument (format, size, ntok or null pointer)";
+        case QG_EALIGN: return "pointer not aligned (W, x and workspace need 16 bytes; y and argmax 4)";
+        case QG_EUNSUPPORTED: return "unsupported shape or device (n_in too large for shared memory?)";
+        case QG_EWORKSPACE: return "argmax workspace missing or smaller than qgemv_argmax_workspace_bytes()";
+        case QG_ECUDA: return "CUDA runtime error at launch";
+        default: return "unknown status";
+    }
+}
+
+int qg_abi_version(void) { return 1; }
+
+qg_status qgemv(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, const float* x, float* y,
+                int ntok, void* stream) {
+    qg_status st = check_common(fmt, W, n_out, n_in, x, ntok);
+    if (st != QG_OK) return st;
+    if (!y) return QG_EINVAL;
+    if (!aligned(y, 4)) return QG_EALIGN;
+    Plan p;
+    st = plan_launch(fmt, n_out, n_in, ntok, false, &p);
+    if (st != QG_OK) return st;
+    KernelArgs a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.x = x;
+    a.y = y;
+    a.stride = row_stride(fmt, n_in);
+    a.n_out = int(n_out);
+    a.n_in = int(n_in);
+    return launch(p, a, stream);
+}
+
+size_t qgemv_argmax_workspace_bytes(int64_t n_out, int ntok) {
+    if (n_out < 1 || ntok < 1 || ntok > kMaxNtok) return 0;
+    return 16 + size_t(kMaxGrid) * size_t(ntok) * sizeof(ArgmaxPartial);
+}
+
+qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, const float* x, float* y,
+                       int32_t* argmax, int ntok, void* workspace, size_t workspace_bytes, void* stream) {
+    qg_status st = check_common(fmt, W, n_out, n_in, x, ntok);
+    if (st != QG_OK) return st;
+    if (!argmax) return QG_EINVAL;
+    if ((y && !aligned(y, 4)) || !aligned(argmax, 4)) return QG_EALIGN;
+    if (!workspace || workspace_bytes < qgemv_argmax_workspace_bytes(n_out, ntok)) return QG_EWORKSPACE;
+    if (!aligned(workspace, 16)) return QG_EALIGN;
+    Plan p;
+    st = plan_launch(fmt, n_out, n_in, ntok, true, &p);
+    if (st != QG_OK) return st;
+    KernelArgs a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.x = x;
+    a.y = y;
+    a.argmax = argmax;
+    a.ticket = static_cast<unsigned int*>(workspace);
+    a.partials = reinterpret_cast<ArgmaxPartial*>(static_cast<uint8_t*>(workspace) + 16);
+    a.stride = row_stride(fmt, n_in);
+    a.n_out = int(n_out);
+    a.n_in = int(n_in);
+    return launch(p, a, stream);
+}
+
+qg_status qg_set_tile_override(const char* spec) {
+    read_env_override();
+    TileOverride o;
+    if (!parse_tile_spec(spec, &o)) return QG_EINVAL;
+    std::lock_guard<std::mutex> lk(g_override_mu);
+    g_override = o;
+    return QG_OK;
+}
+
+qg_status qg_describe_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, int ntok, char* buf, size_t len) {
+    if (!buf || len == 0) return QG_EINVAL;
+    if (!shape_valid(fmt, n_out, n_in) || ntok < 1 || ntok > kMaxNtok) return QG_EINVAL;
+    Plan p;
+    qg_status st = plan_launch(fmt, n_out, n_in, ntok, false, &p);
+    if (st != QG_OK) return st;
+    std::snprintf(buf, len, "%s,grid=%d", tile_to_string(p.tile).c_str(), p.grid);
+    return QG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,27 @@
+// Instantiations of the dequant-GEMV kernel for one weight format, selected at
+// compile time by QG_INST_FMT (the build compiles this file once per format so
+// the four formats build in parallel).
+#include "qgemv_kernels.cuh"
+
+#ifndef QG_INST_FMT
+#error "compile with -DQG_INST_FMT=<0..3>"
+#endif
+
+#define QG_CAT2(a, b) a##b
+#define QG_CAT(a, b) QG_CAT2(a, b)
+
+namespace qg {
+
+const void* QG_CAT(kernel_lookup_fmt, QG_INST_FMT)(int ntok, int rpw, int depth, bool argmax) {
+#define QG_E(NT, R, D)                                                                   \
+    if (ntok == NT && rpw == R && depth == D)                                            \
+        return argmax ? (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, D, true>          \
+                      : (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, D, false>;
+#define QG_E_NT(NT) QG_E(NT, 1, 2) QG_E(NT, 1, 4) QG_E(NT, 2, 2) QG_E(NT, 2, 4) QG_E(NT, 4, 2) QG_E(NT, 4, 4)
+    QG_E_NT(1) QG_E_NT(2) QG_E_NT(3) QG_E_NT(4)
+#undef QG_E_NT
+#undef QG_E
+    return nullptr;
+}
+
+}  // namespace qg

@@ -1,0 +1,161 @@
+/*
+ * qgemv.h -- C ABI of the block-quantized weight mat-vec library for GB300 (sm_103a).
+ *
+ * The operation (Track 2 Audit & Optimization Report: M5 Metal Kernels for
+ * Multi-Token Speculative Decode, section 1 item 1, the multi-token gemv over
+ * ntok activation rows; opus-mtp-turbo Track 1 report, item 3):
+ *
+ *     y[t][o] = sum_i dequant(W)[o][i] * x[t][i],   t < ntok <= 4,  o < n_out,  i < n_in
+ *
+ * and, for a vocabulary-sized head, the per-token argmax of y fused into the
+ * same kernel (perf(speculative): cut the MTP drafter's per-step cost,
+ * "Phase 2", item 2a).  The effective-bandwidth metric the library is built
+ * for is weight bytes / kernel time (Where the time goes on an M2 Max,
+ * "Dense K-quants are integer-ALU bound at small batches").
+ *
+ * Conventions for every call:
+ *   - Device buffers (W, x, y, argmax, workspace) are allocated and owned by
+ *     the caller.  qgemv and qgemv_argmax never allocate, free or synchronize;
+ *     they enqueue one kernel on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and return.
+ *   - Arguments are validated on the host before anything is launched.  A
+ *     failed check returns a negative qg_status and launches nothing.  No
+ *     call ever traps, asserts or exits.
+ *   - The calls are reentrant and thread-safe.  The tile override (below) is
+ *     process-wide.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Weight formats.  Byte counts per 32 weights: Q8_0 34, Q4_0 18, AFFINE4_G64 18, BF16 64. */
+typedef enum {
+    QG_Q8_0 = 0,        /* 32-weight blocks: fp16 d + 32 int8 q; w = q*d                         */
+    QG_Q4_0 = 1,        /* 32-weight blocks: fp16 d + 16 B of nibbles; w = (q-8)*d                */
+    QG_AFFINE4_G64 = 2, /* 64-weight groups: 4-bit q, fp16 scale s, fp16 bias b; w = q*s + b      */
+    QG_BF16 = 3         /* plain bf16                                                             */
+} qg_fmt;
+
+typedef int qg_status;
+#define QG_OK            0
+#define QG_EINVAL       (-1)  /* bad format, size, ntok or null pointer                 */
+#define QG_EALIGN       (-2)  /* a pointer is not aligned as required                     */
+#define QG_EUNSUPPORTED (-3)  /* valid but outside what the kernels handle (e.g. n_in too large) */
+#define QG_EWORKSPACE   (-4)  /* argmax workspace missing or too small                  */
+#define QG_ECUDA        (-5)  /* the CUDA runtime reported an error at launch             */
+
+/* A static, human-readable string for a status code. */
+const char* qg_strerror(qg_status status);
+
+/* ABI version of this header (incremented on incompatible change). */
+int qg_abi_version(void);
+
+/* ------------------------------------------------------------------ sizes and layouts
+ * Canonical layout: the format's stored bytes, row-major, exactly the weight bytes
+ * of the bandwidth metric.
+ *   Q8_0:  per 32-block: little-endian fp16 d, then 32 int8 q.
+ *   Q4_0:  per 32-block: fp16 d, then 16 bytes; byte j holds element j in its low
+ *          nibble and element j+16 in its high nibble.
+ *   AFFINE4_G64: three planes, one after the other: uint32 words [n_out][n_in/8]
+ *          (element k of a word at bits [4k,4k+4)), fp16 scales [n_out][n_in/64],
+ *          fp16 biases [n_out][n_in/64].
+ *   BF16:  bf16 [n_out][n_in].
+ * Device layout: what qgemv reads.  Row-interleaved: each row holds its codes,
+ * then its scales, then zero padding up to a 16-byte multiple (no padding when
+ * n_in is a multiple of 256).  Rows are stored one after the other, so the
+ * first k rows of a packed matrix are themselves a packed k-row matrix (a
+ * reduced draft vocabulary that is a prefix of the head needs no copy).
+ *   Q8_0:  n_in bytes of q+128 (uint8), then n_in/32 fp16 d.
+ *   Q4_0:  n_in/2 bytes as uint32 words of 8 consecutive elements (element k at
+ *          bits [4k,4k+4)), then n_in/32 fp16 d.
+ *   AFFINE4_G64: the row's n_in/8 uint32 words, then n_in/64 (fp16 s, fp16 b) pairs.
+ *   BF16:  the row's n_in bf16 values.
+ * Sizes return 0 for invalid arguments. */
+size_t  qg_canonical_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);
+size_t  qg_packed_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);
+int64_t qg_row_stride(qg_fmt fmt, int64_t n_in);     /* device-layout bytes per row */
+
+/* --------------------------------------------------------------------- host packer
+ * All three work on host memory, use several CPU threads, and return QG_EINVAL on
+ * a null pointer, n_out < 1, or n_in not a multiple of the block (32 for Q8_0
+ * and Q4_0; 64 for AFFINE4_G64; 16 for BF16, the kernels' 16-weight chunk).
+ *
+ * qg_quantize: fp32 W [n_out][n_in] -> canonical bytes (qg_canonical_bytes).
+ *   Q8_0: d = max|w|/127 (fp32), stored fp16 (nearest even); q = roundf(w/d) with
+ *         the fp32 d, clamped to [-127,127]; d = 0, q = 0 for an all-zero block.
+ *   Q4_0: m = the signed value of largest |w| (first on ties); d = m/-8 (fp32),
+ *         stored fp16; q = clamp(roundf(w/d)+8, 0, 15); d = 0, q = 8 when m == 0.
+ *   AFFINE4_G64: s = fp16((max-min)/15), b = fp16(min); q = clamp(roundf((w-b)/s),
+ *         0, 15) in fp32 with the fp16 s and b; q = 0 when s == 0.
+ *   BF16: round to nearest even.
+ * qg_to_device_layout: canonical bytes -> device layout (qg_packed_bytes).
+ * qg_pack: fp32 W -> device layout directly (same bytes as the two steps). */
+qg_status qg_quantize(qg_fmt fmt, const float* W_host, int64_t n_out, int64_t n_in,
+                      void* canonical_host);
+qg_status qg_to_device_layout(qg_fmt fmt, const void* canonical_host, int64_t n_out,
+                              int64_t n_in, void* packed_host);
+qg_status qg_pack(qg_fmt fmt, const float* W_host, int64_t n_out, int64_t n_in,
+                  void* packed_host);
+
+/* --------------------------------------------------------------------------- qgemv
+ * y[t][o] = sum_i dequant(W)[o][i] * x[t][i] for t < ntok, o < n_out.
+ *   W     device, device layout (qg_packed_bytes(fmt, n_out, n_in) bytes), 16-B aligned.
+ *   x     device, fp32 [ntok][n_in] row-major, 16-B aligned.
+ *   y     device, fp32 [ntok][n_out] row-major, 4-B aligned; fully overwritten.
+ *   ntok  1..4.   n_out >= 1.   n_in a positive multiple of the block (as above)
+ *         and small enough that ntok*n_in fp32 values fit in one SM's shared
+ *         memory (QG_EUNSUPPORTED otherwise; n_in <= 12288 always fits at ntok 4).
+ * Each output is an fp32 sum over n_in whose order depends only on (fmt, n_in):
+ * row t of an ntok=k call is bitwise equal to the ntok=1 call on x[t].
+ * Asynchronous on `stream`; returns QG_ECUDA if the launch is rejected. */
+qg_status qgemv(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
+                const float* x, float* y, int ntok, void* stream);
+
+/* ----------------------------------------------------------------- qgemv_argmax
+ * The same mat-vec fused with the per-token argmax over the n_out outputs
+ * (vocabulary-sized LM heads): argmax[t] = the lowest o with y[t][o] equal to
+ * max_o y[t][o].  A NaN output never wins; argmax[t] = -1 if every output is NaN.
+ *   y          device fp32 [ntok][n_out], or NULL to skip writing the logits.
+ *              When written, the logits are bitwise those qgemv produces, and
+ *              argmax is the first-index argmax of exactly these values.
+ *   argmax     device int32 [ntok], 4-B aligned.
+ *   workspace  device, >= qgemv_argmax_workspace_bytes(n_out, ntok) bytes,
+ *              16-B aligned, ZEROED by the caller once before its first use
+ *              (cudaMemset).  Each call leaves it zeroed again for the next
+ *              call; calls sharing one workspace must be serialized on one
+ *              stream.
+ * Same size rules as qgemv; QG_EWORKSPACE if the workspace is NULL or small. */
+size_t    qgemv_argmax_workspace_bytes(int64_t n_out, int ntok);
+qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
+                       const float* x, float* y, int32_t* argmax, int ntok,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------------- tile selection
+ * The kernel geometry (rows per warp, loads in flight, warps per CTA, CTAs per
+ * SM) is chosen per (fmt, n_out, n_in, ntok) by a table measured on GB300 with
+ * a heuristic fallback (the Track 2 audit's per-shape, per-ntok tile rules are
+ * the prior art).  The reduction order never depends on this choice.
+ *
+ * qg_set_tile_override: force a geometry for later calls, e.g.
+ * "rpw=4,depth=2,warps=8,ctas=2" (any subset of the keys; rpw in {1,2,4},
+ * depth in {2,4}, warps in {1..8}, ctas in {1..8}).  NULL or "" clears it.
+ * The environment variable QGEMV_TILE, read at the first call, sets the same
+ * override.  Returns QG_EINVAL on a malformed spec (the override is unchanged).
+ *
+ * qg_describe_tile: writes the geometry a call would use into buf as
+ * "rpw=..,depth=..,warps=..,ctas=..,grid=.." (NUL-terminated, truncated to len). */
+qg_status qg_set_tile_override(const char* spec);
+qg_status qg_describe_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, int ntok,
+                           char* buf, size_t len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

@@ -1,0 +1,78 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/qgemv.h declares, and rejects bad arguments before launching anything."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_quantized_token_format_gb300 as qg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qgemv.h")
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"\b((?:qg|qgemv)\w*)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    lib = ctypes.CDLL(qg._LIB_PATH)
+    names = declared_functions()
+    assert "qgemv" in names and "qgemv_argmax" in names and "qg_pack" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version():
+    assert qg.qg_abi_version() == 1
+    for s in (0, -1, -2, -3, -4, -5):
+        assert qg.qg_strerror(s) and qg.qg_strerror(s) != "unknown status"
+    assert qg.qg_strerror(-99) == "unknown status"
+
+
+A = 1 << 20          # a 16-byte-aligned fake device address (never dereferenced)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((9, A, 8, 256, A, A, 1), -1),        # bad format
+    ((0, A, 0, 256, A, A, 1), -1),        # n_out < 1
+    ((0, A, 8, 48, A, A, 1), -1),         # n_in not a multiple of 32
+    ((2, A, 8, 96, A, A, 1), -1),         # affine needs 64
+    ((3, A, 8, 24, A, A, 1), -1),         # bf16 needs 16
+    ((0, A, 8, 256, A, A, 0), -1),        # ntok 0
+    ((0, A, 8, 256, A, A, 5), -1),        # ntok 5
+    ((0, None, 8, 256, A, A, 1), -1),     # null W
+    ((0, A, 8, 256, None, A, 1), -1),     # null x
+    ((0, A, 8, 256, A, None, 1), -1),     # null y
+    ((0, A + 8, 8, 256, A, A, 1), -2),    # W misaligned
+    ((0, A, 8, 256, A + 4, A, 1), -2),    # x misaligned
+    ((0, A, 8, 256, A, A + 2, 1), -2),    # y misaligned
+])
+def test_qgemv_rejects_before_launch(args, code):
+    lib = qg.load_library()
+    assert lib.qgemv(*args, None) == code
+
+
+def test_argmax_rejects_before_launch():
+    lib = qg.load_library()
+    ws = qg.qgemv_argmax_workspace_bytes(100, 4)
+    assert ws >= 16 + 4096 * 4 * 8
+    assert qg.qgemv_argmax_workspace_bytes(100, 0) == 0
+    assert lib.qgemv_argmax(0, A, 100, 256, A, A, A, 4, None, ws, None) == -4
+    assert lib.qgemv_argmax(0, A, 100, 256, A, A, A, 4, A, ws - 1, None) == -4
+    assert lib.qgemv_argmax(0, A, 100, 256, A, A, None, 4, A, ws, None) == -1
+    assert lib.qgemv_argmax(0, A, 100, 256, A, A, A + 2, 4, A, ws, None) == -2
+    assert lib.qgemv_argmax(0, A, 100, 256, A, A, A, 4, A + 8, ws, None) == -2
+
+
+def test_tile_override_grammar():
+    lib = qg.load_library()
+    for good in (b"rpw=4", b"depth=2,rpw=1", b"rpw=2,depth=4,warps=8,ctas=2", b"", None, b"rpw=1,"):
+        assert lib.qg_set_tile_override(good) == 0, good
+    for bad in (b"rpw=3", b"depth=5", b"warps=0", b"warps=9", b"ctas=0", b"foo=1", b"rpw", b"rpw=x", b"rpw=-1"):
+        assert lib.qg_set_tile_override(bad) == -1, bad
+    assert lib.qg_set_tile_override(None) == 0

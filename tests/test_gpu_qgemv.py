@@ -1,0 +1,190 @@
+"""GPU parity: the CUDA mat-vec (through the C ABI) against the fp64 oracle.
+
+Acceptance (per output): |y_gpu - y_ref| <= 1e-3 * sum_i |deq(W)[o,i] * x[t,i]|,
+the denominator in fp64 from the oracle; all-zero rows give exactly 0.
+fp32 accumulation over n_in <= 6144 terms stays well inside this bound.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle as ORC
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import block_quantized_token_format_gb300 as qg  # noqa: E402
+
+TOL = 1e-3
+FMTS = ["q8_0", "q4_0", "affine4_g64", "bf16"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    qg.qg_set_tile_override(None)
+    yield
+    qg.qg_set_tile_override(None)
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def upload(fmt, canon, n_out, n_in):
+    return torch.from_numpy(qg.qg_to_device_layout(fmt, canon, n_out, n_in)).to(dev())
+
+
+def gpu_qgemv(fmt, packed, n_out, n_in, x):
+    ntok = x.shape[0]
+    xd = torch.from_numpy(np.ascontiguousarray(x)).to(dev())
+    y = torch.full((ntok, n_out), float("nan"), dtype=torch.float32, device=dev())
+    qg.qgemv(fmt, packed, n_out, n_in, xd, y, ntok)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def check_close(y, ref, den, what=""):
+    y = y.astype(np.float64)
+    assert np.all(np.isfinite(y)), what
+    zero = den == 0
+    assert np.all(y[zero] == 0), what
+    rel = np.abs(y[~zero] - ref[~zero]) / den[~zero]
+    worst = float(rel.max()) if rel.size else 0.0
+    assert worst <= TOL, f"{what}: max normalised error {worst:.3g}"
+    return worst
+
+
+def n_in_for(fmt, base):
+    m = {"q8_0": 32, "q4_0": 32, "affine4_g64": 64, "bf16": 16}[fmt]
+    return max(m, base // m * m)
+
+
+# ----------------------------------------------------------------------------- small shapes, ragged tails
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n_out,n_in_base", [(1, 64), (7, 128), (97, 320), (1000, 1088), (2561, 2560), (333, 6144)])
+def test_small_shapes(fmt, n_out, n_in_base):
+    n_in = n_in_for(fmt, n_in_base)
+    W = workloads.gaussian(n_out * 7 + n_in, (n_out, n_in), 0.02)
+    if n_out > 3:
+        W[2] = 0.0
+    x = workloads.gaussian(n_out + n_in, (4, n_in))
+    canon = ORC.quantize(fmt, W)
+    packed = upload(fmt, canon, n_out, n_in)
+    ref = ORC.gemv(fmt, canon, n_out, n_in, x)
+    den = ORC.gemv_abs(fmt, canon, n_out, n_in, x)
+    for ntok in (1, 2, 3, 4):
+        y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
+        check_close(y, ref[:ntok], den[:ntok], f"{fmt} {n_out}x{n_in} ntok={ntok}")
+
+
+# ----------------------------------------------------------------------------- workload shapes, full oracle
+
+SMALL_WORKLOADS = ["q8_0_2560x2560", "q8_0_6144x2560", "q8_0_10240x2560", "q8_0_12288x2560",
+                   "q8_0_2560x6144", "q4_0_8192x2560", "bf16_8192x2560"]
+
+
+@pytest.mark.parametrize("name", SMALL_WORKLOADS)
+def test_workload_full(name):
+    w = workloads.WORKLOADS[name]
+    W = workloads.weights(w.seed, w.n_out, w.n_in)
+    x = workloads.activations(w.seed, w.n_in, 4)
+    canon = ORC.quantize(w.fmt, W)
+    assert np.array_equal(qg.qg_quantize(w.fmt, W), canon)      # the packer's bytes are the oracle's
+    packed = upload(w.fmt, canon, w.n_out, w.n_in)
+    ref = ORC.gemv(w.fmt, canon, w.n_out, w.n_in, x)
+    den = ORC.gemv_abs(w.fmt, canon, w.n_out, w.n_in, x)
+    worst = 0.0
+    for ntok in (1, 2, 3, 4):
+        y = gpu_qgemv(w.fmt, packed, w.n_out, w.n_in, x[:ntok])
+        worst = max(worst, check_close(y, ref[:ntok], den[:ntok], f"{name} ntok={ntok}"))
+    print(f"{name}: max normalised error {worst:.3g}")
+
+
+# ----------------------------------------------------------------------------- invariances
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_token_count_invariance_bitwise(fmt):
+    """Row t of an ntok=k call equals the ntok=1 call on x[t], bit for bit."""
+    n_out, n_in = 3001, n_in_for(fmt, 2560 if fmt != "affine4_g64" else 5120)
+    W = workloads.gaussian(5, (n_out, n_in), 0.02)
+    x = workloads.activations(5, n_in, 4)
+    packed = upload(fmt, ORC.quantize(fmt, W), n_out, n_in)
+    singles = [gpu_qgemv(fmt, packed, n_out, n_in, x[t:t + 1])[0] for t in range(4)]
+    for ntok in (2, 3, 4):
+        y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
+        for t in range(ntok):
+            assert np.array_equal(y[t].view(np.uint32), singles[t].view(np.uint32)), (fmt, ntok, t)
+    same = gpu_qgemv(fmt, packed, n_out, n_in, np.repeat(x[:1], 4, axis=0))
+    for t in range(4):
+        assert np.array_equal(same[t].view(np.uint32), singles[0].view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_tile_choice_does_not_change_bits(fmt):
+    """The reduction order depends only on (fmt, n_in): every geometry gives the same bits."""
+    n_out, n_in = 1537, n_in_for(fmt, 2560)
+    W = workloads.gaussian(8, (n_out, n_in), 0.02)
+    x = workloads.activations(8, n_in, 4)
+    packed = upload(fmt, ORC.quantize(fmt, W), n_out, n_in)
+    qg.qg_set_tile_override(None)
+    base = {ntok: gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok]) for ntok in (1, 3)}
+    try:
+        for spec in ["rpw=1,depth=2", "rpw=1,depth=4,warps=4", "rpw=2,depth=2,warps=2,ctas=1",
+                     "rpw=2,depth=4", "rpw=4,depth=2,warps=8,ctas=2", "rpw=4,depth=4,warps=1"]:
+            qg.qg_set_tile_override(spec)
+            for ntok in (1, 3):
+                y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
+                assert np.array_equal(y.view(np.uint32), base[ntok].view(np.uint32)), (fmt, spec, ntok)
+    finally:
+        qg.qg_set_tile_override(None)
+
+
+def test_deterministic_and_prefix_rows():
+    n_out, n_in = 4099, 2560
+    W = workloads.gaussian(9, (n_out, n_in), 0.02)
+    x = workloads.activations(9, n_in, 4)
+    packed = upload("q8_0", ORC.quantize("q8_0", W), n_out, n_in)
+    a = gpu_qgemv("q8_0", packed, n_out, n_in, x)
+    b = gpu_qgemv("q8_0", packed, n_out, n_in, x)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    # a row prefix of the packed matrix is the smaller matrix (drafted vocabulary)
+    c = gpu_qgemv("q8_0", packed, 1234, n_in, x)
+    assert np.array_equal(c.view(np.uint32), a[:, :1234].view(np.uint32))
+
+
+def test_largest_n_in_and_unsupported():
+    n_out = 64
+    for fmt in FMTS:
+        n_in = 12288
+        W = workloads.gaussian(10, (n_out, n_in), 0.02)
+        x = workloads.gaussian(11, (4, n_in))
+        canon = ORC.quantize(fmt, W)
+        y = gpu_qgemv(fmt, upload(fmt, canon, n_out, n_in), n_out, n_in, x)
+        check_close(y, ORC.gemv(fmt, canon, n_out, n_in, x), ORC.gemv_abs(fmt, canon, n_out, n_in, x), fmt)
+    # x for ntok=4 at n_in = 16384 does not fit in shared memory: refused, nothing launched
+    big = torch.zeros(qg.qg_packed_bytes("q8_0", 4, 16384), dtype=torch.uint8, device=dev())
+    xd = torch.zeros((4, 16384), dtype=torch.float32, device=dev())
+    yd = torch.zeros((4, 4), dtype=torch.float32, device=dev())
+    with pytest.raises(qg.QGError) as e:
+        qg.qgemv("q8_0", big, 4, 16384, xd, yd, 4)
+    assert e.value.status == -3
+
+
+def test_stream_argument():
+    n_out, n_in = 777, 2560
+    W = workloads.gaussian(12, (n_out, n_in), 0.02)
+    x = workloads.activations(12, n_in, 2)
+    canon = ORC.quantize("q8_0", W)
+    packed = upload("q8_0", canon, n_out, n_in)
+    s = torch.cuda.Stream()
+    xd = torch.from_numpy(x).to(dev())
+    y = torch.empty((2, n_out), dtype=torch.float32, device=dev())
+    torch.cuda.synchronize()
+    qg.qgemv("q8_0", packed, n_out, n_in, xd, y, 2, stream=s)
+    s.synchronize()
+    check_close(y.cpu().numpy(), ORC.gemv("q8_0", canon, n_out, n_in, x), ORC.gemv_abs("q8_0", canon, n_out, n_in, x))
