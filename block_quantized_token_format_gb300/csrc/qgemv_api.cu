@@ -132,7 +132,8 @@ qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argma
     if (smem + 1024 > size_t(optin)) return QG_EUNSUPPORTED;   // static smem of the argmax kernels fits in 1 KB
 
     Tile t = apply_override(select_tile(fmt, n_out, n_in, ntok), current_override());
-    if (!rpw_ok(t.rpw) || !depth_ok(t.depth) || t.warps < 1 || t.warps > 8 || t.ctas < 1) return QG_EINVAL;
+    if (!rpw_ok(t.rpw) || !depth_ok(t.depth) || t.warps < 1 || t.warps > 8 || t.ctas < 1 || t.pf < 0)
+        return QG_EINVAL;
     const void* fn = kernel_lookup(fmt, ntok, t.rpw, t.depth, argmax);
     if (!fn) return QG_EUNSUPPORTED;
     const int threads = 32 * t.warps;
@@ -207,6 +208,7 @@ qg_status qgemv(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, const fl
     a.stride = row_stride(fmt, n_in);
     a.n_out = int(n_out);
     a.n_in = int(n_in);
+    a.pf = p.tile.pf;
     return launch(p, a, stream);
 }
 
@@ -236,6 +238,7 @@ qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, c
     a.stride = row_stride(fmt, n_in);
     a.n_out = int(n_out);
     a.n_in = int(n_in);
+    a.pf = p.tile.pf;
     return launch(p, a, stream);
 }
 

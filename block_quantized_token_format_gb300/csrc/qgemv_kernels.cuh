@@ -18,7 +18,12 @@
 //    row-group boundaries so the loads never drain between groups.
 //  * Dequantization in registers without I2F: a code is placed in the
 //    mantissa of 2^23 (byte permute or mask) and the offset is removed with
-//    one exact FADD.  Block scales are applied once per 16-weight chunk.
+//    an exact packed FADD (two codes per add.rn.f32x2).  Block scales are
+//    applied once per 16-weight chunk.
+//  * FP32 math in packed pairs: per (row, token) two partial sums, even and
+//    odd columns, advanced by fma.rn.f32x2 (two columns per instruction) and
+//    added once per chunk.  On GB300 the packed FMA does not raise the FP32
+//    rate, but it halves the instructions issued for the multiply-adds.
 //    4-bit codes at nibble position 4m of a half-word come out as q*16^m; x is
 //    stored pre-multiplied by 16^-m (exact), so the products are q*x exactly.
 //  * The affine bias term b*sum(x) uses per-chunk sums of x computed once per
@@ -57,6 +62,7 @@ struct KernelArgs {
     long long stride;
     int n_out;
     int n_in;
+    int pf;                    // L2 bulk-prefetch distance in row groups of this warp (0 = off)
 };
 
 // ------------------------------------------------------------------------------ loads
@@ -86,6 +92,12 @@ __device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {
     return r;
 }
 
+// One bulk copy of [p, p + bytes) from HBM into L2 (no registers, no shared memory).
+// p and bytes must be multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const uint8_t* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ float h2f(uint32_t bits) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
 }
@@ -106,18 +118,19 @@ template <> struct Fmt<QG_Q8_0> {
         return r;
     }
     // bytes hold q + 128; 2^23 + (q + 128) - (2^23 + 128) = q, exact.
-    static __device__ __forceinline__ void dec(const Raw& r, int i, float (&f)[4]) {
+    static __device__ __forceinline__ void dec(const Raw& r, int i, float2& lo, float2& hi) {
         const uint32_t w = i == 0 ? r.q.x : i == 1 ? r.q.y : i == 2 ? r.q.z : r.q.w;
-        f[0] = __fadd_rn(__int_as_float(__byte_perm(w, 0x4B000000u, 0x7440)), -8388736.0f);
-        f[1] = __fadd_rn(__int_as_float(__byte_perm(w, 0x4B000000u, 0x7441)), -8388736.0f);
-        f[2] = __fadd_rn(__int_as_float(__byte_perm(w, 0x4B000000u, 0x7442)), -8388736.0f);
-        f[3] = __fadd_rn(__int_as_float(__byte_perm(w, 0x4B000000u, 0x7443)), -8388736.0f);
+        const float2 m = make_float2(-8388736.0f, -8388736.0f);
+        lo = __fadd2_rn(make_float2(__int_as_float(__byte_perm(w, 0x4B000000u, 0x7440)),
+                                    __int_as_float(__byte_perm(w, 0x4B000000u, 0x7441))), m);
+        hi = __fadd2_rn(make_float2(__int_as_float(__byte_perm(w, 0x4B000000u, 0x7442)),
+                                    __int_as_float(__byte_perm(w, 0x4B000000u, 0x7443))), m);
     }
 };
 
-// Nibble m (bits 4m..4m+3) of a half-word h, as the float 2^23 + q*16^m, minus `off`.
-__device__ __forceinline__ float nib(uint32_t h, uint32_t mask, float off) {
-    return __fadd_rn(__int_as_float((h & mask) | 0x4B000000u), off);
+// Nibble m (bits 4m..4m+3) of a half-word h as the float 2^23 + q*16^m.
+__device__ __forceinline__ float nib(uint32_t h, uint32_t mask) {
+    return __int_as_float((h & mask) | 0x4B000000u);
 }
 
 template <> struct Fmt<QG_Q4_0> {
@@ -130,13 +143,11 @@ template <> struct Fmt<QG_Q4_0> {
         return r;
     }
     // (2^23 + q*16^m) - (2^23 + 8*16^m) = (q - 8) * 16^m, exact.
-    static __device__ __forceinline__ void dec(const Raw& r, int i, float (&f)[4]) {
+    static __device__ __forceinline__ void dec(const Raw& r, int i, float2& lo, float2& hi) {
         const uint32_t w = (i >> 1) ? r.q.y : r.q.x;
         const uint32_t h = (i & 1) ? (w >> 16) : w;
-        f[0] = nib(h, 0x000Fu, -8388616.0f);
-        f[1] = nib(h, 0x00F0u, -8388736.0f);
-        f[2] = nib(h, 0x0F00u, -8390656.0f);
-        f[3] = nib(h, 0xF000u, -8421376.0f);
+        lo = __fadd2_rn(make_float2(nib(h, 0x000Fu), nib(h, 0x00F0u)), make_float2(-8388616.0f, -8388736.0f));
+        hi = __fadd2_rn(make_float2(nib(h, 0x0F00u), nib(h, 0xF000u)), make_float2(-8390656.0f, -8421376.0f));
     }
 };
 
@@ -150,13 +161,12 @@ template <> struct Fmt<QG_AFFINE4_G64> {
         return r;
     }
     // (2^23 + q*16^m) - 2^23 = q * 16^m, exact.
-    static __device__ __forceinline__ void dec(const Raw& r, int i, float (&f)[4]) {
+    static __device__ __forceinline__ void dec(const Raw& r, int i, float2& lo, float2& hi) {
         const uint32_t w = (i >> 1) ? r.q.y : r.q.x;
         const uint32_t h = (i & 1) ? (w >> 16) : w;
-        f[0] = nib(h, 0x000Fu, -8388608.0f);
-        f[1] = nib(h, 0x00F0u, -8388608.0f);
-        f[2] = nib(h, 0x0F00u, -8388608.0f);
-        f[3] = nib(h, 0xF000u, -8388608.0f);
+        const float2 m = make_float2(-8388608.0f, -8388608.0f);
+        lo = __fadd2_rn(make_float2(nib(h, 0x000Fu), nib(h, 0x00F0u)), m);
+        hi = __fadd2_rn(make_float2(nib(h, 0x0F00u), nib(h, 0xF000u)), m);
     }
 };
 
@@ -169,13 +179,11 @@ template <> struct Fmt<QG_BF16> {
         r.b = ld_stream16(row + 32 * c + 16);
         return r;
     }
-    static __device__ __forceinline__ void dec(const Raw& r, int i, float (&f)[4]) {
+    static __device__ __forceinline__ void dec(const Raw& r, int i, float2& lo, float2& hi) {
         const uint32_t w0 = i == 0 ? r.a.x : i == 1 ? r.a.z : i == 2 ? r.b.x : r.b.z;
         const uint32_t w1 = i == 0 ? r.a.y : i == 1 ? r.a.w : i == 2 ? r.b.y : r.b.w;
-        f[0] = __int_as_float(w0 << 16);
-        f[1] = __int_as_float(w0 & 0xFFFF0000u);
-        f[2] = __int_as_float(w1 << 16);
-        f[3] = __int_as_float(w1 & 0xFFFF0000u);
+        lo = make_float2(__int_as_float(w0 << 16), __int_as_float(w0 & 0xFFFF0000u));
+        hi = make_float2(__int_as_float(w1 << 16), __int_as_float(w1 & 0xFFFF0000u));
     }
 };
 
@@ -231,6 +239,15 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
             lrow[r] = a.W + row * a.stride;
         }
     };
+    // Rows of group g lie in [g*RPW, g*RPW + RPW) and are contiguous in memory, so one
+    // bulk prefetch brings the whole group into L2 ahead of the register loads.
+    auto prefetch_group = [&](int g) {
+        if (lane == 0 && g < ngroups) {
+            const long long r0 = (long long)g * RPW;
+            const long long r1 = r0 + RPW < a.n_out ? r0 + RPW : a.n_out;
+            prefetch_l2(a.W + r0 * a.stride, uint32_t((r1 - r0) * a.stride));
+        }
+    };
     auto load_step = [&](Raw (&b)[RPW]) {
         if (gl < ngroups) {
             const int c = lane + 32 * kl;
@@ -243,10 +260,12 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
             kl = 0;
             gl += GW;
             set_load_rows(gl);
+            if (a.pf > 0) prefetch_group(gl + a.pf * GW);
         }
     };
 
     set_load_rows(gl);
+    for (int j = 0; j <= a.pf && a.pf > 0; ++j) prefetch_group(gw + j * GW);
 #pragma unroll
     for (int u = 0; u < DEPTH; ++u) load_step(buf[u]);
 
@@ -284,11 +303,21 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
     float best_v = -INFINITY;
     int best_i = 0x7FFFFFFF;
 
+    // Per (row, token): within a chunk, a pair of fp32 partial sums (even and odd
+    // columns) advanced with packed fma.rn.f32x2, two columns per instruction; the
+    // pair is added and scaled once per chunk into one fp32 accumulator.  BF16 has
+    // no scale and keeps the pair across the whole row.
+    constexpr bool kPairAcc = (FMT == QG_BF16);
     float acc[RPW][NTOK];
+    float2 acc2[kPairAcc ? RPW : 1][kPairAcc ? NTOK : 1];
 #pragma unroll
     for (int r = 0; r < RPW; ++r)
 #pragma unroll
         for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.f;
+#pragma unroll
+    for (int r = 0; r < (kPairAcc ? RPW : 1); ++r)
+#pragma unroll
+        for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = make_float2(0.f, 0.f);
 
     int gc = gw, kc = 0;
     while (gc < ngroups) {
@@ -299,11 +328,11 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
                 if (c < nchunks) {
                     // ---- one 16-weight chunk of RPW rows against NTOK tokens
                     const float4* xr = xs + 4 * c;
-                    float p[RPW][NTOK];
+                    float2 p[kPairAcc ? 1 : RPW][kPairAcc ? 1 : NTOK];
 #pragma unroll
-                    for (int r = 0; r < RPW; ++r)
+                    for (int r = 0; r < (kPairAcc ? 1 : RPW); ++r)
 #pragma unroll
-                        for (int t = 0; t < NTOK; ++t) p[r][t] = 0.f;
+                        for (int t = 0; t < (kPairAcc ? 1 : NTOK); ++t) p[r][t] = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         float4 xv[NTOK];
@@ -311,17 +340,15 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
                         for (int t = 0; t < NTOK; ++t) xv[t] = xr[t * n4 + (i ^ sw)];
 #pragma unroll
                         for (int r = 0; r < RPW; ++r) {
-                            float f[4];
-                            F::dec(buf[u][r], i, f);
+                            float2 wlo, whi;
+                            F::dec(buf[u][r], i, wlo, whi);
 #pragma unroll
                             for (int t = 0; t < NTOK; ++t) {
-                                float& pp = [&]() -> float& {
-                                    if constexpr (FMT == QG_BF16) return acc[r][t]; else return p[r][t];
+                                float2& pp = [&]() -> float2& {
+                                    if constexpr (kPairAcc) return acc2[r][t]; else return p[r][t];
                                 }();
-                                pp = __fmaf_rn(f[0], xv[t].x, pp);
-                                pp = __fmaf_rn(f[1], xv[t].y, pp);
-                                pp = __fmaf_rn(f[2], xv[t].z, pp);
-                                pp = __fmaf_rn(f[3], xv[t].w, pp);
+                                pp = __ffma2_rn(wlo, make_float2(xv[t].x, xv[t].y), pp);
+                                pp = __ffma2_rn(whi, make_float2(xv[t].z, xv[t].w), pp);
                             }
                         }
                     }
@@ -330,7 +357,8 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
                         for (int r = 0; r < RPW; ++r) {
                             const float d = h2f(buf[u][r].d);
 #pragma unroll
-                            for (int t = 0; t < NTOK; ++t) acc[r][t] = __fmaf_rn(d, p[r][t], acc[r][t]);
+                            for (int t = 0; t < NTOK; ++t)
+                                acc[r][t] = __fmaf_rn(d, __fadd_rn(p[r][t].x, p[r][t].y), acc[r][t]);
                         }
                     } else if constexpr (FMT == QG_AFFINE4_G64) {
                         float csv[NTOK];
@@ -339,10 +367,10 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
 #pragma unroll
                         for (int r = 0; r < RPW; ++r) {
                             const uint32_t sb = buf[u][r].sb;
-                            const float s = h2f(sb & 0xFFFFu), b = h2f(sb >> 16);
+                            const float sc = h2f(sb & 0xFFFFu), b = h2f(sb >> 16);
 #pragma unroll
                             for (int t = 0; t < NTOK; ++t)
-                                acc[r][t] = __fmaf_rn(s, p[r][t], __fmaf_rn(b, csv[t], acc[r][t]));
+                                acc[r][t] = __fmaf_rn(sc, __fadd_rn(p[r][t].x, p[r][t].y), __fmaf_rn(b, csv[t], acc[r][t]));
                         }
                     }
                 }
@@ -351,7 +379,12 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
                     // ---- finish the row group: transposed warp reduction
                     float v[VP];
 #pragma unroll
-                    for (int j = 0; j < VP; ++j) v[j] = j < V ? acc[j / NTOK][j % NTOK] : 0.f;
+                    for (int j = 0; j < VP; ++j) {
+                        if constexpr (kPairAcc)
+                            v[j] = j < V ? __fadd_rn(acc2[j / NTOK][j % NTOK].x, acc2[j / NTOK][j % NTOK].y) : 0.f;
+                        else
+                            v[j] = j < V ? acc[j / NTOK][j % NTOK] : 0.f;
+                    }
 #pragma unroll
                     for (int s = 0; s < LG; ++s) {
                         const int h = VP >> (s + 1);
@@ -379,6 +412,10 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
                     for (int r = 0; r < RPW; ++r)
 #pragma unroll
                         for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.f;
+#pragma unroll
+                    for (int r = 0; r < (kPairAcc ? RPW : 1); ++r)
+#pragma unroll
+                        for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = make_float2(0.f, 0.f);
                     kc = 0;
                     gc += GW;
                 }

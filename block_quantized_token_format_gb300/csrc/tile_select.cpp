@@ -77,6 +77,7 @@ Tile apply_override(Tile t, const TileOverride& o) {
     if (o.depth > 0) t.depth = o.depth;
     if (o.warps > 0) t.warps = o.warps;
     if (o.ctas > 0) t.ctas = o.ctas;
+    if (o.pf >= 0) t.pf = o.pf;
     return t;
 }
 
@@ -101,6 +102,7 @@ bool parse_tile_spec(const char* spec, TileOverride* out) {
         else if (key == "depth") { if (!depth_ok(v)) return false; o.depth = v; }
         else if (key == "warps") { if (v < 1 || v > 8) return false; o.warps = v; }
         else if (key == "ctas") { if (v < 1 || v > 8) return false; o.ctas = v; }
+        else if (key == "pf") { if (v < 0 || v > 16) return false; o.pf = v; }
         else return false;
     }
     *out = o;
@@ -109,7 +111,7 @@ bool parse_tile_spec(const char* spec, TileOverride* out) {
 
 std::string tile_to_string(const Tile& t) {
     char b[96];
-    std::snprintf(b, sizeof b, "rpw=%d,depth=%d,warps=%d,ctas=%d", t.rpw, t.depth, t.warps, t.ctas);
+    std::snprintf(b, sizeof b, "rpw=%d,depth=%d,warps=%d,ctas=%d,pf=%d", t.rpw, t.depth, t.warps, t.ctas, t.pf);
     return b;
 }
 

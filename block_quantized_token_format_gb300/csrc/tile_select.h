@@ -14,12 +14,13 @@ struct Tile {
     int depth = 4;
     int warps = 8;
     int ctas = 2;
+    int pf = 0;      // L2 bulk-prefetch distance, in row groups of the same warp (0 = off)
 };
 
 // Fields left at -1 are not overridden.
 struct TileOverride {
-    int rpw = -1, depth = -1, warps = -1, ctas = -1;
-    bool any() const { return rpw > 0 || depth > 0 || warps > 0 || ctas > 0; }
+    int rpw = -1, depth = -1, warps = -1, ctas = -1, pf = -1;
+    bool any() const { return rpw > 0 || depth > 0 || warps > 0 || ctas > 0 || pf >= 0; }
 };
 
 // The geometry for a call, before the override and the occupancy cap.

@@ -143,8 +143,9 @@ qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
  * the prior art).  The reduction order never depends on this choice.
  *
  * qg_set_tile_override: force a geometry for later calls, e.g.
- * "rpw=4,depth=2,warps=8,ctas=2" (any subset of the keys; rpw in {1,2,4},
- * depth in {2,4}, warps in {1..8}, ctas in {1..8}).  NULL or "" clears it.
+ * "rpw=4,depth=2,warps=8,ctas=2,pf=2" (any subset of the keys; rpw in {1,2,4},
+ * depth in {2,4}, warps in {1..8}, ctas in {1..8}, pf (L2 prefetch distance in
+ * row groups, 0 = off) in {0..16}).  NULL or "" clears it.
  * The environment variable QGEMV_TILE, read at the first call, sets the same
  * override.  Returns QG_EINVAL on a malformed spec (the override is unchanged).
  *

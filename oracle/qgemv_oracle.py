@@ -308,6 +308,8 @@ def argmax_first(y: np.ndarray) -> np.ndarray:
 def top2_gap(y: np.ndarray) -> np.ndarray:
     """Per token, largest minus second-largest logit (absolute, logit units)."""
     y = np.atleast_2d(np.asarray(y, dtype=np.float64))
+    if y.shape[1] < 2:
+        return np.full(y.shape[0], np.inf)          # a single output: no runner-up
     part = -np.partition(-y, 1, axis=1)[:, :2]
     return part[:, 0] - part[:, 1]
 

@@ -310,6 +310,7 @@ def check_argmax(orc):
     assert am[0] == 9
     assert orc.argmax_first(np.array([[1.0, np.nan, 3.0, 3.0]]))[0] == 2
     assert orc.top2_gap(np.array([[1.0, 5.0, 4.5]]))[0] == 0.5
+    assert orc.top2_gap(np.array([[2.0], [3.0]]))[1] == np.inf
 
 
 def check_quant_error_band(orc):
