@@ -19,7 +19,8 @@ __all__ = [
     "QG_Q8_0", "QG_Q4_0", "QG_AFFINE4_G64", "QG_BF16", "FORMATS", "QGError", "load_library",
     "qg_strerror", "qg_abi_version", "qg_canonical_bytes", "qg_packed_bytes", "qg_row_stride",
     "qg_quantize", "qg_to_device_layout", "qg_pack", "qgemv", "qgemv_argmax_workspace_bytes",
-    "qgemv_argmax", "qg_set_tile_override", "qg_describe_tile", "weight_bytes",
+    "qgemv_argmax", "qg_set_tile_override", "qg_describe_tile", "weight_bytes", "qg_device_status",
+    "qg_set_wait_limit", "QG_DEVICE_WAIT_TIMEOUT",
 ]
 
 QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
@@ -69,6 +70,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "qgemv_argmax": (i32, [i32, vp, i64, i64, vp, vp, vp, i32, vp, sz, vp]),
         "qg_set_tile_override": (i32, [ctypes.c_char_p]),
         "qg_describe_tile": (i32, [i32, i64, i64, i32, ctypes.c_char_p, sz]),
+        "qg_device_status": (i32, [i32, ctypes.POINTER(ctypes.c_uint)]),
+        "qg_set_wait_limit": (i32, [ctypes.c_uint, ctypes.c_uint]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -197,6 +200,21 @@ def qgemv_argmax(fmt, W, n_out: int, n_in: int, x, y, argmax, workspace, ntok: i
 
 def qg_set_tile_override(spec: str | None) -> None:
     _check(load_library().qg_set_tile_override(spec.encode() if spec else None), "qg_set_tile_override")
+
+
+def qg_device_status(clear: bool = True) -> int:
+    """The current device's status word (QG_DEVICE_WAIT_TIMEOUT = 1 if a bounded wait gave up)."""
+    v = ctypes.c_uint(0)
+    _check(load_library().qg_device_status(1 if clear else 0, ctypes.byref(v)), "qg_device_status")
+    return v.value
+
+
+def qg_set_wait_limit(polls: int = 0, extra_tx_bytes: int = 0) -> None:
+    """Test hook: mbarrier polls before a wait gives up (0 = default) and extra expected bytes."""
+    _check(load_library().qg_set_wait_limit(int(polls), int(extra_tx_bytes)), "qg_set_wait_limit")
+
+
+QG_DEVICE_WAIT_TIMEOUT = 1
 
 
 def qg_describe_tile(fmt, n_out: int, n_in: int, ntok: int) -> str:

@@ -62,9 +62,7 @@ uint16_t f32_to_bf16(float f) {
 }
 
 inline void put16(uint8_t* p, uint16_t v) { p[0] = uint8_t(v); p[1] = uint8_t(v >> 8); }
-inline uint16_t get16(const uint8_t* p) { return uint16_t(p[0] | (p[1] << 8)); }
 inline void put32(uint8_t* p, uint32_t v) { for (int i = 0; i < 4; ++i) p[i] = uint8_t(v >> (8 * i)); }
-inline uint32_t get32(const uint8_t* p) { return uint32_t(p[0]) | uint32_t(p[1]) << 8 | uint32_t(p[2]) << 16 | uint32_t(p[3]) << 24; }
 
 // ------------------------------------------------------------------ one row, fp32 -> canonical
 
@@ -134,8 +132,8 @@ void quant_row_bf16(const float* w, int64_t n_in, uint8_t* out) {
 // Canonical row pointers (affine has three planes).
 struct CanonRow { const uint8_t* a; const uint8_t* s; const uint8_t* b; };
 
-void device_row(int fmt, CanonRow c, int64_t n_in, uint8_t* dst, int64_t stride) {
-    std::memset(dst, 0, size_t(stride));
+// The row's codes (device byte / nibble order) followed by all its scales.
+void flat_device_row(int fmt, CanonRow c, int64_t n_in, uint8_t* dst) {
     const int64_t cb = qg::codes_bytes(fmt, n_in);
     switch (fmt) {
         case QG_Q8_0:
@@ -168,6 +166,23 @@ void device_row(int fmt, CanonRow c, int64_t n_in, uint8_t* dst, int64_t stride)
         case QG_BF16:
             std::memcpy(dst, c.a, size_t(cb));
             break;
+    }
+}
+
+// Scatter a flat [codes][scales] row into its steps of [512 B codes][their scales][pad].
+void device_row(int fmt, CanonRow c, int64_t n_in, uint8_t* dst, int64_t stride) {
+    thread_local std::vector<uint8_t> flat;
+    const int64_t cb = qg::codes_bytes(fmt, n_in);
+    flat.assign(size_t(qg::canonical_row_bytes(fmt, n_in)), 0);
+    flat_device_row(fmt, c, n_in, flat.data());
+    std::memset(dst, 0, size_t(stride));
+    const int64_t full = qg::full_step_bytes(fmt);
+    for (int64_t k = 0; k < qg::steps_per_row(fmt, n_in); ++k) {
+        const int64_t c0 = qg::kStepCodeBytes * k;
+        const int64_t ck = std::min(qg::kStepCodeBytes, cb - c0);
+        std::memcpy(dst + k * full, flat.data() + c0, size_t(ck));
+        std::memcpy(dst + k * full + ck, flat.data() + cb + qg::scale_bytes_for(fmt, c0),
+                    size_t(qg::scale_bytes_for(fmt, ck)));
     }
 }
 

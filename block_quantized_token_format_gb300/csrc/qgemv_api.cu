@@ -13,20 +13,24 @@
 
 namespace qg {
 
-const void* kernel_lookup_fmt0(int, int, int, bool);
-const void* kernel_lookup_fmt1(int, int, int, bool);
-const void* kernel_lookup_fmt2(int, int, int, bool);
-const void* kernel_lookup_fmt3(int, int, int, bool);
+const void* kernel_lookup_fmt0(int, int, bool);
+const void* kernel_lookup_fmt1(int, int, bool);
+const void* kernel_lookup_fmt2(int, int, bool);
+const void* kernel_lookup_fmt3(int, int, bool);
 
-const void* kernel_lookup(int fmt, int ntok, int rpw, int depth, bool argmax) {
+const void* kernel_lookup(int fmt, int ntok, int rpw, bool argmax) {
     switch (fmt) {
-        case 0: return kernel_lookup_fmt0(ntok, rpw, depth, argmax);
-        case 1: return kernel_lookup_fmt1(ntok, rpw, depth, argmax);
-        case 2: return kernel_lookup_fmt2(ntok, rpw, depth, argmax);
-        case 3: return kernel_lookup_fmt3(ntok, rpw, depth, argmax);
+        case 0: return kernel_lookup_fmt0(ntok, rpw, argmax);
+        case 1: return kernel_lookup_fmt1(ntok, rpw, argmax);
+        case 2: return kernel_lookup_fmt2(ntok, rpw, argmax);
+        case 3: return kernel_lookup_fmt3(ntok, rpw, argmax);
         default: return nullptr;
     }
 }
+
+// Device status word: kernels OR bits into it (kStatusWaitTimeout when a bounded
+// mbarrier wait gave up); read and cleared by qg_device_status.
+__device__ unsigned int g_device_status;
 
 namespace {
 
@@ -36,8 +40,13 @@ constexpr int kMaxDevices = 64;
 struct DevInfo {
     std::atomic<int> sms{0};
     std::atomic<int> smem_optin{0};
+    std::atomic<unsigned int*> status{nullptr};
 };
 DevInfo g_dev[kMaxDevices];
+
+// Test hook values (qg_set_wait_limit).
+std::atomic<uint32_t> g_wait_limit{kWaitLimit};
+std::atomic<uint32_t> g_test_extra_tx{0};
 
 // Tile override: QGEMV_TILE at first use, or qg_set_tile_override.
 std::mutex g_override_mu;
@@ -67,23 +76,29 @@ std::mutex g_occ_mu;
 std::map<std::tuple<const void*, int, size_t, int>, int> g_occ;
 std::map<std::pair<const void*, int>, bool> g_configured;
 
-qg_status device_info(int* dev, int* sms, int* smem_optin) {
+qg_status device_info(int* dev, int* sms, int* smem_optin, unsigned int** status) {
     if (cudaGetDevice(dev) != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
     if (*dev < 0 || *dev >= kMaxDevices) return QG_EUNSUPPORTED;
     DevInfo& d = g_dev[*dev];
-    int s = d.sms.load(std::memory_order_relaxed);
-    int m = d.smem_optin.load(std::memory_order_relaxed);
-    if (s == 0 || m == 0) {
+    int s = d.sms.load(std::memory_order_acquire);
+    int m = d.smem_optin.load(std::memory_order_acquire);
+    unsigned int* st = d.status.load(std::memory_order_acquire);
+    if (s == 0 || m == 0 || st == nullptr) {
+        void* addr = nullptr;
         if (cudaDeviceGetAttribute(&s, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&m, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev) != cudaSuccess) {
+            cudaDeviceGetAttribute(&m, cudaDevAttrMaxSharedMemoryPerBlockOptin, *dev) != cudaSuccess ||
+            cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) {
             cudaGetLastError();
             return QG_ECUDA;
         }
-        d.sms.store(s, std::memory_order_relaxed);
-        d.smem_optin.store(m, std::memory_order_relaxed);
+        st = static_cast<unsigned int*>(addr);
+        d.sms.store(s, std::memory_order_release);
+        d.smem_optin.store(m, std::memory_order_release);
+        d.status.store(st, std::memory_order_release);
     }
     *sms = s;
     *smem_optin = m;
+    if (status) *status = st;
     return QG_OK;
 }
 
@@ -121,20 +136,29 @@ struct Plan {
     int grid = 0;
     int threads = 0;
     size_t smem = 0;
+    unsigned int* status = nullptr;
 };
+
+constexpr size_t kStaticSmemReserve = 1024;   // the argmax kernels' static shared memory
 
 // Everything up to the launch.  Checks that need no CUDA call come first.
 qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argmax, Plan* plan) {
     int dev = 0, sms = 0, optin = 0;
-    qg_status st = device_info(&dev, &sms, &optin);
+    unsigned int* status = nullptr;
+    qg_status st = device_info(&dev, &sms, &optin, &status);
     if (st != QG_OK) return st;
-    const size_t smem = smem_bytes(fmt, ntok, int(n_in));
-    if (smem + 1024 > size_t(optin)) return QG_EUNSUPPORTED;   // static smem of the argmax kernels fits in 1 KB
-
     Tile t = apply_override(select_tile(fmt, n_out, n_in, ntok), current_override());
-    if (!rpw_ok(t.rpw) || !depth_ok(t.depth) || t.warps < 1 || t.warps > 8 || t.ctas < 1 || t.pf < 0)
+    if (!rpw_ok(t.rpw) || !depth_ok(t.depth) || t.warps < 1 || t.warps > kMaxWarps || t.ctas < 1)
         return QG_EINVAL;
-    const void* fn = kernel_lookup(fmt, ntok, t.rpw, t.depth, argmax);
+    // Shrink the ring until the CTA fits in shared memory; x alone must fit.
+    auto total = [&](int depth, int warps) {
+        return size_t(smem_plan(fmt, ntok, int(n_in), t.rpw, depth, warps).total);
+    };
+    while (total(t.depth, t.warps) + kStaticSmemReserve > size_t(optin) && t.depth > 2) --t.depth;
+    while (total(t.depth, t.warps) + kStaticSmemReserve > size_t(optin) && t.warps > 1) --t.warps;
+    const size_t smem = total(t.depth, t.warps);
+    if (smem + kStaticSmemReserve > size_t(optin)) return QG_EUNSUPPORTED;
+    const void* fn = kernel_lookup(fmt, ntok, t.rpw, argmax);
     if (!fn) return QG_EUNSUPPORTED;
     const int threads = 32 * t.warps;
     const int occ = blocks_per_sm(fn, dev, optin, threads, smem);
@@ -151,7 +175,24 @@ qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argma
     plan->grid = int(grid);
     plan->threads = threads;
     plan->smem = smem;
+    plan->status = status;
     return QG_OK;
+}
+
+void fill_common(KernelArgs& a, const Plan& p, int fmt, const void* W, int64_t n_out, int64_t n_in,
+                 const float* x, float* y) {
+    a.W = static_cast<const uint8_t*>(W);
+    a.x = x;
+    a.y = y;
+    a.status = p.status;
+    a.stride = row_stride(fmt, n_in);
+    a.n_out = int(n_out);
+    a.n_in = int(n_in);
+    a.depth = p.tile.depth;
+    a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+    a.drain_limit = std::max<uint32_t>(a.wait_limit, 1u << 16);
+    a.test_extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
+    a.fmagic = 0x4B000000u;
 }
 
 qg_status check_common(int fmt, const void* W, int64_t n_out, int64_t n_in, const float* x, int ntok) {
@@ -202,13 +243,7 @@ qg_status qgemv(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, const fl
     st = plan_launch(fmt, n_out, n_in, ntok, false, &p);
     if (st != QG_OK) return st;
     KernelArgs a{};
-    a.W = static_cast<const uint8_t*>(W);
-    a.x = x;
-    a.y = y;
-    a.stride = row_stride(fmt, n_in);
-    a.n_out = int(n_out);
-    a.n_in = int(n_in);
-    a.pf = p.tile.pf;
+    fill_common(a, p, fmt, W, n_out, n_in, x, y);
     return launch(p, a, stream);
 }
 
@@ -229,16 +264,10 @@ qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, c
     st = plan_launch(fmt, n_out, n_in, ntok, true, &p);
     if (st != QG_OK) return st;
     KernelArgs a{};
-    a.W = static_cast<const uint8_t*>(W);
-    a.x = x;
-    a.y = y;
+    fill_common(a, p, fmt, W, n_out, n_in, x, y);
     a.argmax = argmax;
     a.ticket = static_cast<unsigned int*>(workspace);
     a.partials = reinterpret_cast<ArgmaxPartial*>(static_cast<uint8_t*>(workspace) + 16);
-    a.stride = row_stride(fmt, n_in);
-    a.n_out = int(n_out);
-    a.n_in = int(n_in);
-    a.pf = p.tile.pf;
     return launch(p, a, stream);
 }
 
@@ -248,6 +277,31 @@ qg_status qg_set_tile_override(const char* spec) {
     if (!parse_tile_spec(spec, &o)) return QG_EINVAL;
     std::lock_guard<std::mutex> lk(g_override_mu);
     g_override = o;
+    return QG_OK;
+}
+
+qg_status qg_device_status(int clear, unsigned int* status) {
+    if (!status) return QG_EINVAL;
+    int dev = 0, sms = 0, optin = 0;
+    unsigned int* addr = nullptr;
+    qg_status st = device_info(&dev, &sms, &optin, &addr);
+    if (st != QG_OK) return st;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, addr, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
+    if (clear && v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(addr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaGetLastError();
+            return QG_ECUDA;
+        }
+    }
+    *status = v;
+    return QG_OK;
+}
+
+qg_status qg_set_wait_limit(uint32_t polls, uint32_t extra_tx_bytes) {
+    g_wait_limit.store(polls == 0 ? kWaitLimit : polls, std::memory_order_relaxed);
+    g_test_extra_tx.store(extra_tx_bytes, std::memory_order_relaxed);
     return QG_OK;
 }
 

@@ -12,12 +12,12 @@
 
 namespace qg {
 
-const void* QG_CAT(kernel_lookup_fmt, QG_INST_FMT)(int ntok, int rpw, int depth, bool argmax) {
-#define QG_E(NT, R, D)                                                                   \
-    if (ntok == NT && rpw == R && depth == D)                                            \
-        return argmax ? (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, D, true>          \
-                      : (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, D, false>;
-#define QG_E_NT(NT) QG_E(NT, 1, 2) QG_E(NT, 1, 4) QG_E(NT, 2, 2) QG_E(NT, 2, 4) QG_E(NT, 4, 2) QG_E(NT, 4, 4)
+const void* QG_CAT(kernel_lookup_fmt, QG_INST_FMT)(int ntok, int rpw, bool argmax) {
+#define QG_E(NT, R)                                                                      \
+    if (ntok == NT && rpw == R)                                                          \
+        return argmax ? (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, true>             \
+                      : (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, false>;
+#define QG_E_NT(NT) QG_E(NT, 1) QG_E(NT, 2) QG_E(NT, 4)
     QG_E_NT(1) QG_E_NT(2) QG_E_NT(3) QG_E_NT(4)
 #undef QG_E_NT
 #undef QG_E

@@ -8,35 +8,38 @@
 // pages were made for Apple GPUs; this is a GB300 design:
 //
 //  * Persistent grid (a few CTAs per SM).  Each CTA stages x once, in fp32,
-//    in shared memory with an XOR swizzle that makes the per-lane 16-column
-//    reads conflict-free, so x never costs HBM traffic after the first read.
-//  * Every row is streamed exactly once with 16-byte (8-bit, BF16) or 8-byte
-//    (4-bit) non-allocating loads; a lane owns 16-weight chunks lane, lane+32,
-//    ... of the row.  A warp walks RPW rows at once (x is read from shared
-//    memory once per chunk and reused for the RPW rows) and keeps DEPTH chunk
-//    sets in flight in registers, in one flat pipeline that runs across
-//    row-group boundaries so the loads never drain between groups.
+//    in shared memory with an XOR swizzle that makes the lanes' reads
+//    conflict-free, so x never costs HBM traffic after the first read.
+//  * Weights move HBM -> shared memory by TMA bulk copies
+//    (cp.async.bulk, completion counted on an mbarrier), never through
+//    registers: each warp owns a ring of `depth` stages, a stage holds one
+//    512-byte code step (plus its scales) of each of the warp's RPW rows, so
+//    the bytes in flight per SM are set by shared memory, not by registers.
+//    Every weight byte is copied exactly once.  One flat pipeline runs across
+//    row-group boundaries, so the copies never drain between groups.
 //  * Dequantization in registers without I2F: a code is placed in the
-//    mantissa of 2^23 (byte permute or mask) and the offset is removed with
-//    an exact packed FADD (two codes per add.rn.f32x2).  Block scales are
-//    applied once per 16-weight chunk.
-//  * FP32 math in packed pairs: per (row, token) two partial sums, even and
-//    odd columns, advanced by fma.rn.f32x2 (two columns per instruction) and
-//    added once per chunk.  On GB300 the packed FMA does not raise the FP32
-//    rate, but it halves the instructions issued for the multiply-adds.
-//    4-bit codes at nibble position 4m of a half-word come out as q*16^m; x is
-//    stored pre-multiplied by 16^-m (exact), so the products are q*x exactly.
+//    mantissa of 2^23 (byte permute or mask) and the offset is removed with an
+//    exact packed FADD (add.rn.f32x2).  4-bit codes at nibble position 4m of a
+//    half-word come out as q*16^m; x is stored pre-multiplied by 16^-m (exact),
+//    so the products are q*x exactly.  Block scales are applied once per chunk.
+//  * FP32 math in packed pairs: per (row, token) a pair of partial sums (even
+//    and odd columns) advanced by fma.rn.f32x2, added and scaled once per
+//    chunk.  On GB300 the packed FMA does not raise the FP32 rate, but it
+//    halves the instructions issued for the multiply-adds.
 //  * The affine bias term b*sum(x) uses per-chunk sums of x computed once per
 //    CTA; the per-chunk fp32 order is fixed.
 //  * Reduction: per lane, chunks in increasing order; across the warp, a
 //    transposed butterfly (reduce-scatter by halving, then xor steps).  The
-//    order depends only on (fmt, n_in), never on ntok, RPW or the grid, so a
-//    token's outputs are bitwise identical for every ntok (the opus-mtp-turbo
+//    order depends only on (fmt, n_in), never on ntok, the tile or the grid, so
+//    a token's outputs are bitwise identical for every ntok (the opus-mtp-turbo
 //    Track 1 report, item 3, relies on exactly this property).
 //  * The fused argmax (perf(speculative): cut the MTP drafter's per-step
 //    cost, Phase 2 item 2a) keeps a running (max, lowest index) per lane,
 //    reduces it per CTA into the workspace, and the last CTA to take a ticket
-//    reduces the partials.  Nothing ever waits on another CTA.
+//    reduces the partials.  No CTA ever waits on another CTA.
+//  * Every mbarrier wait is bounded: after `wait_limit` polls it sets bit 0 of
+//    the device status word, stops issuing copies, drains (again bounded) the
+//    copies it already issued, and the kernel runs to its normal exit.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -48,7 +51,10 @@
 namespace qg {
 
 constexpr int kMaxGrid = 4096;            // upper bound on CTAs of any launch (workspace sizing)
+constexpr int kMaxWarps = 16;             // warps per CTA (launch bound 512 threads)
 constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr uint32_t kWaitLimit = 1u << 22; // mbarrier polls before a wait is declared failed
+constexpr unsigned kStatusWaitTimeout = 1u;
 
 struct ArgmaxPartial { float v; int i; };
 
@@ -59,138 +65,192 @@ struct KernelArgs {
     int* argmax;               // [ntok] (argmax kernels)
     ArgmaxPartial* partials;   // [gridDim.x][ntok] (argmax kernels)
     unsigned int* ticket;      // zero on entry, left zero on exit (argmax kernels)
+    unsigned int* status;      // device status word (bit 0: a bounded wait gave up)
     long long stride;
     int n_out;
     int n_in;
-    int pf;                    // L2 bulk-prefetch distance in row groups of this warp (0 = off)
+    int depth;                 // ring stages per warp
+    uint32_t wait_limit;       // polls per mbarrier wait before giving up
+    uint32_t drain_limit;      // polls per wait while draining after giving up
+    uint32_t test_extra_tx;    // test hook: bytes added to the first expected transaction of
+                               // every warp, so that wait can never complete (0 = off)
+    uint32_t fmagic;           // 0x4B000000, the bits of 2^23; passed in so that the nibble
+                               // extraction (h & mask) | magic is one LOP3 with the mask as
+                               // its only immediate
 };
 
-// ------------------------------------------------------------------------------ loads
+// ------------------------------------------------------------------------------ PTX helpers
 
-__device__ __forceinline__ uint4 ld_stream16(const uint8_t* p) {
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false if the phase did not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Bulk copy global -> this CTA's shared memory, completion counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
     return r;
 }
-
-__device__ __forceinline__ uint2 ld_stream8(const uint8_t* p) {
-    uint2 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) {
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
     unsigned short r;
-    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(a));
     return r;
 }
-
-__device__ __forceinline__ uint32_t ld_u32(const uint8_t* p) {
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
     uint32_t r;
-    asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(a));
     return r;
-}
-
-// One bulk copy of [p, p + bytes) from HBM into L2 (no registers, no shared memory).
-// p and bytes must be multiples of 16.
-__device__ __forceinline__ void prefetch_l2(const uint8_t* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ float h2f(uint32_t bits) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
 }
 
+// Nibble m (bits 4m..4m+3) of a half-word h, as the bits of the float 2^23 + q*16^m
+// (magic = 0x4B000000, held in a register).
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t nib(uint32_t h, uint32_t magic) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(h), "n"(MASK), "r"(magic));
+    return d;
+}
+
+// A pair of fp32 values in one 64-bit register pair, as the packed f32x2
+// instructions take them.  Keeping pairs as 64-bit PTX values lets ptxas build
+// each pair in place (no register moves to assemble operands).
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2_pack(uint32_t lo, uint32_t hi) {
+    f2_t d;
+    asm("mov.b64 %0, {%1,%2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_const(float v) {
+    return f2_pack(__float_as_uint(v), __float_as_uint(v));
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+    f2_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+    f2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// lo + hi of a pair, in that order.
+__device__ __forceinline__ float f2_sum(f2_t a) {
+    float x, y;
+    asm("mov.b64 {%0,%1}, %2;" : "=f"(x), "=f"(y) : "l"(a));
+    return __fadd_rn(x, y);
+}
+// Two consecutive pairs (four floats) from shared memory.
+__device__ __forceinline__ void lds_f2x2(uint32_t a, f2_t& p0, f2_t& p1) {
+    asm volatile("ld.shared.v2.b64 {%0,%1}, [%2];" : "=l"(p0), "=l"(p1) : "r"(a));
+}
+
 // ------------------------------------------------------------------------------ formats
-// Raw: what one lane loads for one 16-weight chunk of one row.
-// load(row, n_in, c): chunk c of the row.   dec(raw, i, f): columns 4i..4i+3 as floats.
+// A lane's chunk is 16 bytes of codes.  kW: weights per chunk; kW / 4 float4
+// slots of x per chunk.  dec(q, i, lo, hi): columns 4i..4i+3 of the chunk as
+// two pairs.  The scale word of chunk j of a step sits scale_off(j) bytes after
+// the step's codes; scale(addr) loads it.
 
 template <int FMT> struct Fmt;
 
 template <> struct Fmt<QG_Q8_0> {
+    static constexpr int kW = 16;
     static constexpr bool kFour = false;
-    struct Raw { uint4 q; uint32_t d; };
-    static __device__ __forceinline__ Raw load(const uint8_t* row, int n_in, int c) {
-        Raw r;
-        r.q = ld_stream16(row + 16 * c);
-        r.d = ld_u16(row + n_in + 2 * (c >> 1));
-        return r;
-    }
+    static constexpr int kStepScale = 32;
+    static __device__ __forceinline__ uint32_t scale_off(int j) { return 2u * uint32_t(j >> 1); }
+    static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds16(a); }
     // bytes hold q + 128; 2^23 + (q + 128) - (2^23 + 128) = q, exact.
-    static __device__ __forceinline__ void dec(const Raw& r, int i, float2& lo, float2& hi) {
-        const uint32_t w = i == 0 ? r.q.x : i == 1 ? r.q.y : i == 2 ? r.q.z : r.q.w;
-        const float2 m = make_float2(-8388736.0f, -8388736.0f);
-        lo = __fadd2_rn(make_float2(__int_as_float(__byte_perm(w, 0x4B000000u, 0x7440)),
-                                    __int_as_float(__byte_perm(w, 0x4B000000u, 0x7441))), m);
-        hi = __fadd2_rn(make_float2(__int_as_float(__byte_perm(w, 0x4B000000u, 0x7442)),
-                                    __int_as_float(__byte_perm(w, 0x4B000000u, 0x7443))), m);
+    static __device__ __forceinline__ void dec(const uint4& q, int i, f2_t& lo, f2_t& hi, uint32_t mg) {
+        const uint32_t w = i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
+        const f2_t m = f2_const(-8388736.0f);
+        lo = f2_add(f2_pack(__byte_perm(w, mg, 0x7440), __byte_perm(w, mg, 0x7441)), m);
+        hi = f2_add(f2_pack(__byte_perm(w, mg, 0x7442), __byte_perm(w, mg, 0x7443)), m);
     }
 };
 
-// Nibble m (bits 4m..4m+3) of a half-word h as the float 2^23 + q*16^m.
-__device__ __forceinline__ float nib(uint32_t h, uint32_t mask) {
-    return __int_as_float((h & mask) | 0x4B000000u);
-}
-
 template <> struct Fmt<QG_Q4_0> {
+    static constexpr int kW = 32;
     static constexpr bool kFour = true;
-    struct Raw { uint2 q; uint32_t d; };
-    static __device__ __forceinline__ Raw load(const uint8_t* row, int n_in, int c) {
-        Raw r;
-        r.q = ld_stream8(row + 8 * c);
-        r.d = ld_u16(row + n_in / 2 + 2 * (c >> 1));
-        return r;
-    }
+    static constexpr int kStepScale = 64;
+    static __device__ __forceinline__ uint32_t scale_off(int j) { return 2u * uint32_t(j); }
+    static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds16(a); }
     // (2^23 + q*16^m) - (2^23 + 8*16^m) = (q - 8) * 16^m, exact.
-    static __device__ __forceinline__ void dec(const Raw& r, int i, float2& lo, float2& hi) {
-        const uint32_t w = (i >> 1) ? r.q.y : r.q.x;
+    static __device__ __forceinline__ void dec(const uint4& q, int i, f2_t& lo, f2_t& hi, uint32_t mg) {
+        const uint32_t w = (i >> 1) == 0 ? q.x : (i >> 1) == 1 ? q.y : (i >> 1) == 2 ? q.z : q.w;
         const uint32_t h = (i & 1) ? (w >> 16) : w;
-        lo = __fadd2_rn(make_float2(nib(h, 0x000Fu), nib(h, 0x00F0u)), make_float2(-8388616.0f, -8388736.0f));
-        hi = __fadd2_rn(make_float2(nib(h, 0x0F00u), nib(h, 0xF000u)), make_float2(-8390656.0f, -8421376.0f));
+        lo = f2_add(f2_pack(nib<0x000Fu>(h, mg), nib<0x00F0u>(h, mg)),
+                    f2_pack(__float_as_uint(-8388616.0f), __float_as_uint(-8388736.0f)));
+        hi = f2_add(f2_pack(nib<0x0F00u>(h, mg), nib<0xF000u>(h, mg)),
+                    f2_pack(__float_as_uint(-8390656.0f), __float_as_uint(-8421376.0f)));
     }
 };
 
 template <> struct Fmt<QG_AFFINE4_G64> {
+    static constexpr int kW = 32;
     static constexpr bool kFour = true;
-    struct Raw { uint2 q; uint32_t sb; };
-    static __device__ __forceinline__ Raw load(const uint8_t* row, int n_in, int c) {
-        Raw r;
-        r.q = ld_stream8(row + 8 * c);
-        r.sb = ld_u32(row + n_in / 2 + 4 * (c >> 2));
-        return r;
-    }
+    static constexpr int kStepScale = 64;
+    static __device__ __forceinline__ uint32_t scale_off(int j) { return 4u * uint32_t(j >> 1); }
+    static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds32(a); }
     // (2^23 + q*16^m) - 2^23 = q * 16^m, exact.
-    static __device__ __forceinline__ void dec(const Raw& r, int i, float2& lo, float2& hi) {
-        const uint32_t w = (i >> 1) ? r.q.y : r.q.x;
+    static __device__ __forceinline__ void dec(const uint4& q, int i, f2_t& lo, f2_t& hi, uint32_t mg) {
+        const uint32_t w = (i >> 1) == 0 ? q.x : (i >> 1) == 1 ? q.y : (i >> 1) == 2 ? q.z : q.w;
         const uint32_t h = (i & 1) ? (w >> 16) : w;
-        const float2 m = make_float2(-8388608.0f, -8388608.0f);
-        lo = __fadd2_rn(make_float2(nib(h, 0x000Fu), nib(h, 0x00F0u)), m);
-        hi = __fadd2_rn(make_float2(nib(h, 0x0F00u), nib(h, 0xF000u)), m);
+        const f2_t m = f2_const(-8388608.0f);
+        lo = f2_add(f2_pack(nib<0x000Fu>(h, mg), nib<0x00F0u>(h, mg)), m);
+        hi = f2_add(f2_pack(nib<0x0F00u>(h, mg), nib<0xF000u>(h, mg)), m);
     }
 };
 
 template <> struct Fmt<QG_BF16> {
+    static constexpr int kW = 8;
     static constexpr bool kFour = false;
-    struct Raw { uint4 a; uint4 b; };
-    static __device__ __forceinline__ Raw load(const uint8_t* row, int, int c) {
-        Raw r;
-        r.a = ld_stream16(row + 32 * c);
-        r.b = ld_stream16(row + 32 * c + 16);
-        return r;
-    }
-    static __device__ __forceinline__ void dec(const Raw& r, int i, float2& lo, float2& hi) {
-        const uint32_t w0 = i == 0 ? r.a.x : i == 1 ? r.a.z : i == 2 ? r.b.x : r.b.z;
-        const uint32_t w1 = i == 0 ? r.a.y : i == 1 ? r.a.w : i == 2 ? r.b.y : r.b.w;
-        lo = make_float2(__int_as_float(w0 << 16), __int_as_float(w0 & 0xFFFF0000u));
-        hi = make_float2(__int_as_float(w1 << 16), __int_as_float(w1 & 0xFFFF0000u));
+    static constexpr int kStepScale = 0;
+    static __device__ __forceinline__ uint32_t scale_off(int) { return 0u; }
+    static __device__ __forceinline__ uint32_t scale(uint32_t) { return 0u; }
+    static __device__ __forceinline__ void dec(const uint4& q, int i, f2_t& lo, f2_t& hi, uint32_t) {
+        const uint32_t w0 = i == 0 ? q.x : q.z;
+        const uint32_t w1 = i == 0 ? q.y : q.w;
+        lo = f2_pack(w0 << 16, w0 & 0xFFFF0000u);
+        hi = f2_pack(w1 << 16, w1 & 0xFFFF0000u);
     }
 };
 
 // ------------------------------------------------------------------------------ helpers
-
-// Physical float4 slot of logical slot g within one token's staged x row.
-__device__ __forceinline__ int xswz(int g) { return g ^ ((g >> 3) & 3); }
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
@@ -200,24 +260,50 @@ template <int V> struct Pow2Up { static constexpr int value = V <= 1 ? 1 : V <= 
 template <int V> struct Log2 { static constexpr int value = V <= 1 ? 0 : 1 + Log2<V / 2>::value; };
 template <> struct Log2<1> { static constexpr int value = 0; };
 
+// Shared memory layout of one CTA (bytes): staged x, the warps' mbarriers, the
+// warps' rings.  x is stored chunk by chunk: for lane-chunk c, the NTOK*S float4
+// slots of its columns (token-major), then one pad slot that holds the chunk's
+// per-token sums of x (used by the affine format).  The chunk stride of
+// NTOK*S+1 slots is odd, so the 8 lanes of a 128-byte shared-memory phase hit 8
+// distinct 16-byte bank groups, and every load offset is a compile-time constant.
+struct SmemPlan {
+    int x_bytes, bar_off, ring_off, total;
+};
+
+__host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int rpw, int depth, int warps) {
+    SmemPlan p;
+    const int w = fmt == QG_Q8_0 ? 16 : fmt == QG_BF16 ? 8 : 32;
+    const int slots = w / 4;
+    p.x_bytes = (n_in / w) * (ntok * slots + 1) * 16;
+    p.bar_off = (p.x_bytes + 15) / 16 * 16;
+    p.ring_off = (p.bar_off + warps * depth * 8 + 127) / 128 * 128;
+    const int step = int(kStepCodeBytes) + (fmt == QG_Q8_0 ? 32 : fmt == QG_BF16 ? 0 : 64);
+    p.total = p.ring_off + warps * depth * rpw * step;
+    return p;
+}
+
 // ------------------------------------------------------------------------------ kernel
 
-template <int FMT, int NTOK, int RPW, int DEPTH, bool ARGMAX>
-__global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
+template <int FMT, int NTOK, int RPW, bool ARGMAX>
+__global__ void __launch_bounds__(512, 1) qgemv_kernel(const KernelArgs a) {
     using F = Fmt<FMT>;
-    using Raw = typename F::Raw;
+    constexpr int S = F::kW / 4;                    // x float4 slots per chunk
     constexpr int V = RPW * NTOK;                   // outputs per row group
     constexpr int VP = Pow2Up<V>::value;
     constexpr int LG = Log2<VP>::value;
     constexpr int SPAN = 32 / VP;                   // lanes sharing one reduced value
+    constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
 
-    extern __shared__ float4 smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     const int n_in = a.n_in;
     const int n4 = n_in >> 2;
-    const int nchunks = n_in >> 4;
-    const int kmax = (nchunks + 31) >> 5;
-    float4* xs = smem;                                          // [NTOK][n4], swizzled
-    float* cs = reinterpret_cast<float*>(smem + NTOK * n4);     // affine: [NTOK][nchunks]
+    const int nchunks = n_in / F::kW;
+    const int codes = FMT == QG_Q8_0 ? n_in : FMT == QG_BF16 ? 2 * n_in : n_in / 2;
+    const int spr = (codes + 511) >> 9;             // steps per row
+    const int last_codes = codes - 512 * (spr - 1);
+    const int last_bytes = (last_codes + last_codes * F::kStepScale / 512 + 15) & ~15;
+    const int depth = a.depth;
+    const uint32_t limit = a.wait_limit;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -225,51 +311,45 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
     const int gw = blockIdx.x * nwarps + warp;
     const int GW = gridDim.x * nwarps;
     const int ngroups = (a.n_out + RPW - 1) / RPW;
-    const int sw = (lane >> 1) & 3;
 
-    // ---- load-side pipeline state (runs DEPTH chunk-steps ahead of compute)
-    Raw buf[DEPTH][RPW];
-    int gl = gw, kl = 0;
-    const uint8_t* lrow[RPW];
-    auto set_load_rows = [&](int g) {
-#pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            long long row = (long long)g * RPW + r;
-            if (row >= a.n_out) row = a.n_out - 1;      // tail group: re-read the last row, result dropped
-            lrow[r] = a.W + row * a.stride;
+    constexpr int kCS = NTOK * S + 1;               // float4 slots per chunk in staged x
+    const SmemPlan plan = smem_plan(FMT, NTOK, n_in, RPW, depth, nwarps);
+    float4* xs = reinterpret_cast<float4*>(smem);   // [nchunks][kCS]
+    const uint32_t xs_base = smem_addr(smem);
+    const uint32_t bars = smem_addr(smem + plan.bar_off) + warp * depth * 8;
+    const uint32_t ring = smem_addr(smem + plan.ring_off) + warp * depth * RPW * kFullStep;
+
+    // ---- issue side of the warp's ring: runs `depth` steps ahead of the compute side
+    int gi = gw, ki = 0, si = 0;                   // group, step in row, stage
+    uint32_t issued = 0;
+    bool failed = false;
+    // Lane 0 announces the step's bytes on the stage's mbarrier, then lanes
+    // 0..RPW-1 each start the bulk copy of one row in the same instruction.
+    auto issue = [&]() {
+        if (gi < ngroups && !failed) {
+            const uint32_t bar = bars + si * 8;
+            const int bytes = (ki == spr - 1) ? last_bytes : kFullStep;
+            const long long row0 = (long long)gi * RPW;
+            const int nrows = (a.n_out - row0) < RPW ? int(a.n_out - row0) : RPW;
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar, uint32_t(bytes * nrows) + (issued == 0 ? a.test_extra_tx : 0u));
+            __syncwarp();
+            if (lane < nrows)
+                bulk_g2s(ring + (si * RPW + lane) * kFullStep,
+                         a.W + (row0 + lane) * a.stride + (long long)ki * kFullStep, uint32_t(bytes), bar);
+            ++issued;
         }
-    };
-    // Rows of group g lie in [g*RPW, g*RPW + RPW) and are contiguous in memory, so one
-    // bulk prefetch brings the whole group into L2 ahead of the register loads.
-    auto prefetch_group = [&](int g) {
-        if (lane == 0 && g < ngroups) {
-            const long long r0 = (long long)g * RPW;
-            const long long r1 = r0 + RPW < a.n_out ? r0 + RPW : a.n_out;
-            prefetch_l2(a.W + r0 * a.stride, uint32_t((r1 - r0) * a.stride));
-        }
-    };
-    auto load_step = [&](Raw (&b)[RPW]) {
-        if (gl < ngroups) {
-            const int c = lane + 32 * kl;
-            if (c < nchunks) {
-#pragma unroll
-                for (int r = 0; r < RPW; ++r) b[r] = F::load(lrow[r], n_in, c);
-            }
-        }
-        if (++kl == kmax) {
-            kl = 0;
-            gl += GW;
-            set_load_rows(gl);
-            if (a.pf > 0) prefetch_group(gl + a.pf * GW);
-        }
+        if (++ki == spr) { ki = 0; gi += GW; }
+        if (++si == depth) si = 0;
     };
 
-    set_load_rows(gl);
-    for (int j = 0; j <= a.pf && a.pf > 0; ++j) prefetch_group(gw + j * GW);
-#pragma unroll
-    for (int u = 0; u < DEPTH; ++u) load_step(buf[u]);
+    if (lane == 0)
+        for (int s = 0; s < depth; ++s) mbar_init(bars + s * 8, 1);
+    mbar_fence_init();
+    __syncwarp();
+    for (int s = 0; s < depth; ++s) issue();
 
-    // ---- stage x (overlaps the first weight loads)
+    // ---- stage x (overlaps the first copies)
     {
         const float4* x4 = reinterpret_cast<const float4*>(a.x);
         for (int i = threadIdx.x; i < NTOK * n4; i += blockDim.x) {
@@ -281,20 +361,23 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
                 v.z *= 0.00390625f;
                 v.w *= 0.000244140625f;
             }
-            xs[t * n4 + xswz(g)] = v;
+            const int c = g / S;
+            xs[c * kCS + t * S + (g - c * S)] = v;
         }
         if constexpr (FMT == QG_AFFINE4_G64) {
+            float* xf = reinterpret_cast<float*>(smem);
             for (int i = threadIdx.x; i < NTOK * nchunks; i += blockDim.x) {
                 const int t = i / nchunks;
                 const int c = i - t * nchunks;
-                const float4* src = x4 + t * n4 + 4 * c;
-                float s = 0.f;
+                const float4* src = x4 + t * n4 + S * c;
+                float sum = 0.f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < S; ++q) {
                     const float4 v = __ldg(src + q);
-                    s = __fadd_rn(s, v.x); s = __fadd_rn(s, v.y); s = __fadd_rn(s, v.z); s = __fadd_rn(s, v.w);
+                    sum = __fadd_rn(sum, v.x); sum = __fadd_rn(sum, v.y);
+                    sum = __fadd_rn(sum, v.z); sum = __fadd_rn(sum, v.w);
                 }
-                cs[i] = s;
+                xf[(c * kCS + NTOK * S) * 4 + t] = sum;
             }
         }
     }
@@ -302,14 +385,17 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
 
     float best_v = -INFINITY;
     int best_i = 0x7FFFFFFF;
+    const uint32_t magic = a.fmagic;
+    const uint32_t x_lane = xs_base + uint32_t(lane) * (kCS * 16);          // chunk `lane` of step 0
+    const uint32_t code_lane = ring + 16u * uint32_t(lane);
+    const uint32_t scale_lane = ring + F::scale_off(lane);
 
-    // Per (row, token): within a chunk, a pair of fp32 partial sums (even and odd
-    // columns) advanced with packed fma.rn.f32x2, two columns per instruction; the
-    // pair is added and scaled once per chunk into one fp32 accumulator.  BF16 has
-    // no scale and keeps the pair across the whole row.
+    // Per (row, token): within a chunk a pair of partial sums (even / odd columns),
+    // then added and scaled into one fp32 accumulator.  BF16 (no scales) keeps the
+    // pair over the whole row.
     constexpr bool kPairAcc = (FMT == QG_BF16);
     float acc[RPW][NTOK];
-    float2 acc2[kPairAcc ? RPW : 1][kPairAcc ? NTOK : 1];
+    f2_t acc2[kPairAcc ? RPW : 1][kPairAcc ? NTOK : 1];
 #pragma unroll
     for (int r = 0; r < RPW; ++r)
 #pragma unroll
@@ -317,115 +403,138 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
 #pragma unroll
     for (int r = 0; r < (kPairAcc ? RPW : 1); ++r)
 #pragma unroll
-        for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = make_float2(0.f, 0.f);
+        for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = 0ull;
 
-    int gc = gw, kc = 0;
+    int gc = gw, kc = 0, sc = 0;
+    uint32_t consumed = 0, phase = 0;
     while (gc < ngroups) {
+        // The decision to give up is warp-uniform: every lane leaves together.
+        if (!__all_sync(kFull, mbar_wait(bars + sc * 8, phase, limit))) {
+            failed = true;
+            break;
+        }
+        ++consumed;
+        const int codes_k = (kc == spr - 1) ? last_codes : 512;
+        if (16 * lane < codes_k) {
+            const uint32_t xr = x_lane + uint32_t(kc) * (32u * kCS * 16u);
+            const uint32_t stage = uint32_t(sc) * (RPW * kFullStep);
+            uint4 qv[RPW];
+            uint32_t sv[RPW];
 #pragma unroll
-        for (int u = 0; u < DEPTH; ++u) {
-            if (gc < ngroups) {
-                const int c = lane + 32 * kc;
-                if (c < nchunks) {
-                    // ---- one 16-weight chunk of RPW rows against NTOK tokens
-                    const float4* xr = xs + 4 * c;
-                    float2 p[kPairAcc ? 1 : RPW][kPairAcc ? 1 : NTOK];
+            for (int r = 0; r < RPW; ++r) {
+                qv[r] = lds128(code_lane + stage + r * kFullStep);
+                sv[r] = F::scale(scale_lane + stage + uint32_t(codes_k) + r * kFullStep);
+            }
+            f2_t p[kPairAcc ? 1 : RPW][kPairAcc ? 1 : NTOK];
 #pragma unroll
-                    for (int r = 0; r < (kPairAcc ? 1 : RPW); ++r)
+            for (int r = 0; r < (kPairAcc ? 1 : RPW); ++r)
 #pragma unroll
-                        for (int t = 0; t < (kPairAcc ? 1 : NTOK); ++t) p[r][t] = make_float2(0.f, 0.f);
+                for (int t = 0; t < (kPairAcc ? 1 : NTOK); ++t) p[r][t] = 0ull;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float4 xv[NTOK];
+            for (int i = 0; i < S; ++i) {
+                f2_t x01[NTOK], x23[NTOK];
 #pragma unroll
-                        for (int t = 0; t < NTOK; ++t) xv[t] = xr[t * n4 + (i ^ sw)];
+                for (int t = 0; t < NTOK; ++t) lds_f2x2(xr + 16u * uint32_t(t * S + i), x01[t], x23[t]);
 #pragma unroll
-                        for (int r = 0; r < RPW; ++r) {
-                            float2 wlo, whi;
-                            F::dec(buf[u][r], i, wlo, whi);
+                for (int r = 0; r < RPW; ++r) {
+                    f2_t wlo, whi;
+                    F::dec(qv[r], i, wlo, whi, magic);
 #pragma unroll
-                            for (int t = 0; t < NTOK; ++t) {
-                                float2& pp = [&]() -> float2& {
-                                    if constexpr (kPairAcc) return acc2[r][t]; else return p[r][t];
-                                }();
-                                pp = __ffma2_rn(wlo, make_float2(xv[t].x, xv[t].y), pp);
-                                pp = __ffma2_rn(whi, make_float2(xv[t].z, xv[t].w), pp);
-                            }
-                        }
+                    for (int t = 0; t < NTOK; ++t) {
+                        f2_t& pp = [&]() -> f2_t& {
+                            if constexpr (kPairAcc) return acc2[r][t]; else return p[r][t];
+                        }();
+                        pp = f2_fma(wlo, x01[t], pp);
+                        pp = f2_fma(whi, x23[t], pp);
                     }
-                    if constexpr (FMT == QG_Q8_0 || FMT == QG_Q4_0) {
-#pragma unroll
-                        for (int r = 0; r < RPW; ++r) {
-                            const float d = h2f(buf[u][r].d);
-#pragma unroll
-                            for (int t = 0; t < NTOK; ++t)
-                                acc[r][t] = __fmaf_rn(d, __fadd_rn(p[r][t].x, p[r][t].y), acc[r][t]);
-                        }
-                    } else if constexpr (FMT == QG_AFFINE4_G64) {
-                        float csv[NTOK];
-#pragma unroll
-                        for (int t = 0; t < NTOK; ++t) csv[t] = cs[t * nchunks + c];
-#pragma unroll
-                        for (int r = 0; r < RPW; ++r) {
-                            const uint32_t sb = buf[u][r].sb;
-                            const float sc = h2f(sb & 0xFFFFu), b = h2f(sb >> 16);
-#pragma unroll
-                            for (int t = 0; t < NTOK; ++t)
-                                acc[r][t] = __fmaf_rn(sc, __fadd_rn(p[r][t].x, p[r][t].y), __fmaf_rn(b, csv[t], acc[r][t]));
-                        }
-                    }
-                }
-                load_step(buf[u]);
-                if (++kc == kmax) {
-                    // ---- finish the row group: transposed warp reduction
-                    float v[VP];
-#pragma unroll
-                    for (int j = 0; j < VP; ++j) {
-                        if constexpr (kPairAcc)
-                            v[j] = j < V ? __fadd_rn(acc2[j / NTOK][j % NTOK].x, acc2[j / NTOK][j % NTOK].y) : 0.f;
-                        else
-                            v[j] = j < V ? acc[j / NTOK][j % NTOK] : 0.f;
-                    }
-#pragma unroll
-                    for (int s = 0; s < LG; ++s) {
-                        const int h = VP >> (s + 1);
-                        const int mask = 16 >> s;
-                        const bool upper = (lane & mask) != 0;
-#pragma unroll
-                        for (int j = 0; j < h; ++j) {
-                            const float send = upper ? v[j] : v[j + h];
-                            const float keep = upper ? v[j + h] : v[j];
-                            v[j] = keep + __shfl_xor_sync(kFull, send, mask);
-                        }
-                    }
-#pragma unroll
-                    for (int mask = 16 >> LG; mask >= 1; mask >>= 1) v[0] += __shfl_xor_sync(kFull, v[0], mask);
-                    const int vi = lane / SPAN;                       // value index this lane holds
-                    if (vi < V && (lane % SPAN) == 0) {
-                        const int r = vi / NTOK, t = vi - r * NTOK;
-                        const long long row = (long long)gc * RPW + r;
-                        if (row < a.n_out) {
-                            if (!ARGMAX || a.y) a.y[(long long)t * a.n_out + row] = v[0];
-                            if (ARGMAX && better(v[0], int(row), best_v, best_i)) { best_v = v[0]; best_i = int(row); }
-                        }
-                    }
-#pragma unroll
-                    for (int r = 0; r < RPW; ++r)
-#pragma unroll
-                        for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.f;
-#pragma unroll
-                    for (int r = 0; r < (kPairAcc ? RPW : 1); ++r)
-#pragma unroll
-                        for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = make_float2(0.f, 0.f);
-                    kc = 0;
-                    gc += GW;
                 }
             }
+            if constexpr (FMT == QG_Q8_0 || FMT == QG_Q4_0) {
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    const float d = h2f(sv[r]);
+#pragma unroll
+                    for (int t = 0; t < NTOK; ++t)
+                        acc[r][t] = __fmaf_rn(d, f2_sum(p[r][t]), acc[r][t]);
+                }
+            } else if constexpr (FMT == QG_AFFINE4_G64) {
+                float csv[4];
+                {
+                    const uint4 cv = lds128(xr + 16u * uint32_t(NTOK * S));
+                    csv[0] = __uint_as_float(cv.x); csv[1] = __uint_as_float(cv.y);
+                    csv[2] = __uint_as_float(cv.z); csv[3] = __uint_as_float(cv.w);
+                }
+#pragma unroll
+                for (int r = 0; r < RPW; ++r) {
+                    const float s = h2f(sv[r] & 0xFFFFu), b = h2f(sv[r] >> 16);
+#pragma unroll
+                    for (int t = 0; t < NTOK; ++t)
+                        acc[r][t] = __fmaf_rn(s, f2_sum(p[r][t]), __fmaf_rn(b, csv[t], acc[r][t]));
+                }
+            }
+        }
+        __syncwarp();          // every lane has read this stage before it is refilled
+        issue();
+        if (++sc == depth) { sc = 0; phase ^= 1u; }
+        if (++kc == spr) {
+            // ---- finish the row group: transposed warp reduction
+            float v[VP];
+#pragma unroll
+            for (int j = 0; j < VP; ++j) {
+                if constexpr (kPairAcc)
+                    v[j] = j < V ? f2_sum(acc2[j / NTOK][j % NTOK]) : 0.f;
+                else
+                    v[j] = j < V ? acc[j / NTOK][j % NTOK] : 0.f;
+            }
+#pragma unroll
+            for (int s = 0; s < LG; ++s) {
+                const int h = VP >> (s + 1);
+                const int mask = 16 >> s;
+                const bool upper = (lane & mask) != 0;
+#pragma unroll
+                for (int j = 0; j < h; ++j) {
+                    const float send = upper ? v[j] : v[j + h];
+                    const float keep = upper ? v[j + h] : v[j];
+                    v[j] = keep + __shfl_xor_sync(kFull, send, mask);
+                }
+            }
+#pragma unroll
+            for (int mask = 16 >> LG; mask >= 1; mask >>= 1) v[0] += __shfl_xor_sync(kFull, v[0], mask);
+            const int vi = lane / SPAN;                       // value index this lane holds
+            if (vi < V && (lane % SPAN) == 0) {
+                const int r = vi / NTOK, t = vi - r * NTOK;
+                const long long row = (long long)gc * RPW + r;
+                if (row < a.n_out) {
+                    if (!ARGMAX || a.y) a.y[(long long)t * a.n_out + row] = v[0];
+                    if (ARGMAX && better(v[0], int(row), best_v, best_i)) { best_v = v[0]; best_i = int(row); }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RPW; ++r)
+#pragma unroll
+                for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.f;
+#pragma unroll
+            for (int r = 0; r < (kPairAcc ? RPW : 1); ++r)
+#pragma unroll
+                for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = 0ull;
+            kc = 0;
+            gc += GW;
+        }
+    }
+
+    if (failed) {
+        // Report, then drain (bounded) every copy this warp issued but did not consume,
+        // so no bulk copy is still writing this CTA's shared memory when it exits.
+        if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+        for (uint32_t f = consumed; f < issued; ++f) {
+            mbar_wait(bars + sc * 8, phase, a.drain_limit);
+            if (++sc == depth) { sc = 0; phase ^= 1u; }
         }
     }
 
     if constexpr (ARGMAX) {
         // ---- per-token argmax: warp -> CTA partial -> last CTA reduces all partials
-        __shared__ ArgmaxPartial wbest[16][kMaxNtok];
+        __shared__ ArgmaxPartial wbest[kMaxWarps][kMaxNtok];
         __shared__ bool last_cta;
         const int vi = lane / SPAN;
         const int my_t = (vi < V && (lane % SPAN) == 0) ? vi % NTOK : -1;
@@ -476,14 +585,7 @@ __global__ void __launch_bounds__(256, 2) qgemv_kernel(const KernelArgs a) {
     }
 }
 
-// Shared memory bytes of one CTA.
-inline size_t smem_bytes(int fmt, int ntok, int n_in) {
-    size_t b = size_t(ntok) * size_t(n_in) * 4;
-    if (fmt == QG_AFFINE4_G64) b += size_t(ntok) * size_t(n_in / 16) * 4;
-    return b;
-}
-
 // Lookup of an instantiated kernel (defined in the per-format instantiation units).
-const void* kernel_lookup(int fmt, int ntok, int rpw, int depth, bool argmax);
+const void* kernel_lookup(int fmt, int ntok, int rpw, bool argmax);
 
 }  // namespace qg

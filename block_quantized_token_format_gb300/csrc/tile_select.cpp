@@ -18,17 +18,7 @@
 namespace qg {
 
 bool rpw_ok(int v) { return v == 1 || v == 2 || v == 4; }
-bool depth_ok(int v) { return v == 2 || v == 4; }
-
-// Register budget at 128 registers per thread: the (rpw, depth) pairs that spill,
-// from -Xptxas -v of every instantiation (8-bit and BF16 chunks hold 16-32 bytes
-// of codes per row, 4-bit chunks 8 bytes).
-bool tile_fits_registers(int fmt, int ntok, int rpw, int depth) {
-    const bool four = (fmt == QG_Q4_0 || fmt == QG_AFFINE4_G64);
-    if (rpw == 4 && depth == 4 && !four && ntok >= 3) return false;
-    if (rpw == 4 && depth == 4 && fmt == QG_BF16 && ntok >= 2) return false;
-    return true;
-}
+bool depth_ok(int v) { return v >= 2 && v <= 16; }
 
 namespace {
 
@@ -56,19 +46,12 @@ Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
         return e.tile;
     }
     Tile t;
-    const bool four = (fmt == QG_Q4_0 || fmt == QG_AFFINE4_G64);
-    if (four) {
-        t.rpw = 4;
-        t.depth = 4;
-    } else {
-        t.rpw = ntok <= 2 ? 2 : 2;
-        t.depth = 4;
-    }
-    // Few rows: spread them over more warps.
-    if (n_out < 8192 && t.rpw > 1) t.rpw = 2;
-    if (!tile_fits_registers(fmt, ntok, t.rpw, t.depth)) t.depth = 2;
-    t.warps = 8;
-    t.ctas = 2;
+    // Many rows: 4 rows per warp amortise x reads; few rows: spread them thinner.
+    t.rpw = n_out >= 8192 ? 4 : 2;
+    t.depth = 2;
+    t.warps = 16;
+    t.ctas = 1;
+    (void)fmt; (void)n_in; (void)ntok;
     return t;
 }
 
@@ -77,7 +60,6 @@ Tile apply_override(Tile t, const TileOverride& o) {
     if (o.depth > 0) t.depth = o.depth;
     if (o.warps > 0) t.warps = o.warps;
     if (o.ctas > 0) t.ctas = o.ctas;
-    if (o.pf >= 0) t.pf = o.pf;
     return t;
 }
 
@@ -100,9 +82,8 @@ bool parse_tile_spec(const char* spec, TileOverride* out) {
         int v = std::atoi(val.c_str());
         if (key == "rpw") { if (!rpw_ok(v)) return false; o.rpw = v; }
         else if (key == "depth") { if (!depth_ok(v)) return false; o.depth = v; }
-        else if (key == "warps") { if (v < 1 || v > 8) return false; o.warps = v; }
+        else if (key == "warps") { if (v < 1 || v > 16) return false; o.warps = v; }
         else if (key == "ctas") { if (v < 1 || v > 8) return false; o.ctas = v; }
-        else if (key == "pf") { if (v < 0 || v > 16) return false; o.pf = v; }
         else return false;
     }
     *out = o;
@@ -111,7 +92,7 @@ bool parse_tile_spec(const char* spec, TileOverride* out) {
 
 std::string tile_to_string(const Tile& t) {
     char b[96];
-    std::snprintf(b, sizeof b, "rpw=%d,depth=%d,warps=%d,ctas=%d,pf=%d", t.rpw, t.depth, t.warps, t.ctas, t.pf);
+    std::snprintf(b, sizeof b, "rpw=%d,depth=%d,warps=%d,ctas=%d", t.rpw, t.depth, t.warps, t.ctas);
     return b;
 }
 

@@ -66,16 +66,18 @@ int qg_abi_version(void);
  *          (element k of a word at bits [4k,4k+4)), fp16 scales [n_out][n_in/64],
  *          fp16 biases [n_out][n_in/64].
  *   BF16:  bf16 [n_out][n_in].
- * Device layout: what qgemv reads.  Row-interleaved: each row holds its codes,
- * then its scales, then zero padding up to a 16-byte multiple (no padding when
- * n_in is a multiple of 256).  Rows are stored one after the other, so the
- * first k rows of a packed matrix are themselves a packed k-row matrix (a
- * reduced draft vocabulary that is a prefix of the head needs no copy).
- *   Q8_0:  n_in bytes of q+128 (uint8), then n_in/32 fp16 d.
- *   Q4_0:  n_in/2 bytes as uint32 words of 8 consecutive elements (element k at
- *          bits [4k,4k+4)), then n_in/32 fp16 d.
- *   AFFINE4_G64: the row's n_in/8 uint32 words, then n_in/64 (fp16 s, fp16 b) pairs.
- *   BF16:  the row's n_in bf16 values.
+ * Device layout: what qgemv reads.  Rows are stored one after the other, so
+ * the first k rows of a packed matrix are themselves a packed k-row matrix (a
+ * reduced draft vocabulary that is a prefix of the head needs no copy).  A row
+ * is a run of steps; a step is 512 bytes of codes followed by the scales of
+ * exactly those codes, zero-padded to a 16-byte multiple (only the last step
+ * of a row can be shorter).  No padding at all when the codes of a row are a
+ * multiple of 512 bytes (n_in a multiple of 512 for Q8_0, 1024 for the 4-bit
+ * formats, 256 for BF16), so then qg_packed_bytes == qg_canonical_bytes.
+ *   codes:  Q8_0 q+128 (uint8); Q4_0 and AFFINE4_G64 uint32 words of 8
+ *           consecutive elements (element k at bits [4k,4k+4)); BF16 raw.
+ *   scales: Q8_0 / Q4_0 one fp16 d per 32 weights; AFFINE4_G64 one (fp16 s,
+ *           fp16 b) pair per 64 weights.
  * Sizes return 0 for invalid arguments. */
 size_t  qg_canonical_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);
 size_t  qg_packed_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);
@@ -137,23 +139,41 @@ qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /* --------------------------------------------------------------- tile selection
- * The kernel geometry (rows per warp, loads in flight, warps per CTA, CTAs per
- * SM) is chosen per (fmt, n_out, n_in, ntok) by a table measured on GB300 with
- * a heuristic fallback (the Track 2 audit's per-shape, per-ntok tile rules are
- * the prior art).  The reduction order never depends on this choice.
+ * The kernel geometry (rows per warp, ring stages per warp, warps per CTA, CTAs
+ * per SM) is chosen per (fmt, n_out, n_in, ntok) by a table measured on GB300
+ * with a heuristic fallback (the Track 2 audit's per-shape, per-ntok tile
+ * rules are the prior art).  The reduction order never depends on this choice.
  *
  * qg_set_tile_override: force a geometry for later calls, e.g.
- * "rpw=4,depth=2,warps=8,ctas=2,pf=2" (any subset of the keys; rpw in {1,2,4},
- * depth in {2,4}, warps in {1..8}, ctas in {1..8}, pf (L2 prefetch distance in
- * row groups, 0 = off) in {0..16}).  NULL or "" clears it.
- * The environment variable QGEMV_TILE, read at the first call, sets the same
- * override.  Returns QG_EINVAL on a malformed spec (the override is unchanged).
+ * "rpw=4,depth=4,warps=8,ctas=2" (any subset of the keys; rpw in {1,2,4},
+ * depth in {2..16}, warps in {1..16}, ctas in {1..8}; the ring depth and then
+ * the warp count are lowered if the CTA would not fit in shared memory).
+ * NULL or "" clears it.  The environment variable QGEMV_TILE, read at the
+ * first call, sets the same override.  Returns QG_EINVAL on a malformed spec
+ * (the override is unchanged).
  *
  * qg_describe_tile: writes the geometry a call would use into buf as
  * "rpw=..,depth=..,warps=..,ctas=..,grid=.." (NUL-terminated, truncated to len). */
 qg_status qg_set_tile_override(const char* spec);
 qg_status qg_describe_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, int ntok,
                            char* buf, size_t len);
+
+/* ------------------------------------------------------------ device status
+ * Every wait inside the kernels (on the mbarrier that counts a bulk copy into
+ * shared memory) is bounded.  If a wait gives up, the kernel sets
+ * QG_DEVICE_WAIT_TIMEOUT in a per-device status word, stops issuing copies,
+ * drains the copies it already issued (again bounded) and exits normally; its
+ * outputs are then not valid.  qg_device_status copies the current device's
+ * word into *status (synchronously: it waits for the device) and, if `clear`,
+ * resets it to 0. */
+#define QG_DEVICE_WAIT_TIMEOUT 1u
+qg_status qg_device_status(int clear, unsigned int* status);
+
+/* Test hook: `polls` = polls of an mbarrier before a wait gives up (0 restores
+ * the default, about 4 million); `extra_tx_bytes` > 0 adds that many bytes to
+ * the first expected transaction of every warp, so that wait can never
+ * complete and the timeout path runs.  Process-wide; for tests only. */
+qg_status qg_set_wait_limit(uint32_t polls, uint32_t extra_tx_bytes);
 
 #ifdef __cplusplus
 }

@@ -134,8 +134,8 @@ def test_tile_choice_does_not_change_bits(fmt):
     qg.qg_set_tile_override(None)
     base = {ntok: gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok]) for ntok in (1, 3)}
     try:
-        for spec in ["rpw=1,depth=2", "rpw=1,depth=4,warps=4,pf=1", "rpw=2,depth=2,warps=2,ctas=1",
-                     "rpw=2,depth=4,pf=2", "rpw=4,depth=2,warps=8,ctas=2,pf=4", "rpw=4,depth=4,warps=1,pf=16"]:
+        for spec in ["rpw=1,depth=2", "rpw=1,depth=4,warps=4", "rpw=2,depth=2,warps=2,ctas=1",
+                     "rpw=2,depth=8", "rpw=4,depth=3,warps=8,ctas=2", "rpw=4,depth=16,warps=1"]:
             qg.qg_set_tile_override(spec)
             for ntok in (1, 3):
                 y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
