@@ -20,7 +20,7 @@ __all__ = [
     "qg_strerror", "qg_abi_version", "qg_canonical_bytes", "qg_packed_bytes", "qg_row_stride",
     "qg_quantize", "qg_to_device_layout", "qg_pack", "qgemv", "qgemv_argmax_workspace_bytes",
     "qgemv_argmax", "qg_set_tile_override", "qg_describe_tile", "weight_bytes", "qg_device_status",
-    "qg_set_wait_limit", "QG_DEVICE_WAIT_TIMEOUT",
+    "qg_set_wait_limit", "QG_DEVICE_WAIT_TIMEOUT", "qgemv_argmax_noalloc",
 ]
 
 QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
@@ -72,6 +72,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "qg_describe_tile": (i32, [i32, i64, i64, i32, ctypes.c_char_p, sz]),
         "qg_device_status": (i32, [i32, ctypes.POINTER(ctypes.c_uint)]),
         "qg_set_wait_limit": (i32, [ctypes.c_uint, ctypes.c_uint]),
+        "qgemv_argmax_noalloc": (i32, [i32, vp, i64, i64, vp, vp, vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -196,6 +197,17 @@ def qgemv_argmax(fmt, W, n_out: int, n_in: int, x, y, argmax, workspace, ntok: i
     st = load_library().qgemv_argmax(_fmt(fmt), _ptr(W), n_out, n_in, _ptr(x), _ptr(y), _ptr(argmax),
                                      int(ntok), _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "qgemv_argmax")
+
+
+def qgemv_argmax_noalloc(fmt, W, n_out: int, n_in: int, x, y, argmax, ntok: int | None = None,
+                         stream=None) -> None:
+    """qgemv_argmax without a workspace, for callers that cannot allocate device memory:
+    the scratch is a fixed array inside the library (calls that overlap on the GPU race)."""
+    if ntok is None:
+        ntok = x.shape[0] if getattr(x, "dim", lambda: 1)() == 2 else 1
+    st = load_library().qgemv_argmax_noalloc(_fmt(fmt), _ptr(W), n_out, n_in, _ptr(x), _ptr(y), _ptr(argmax),
+                                             int(ntok), _stream(stream))
+    _check(st, "qgemv_argmax_noalloc")
 
 
 def qg_set_tile_override(spec: str | None) -> None:

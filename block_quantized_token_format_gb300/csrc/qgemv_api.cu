@@ -316,3 +316,66 @@ qg_status qg_describe_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, int ntok, ch
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ no-allocation variant
+// qgemv_argmax_noalloc: the fused LM-head argmax for callers that cannot call
+// cudaMalloc.  Its scratch (the CTA ticket and the per-CTA partial maxima) is a
+// fixed array in this library's device image instead of a caller-provided
+// workspace.  Nothing here allocates: the array exists on every GPU the
+// library is loaded on, for the life of the process.
+namespace qg {
+namespace {
+
+constexpr int kNoAllocMaxGrid = 1024;        // CTAs whose partials fit in the array
+constexpr size_t kNoAllocScratchBytes = 16 + size_t(kNoAllocMaxGrid) * kMaxNtok * sizeof(ArgmaxPartial);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch per device, looked up once per device.
+std::atomic<void*> g_noalloc_addr[kMaxDevices];
+
+}  // namespace
+}  // namespace qg
+
+extern "C" qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
+                                          const float* x, float* y, int32_t* argmax, int ntok,
+                                          void* stream) {
+    qg_status st = check_common(fmt, W, n_out, n_in, x, ntok);
+    if (st != QG_OK) return st;
+    if (!argmax) return QG_EINVAL;
+    if ((y && !aligned(y, 4)) || !aligned(argmax, 4)) return QG_EALIGN;
+
+    // Set-up, once per device, with that device current: the host-side name of the
+    // array is only a stand-in, so ask the runtime for its device address.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return QG_EUNSUPPORTED;
+    void* scratch = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (scratch == nullptr) {
+        if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr) {
+            cudaGetLastError();
+            return QG_ECUDA;
+        }
+        g_noalloc_addr[dev].store(scratch, std::memory_order_release);
+    }
+
+    Plan p;
+    st = plan_launch(fmt, n_out, n_in, ntok, true, &p);
+    if (st != QG_OK) return st;
+    // The launch needs a ticket plus one partial per CTA and token; refuse a launch
+    // geometry (possible only through a tile override) that the array cannot hold.
+    const size_t need = 16 + size_t(p.grid) * size_t(ntok) * sizeof(ArgmaxPartial);
+    if (need > kNoAllocScratchBytes) return QG_EWORKSPACE;
+
+    // The array keeps whatever the last call left; the ticket must start at zero.
+    if (cudaMemsetAsync(scratch, 0, 16, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return QG_ECUDA;
+    }
+    KernelArgs a{};
+    fill_common(a, p, fmt, W, n_out, n_in, x, y);
+    a.argmax = argmax;
+    a.ticket = static_cast<unsigned int*>(scratch);
+    a.partials = reinterpret_cast<ArgmaxPartial*>(static_cast<uint8_t*>(scratch) + 16);
+    return launch(p, a, stream);
+}

@@ -138,6 +138,30 @@ qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
                        const float* x, float* y, int32_t* argmax, int ntok,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------- qgemv_argmax_noalloc
+ * No counterpart on the source pages: an addition for callers that cannot call
+ * cudaMalloc, such as a plugin inside a host framework that owns every device
+ * allocation, or a decode loop that must never hit the device allocator (which
+ * can synchronize the device).  Same computation, arguments and rules as
+ * qgemv_argmax, but without a workspace: the scratch it needs (a ticket and one
+ * partial maximum per CTA and token) is a fixed array inside this library,
+ * 32 KiB + 16 bytes, present on every GPU that loads the library until the
+ * process exits.  It allocates nothing and calls no allocating routine.
+ *   - The first call on a device looks up that array's device address for the
+ *     current device (a one-time set-up); make that first call before any
+ *     stream capture.
+ *   - Each call clears the ticket (cudaMemsetAsync on `stream`) before its
+ *     kernel; the array otherwise keeps the last call's contents.
+ *   - All calls on a device share the one array: calls that overlap on the GPU
+ *     (different streams, no ordering between them) race and give wrong
+ *     results.  Serialize them, e.g. on one stream.
+ *   - A launch that would need partials for more than 1024 CTAs is refused
+ *     with QG_EWORKSPACE (possible only with a tile override of many CTAs per
+ *     SM); otherwise the errors are those of qgemv_argmax. */
+qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
+                               const float* x, float* y, int32_t* argmax, int ntok,
+                               void* stream);
+
 /* --------------------------------------------------------------- tile selection
  * The kernel geometry (rows per warp, ring stages per warp, warps per CTA, CTAs
  * per SM) is chosen per (fmt, n_out, n_in, ntok) by a table measured on GB300
