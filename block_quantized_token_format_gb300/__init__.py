@@ -20,7 +20,8 @@ __all__ = [
     "qg_strerror", "qg_abi_version", "qg_canonical_bytes", "qg_packed_bytes", "qg_row_stride",
     "qg_quantize", "qg_to_device_layout", "qg_pack", "qgemv", "qgemv_argmax_workspace_bytes",
     "qgemv_argmax", "qg_set_tile_override", "qg_describe_tile", "weight_bytes", "qg_device_status",
-    "qg_set_wait_limit", "QG_DEVICE_WAIT_TIMEOUT", "qgemv_argmax_noalloc",
+    "qg_set_wait_limit", "QG_DEVICE_WAIT_TIMEOUT", "qgemv_argmax_noalloc", "qg_set_launch_options",
+    "QG_LAUNCH_EARLY_START",
 ]
 
 QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
@@ -73,6 +74,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "qg_device_status": (i32, [i32, ctypes.POINTER(ctypes.c_uint)]),
         "qg_set_wait_limit": (i32, [ctypes.c_uint, ctypes.c_uint]),
         "qgemv_argmax_noalloc": (i32, [i32, vp, i64, i64, vp, vp, vp, i32, vp]),
+        "qg_set_launch_options": (i32, [ctypes.c_uint]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -227,6 +229,12 @@ def qg_set_wait_limit(polls: int = 0, extra_tx_bytes: int = 0) -> None:
 
 
 QG_DEVICE_WAIT_TIMEOUT = 1
+QG_LAUNCH_EARLY_START = 1
+
+
+def qg_set_launch_options(flags: int) -> None:
+    """QG_LAUNCH_EARLY_START: overlap back-to-back calls (weights must not be written in flight)."""
+    _check(load_library().qg_set_launch_options(int(flags)), "qg_set_launch_options")
 
 
 def qg_describe_tile(fmt, n_out: int, n_in: int, ntok: int) -> str:

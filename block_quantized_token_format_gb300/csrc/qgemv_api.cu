@@ -203,11 +203,34 @@ qg_status check_common(int fmt, const void* W, int64_t n_out, int64_t n_in, cons
     return QG_OK;
 }
 
+// Launch options (qg_set_launch_options / QGEMV_EARLY_START).
+std::atomic<unsigned> g_launch_flags{0};
+std::once_flag g_launch_env_once;
+
+unsigned launch_flags() {
+    std::call_once(g_launch_env_once, [] {
+        const char* e = std::getenv("QGEMV_EARLY_START");
+        if (e && e[0] == '1') g_launch_flags.fetch_or(QG_LAUNCH_EARLY_START);
+    });
+    return g_launch_flags.load(std::memory_order_relaxed);
+}
+
 qg_status launch(const Plan& p, const KernelArgs& args, void* stream) {
     KernelArgs a = args;
     void* params[] = {&a};
-    cudaError_t e = cudaLaunchKernel(p.fn, dim3(p.grid), dim3(p.threads), params, p.smem,
-                                     static_cast<cudaStream_t>(stream));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(p.threads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    if (launch_flags() & QG_LAUNCH_EARLY_START) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelExC(&cfg, p.fn, params);
     if (e != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
     return QG_OK;
 }
@@ -296,6 +319,13 @@ qg_status qg_device_status(int clear, unsigned int* status) {
         }
     }
     *status = v;
+    return QG_OK;
+}
+
+qg_status qg_set_launch_options(unsigned int flags) {
+    if (flags & ~unsigned(QG_LAUNCH_EARLY_START)) return QG_EINVAL;
+    launch_flags();                       // consume the environment first, then override it
+    g_launch_flags.store(flags, std::memory_order_relaxed);
     return QG_OK;
 }
 

@@ -343,11 +343,21 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const KernelArgs a) {
         if (++si == depth) si = 0;
     };
 
+    // Programmatic dependent launch: let the next kernel in the stream start its
+    // own weight copies as soon as SMs free up (a no-op without that launch mode).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     if (lane == 0)
         for (int s = 0; s < depth; ++s) mbar_init(bars + s * 8, 1);
     mbar_fence_init();
     __syncwarp();
+    // The first copies read only W, which no earlier kernel writes (the caller's
+    // promise when it enables the early start), so they go before the wait.
     for (int s = 0; s < depth; ++s) issue();
+
+    // Everything below may depend on the previous kernel in the stream (x, y, the
+    // argmax workspace): wait for it to complete (a no-op without the early start).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- stage x (overlaps the first copies)
     {

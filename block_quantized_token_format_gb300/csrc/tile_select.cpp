@@ -8,6 +8,7 @@
 // kTable (filled from sweeps on GB300).
 #include "tile_select.h"
 
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -27,12 +28,48 @@ struct Entry {
     int64_t n_out_min, n_out_max;   // inclusive range of n_out
     int64_t n_in;                   // 0 = any
     int ntok;                       // 0 = any
-    Tile tile;
+    Tile tile;                      // {rpw, depth, warps, ctas}
 };
 
-// Measured on GB300 (see the sweep summary in profiles/); first match wins.
+// Measured on GB300 (tile sweeps over rows per warp, ring depth, warps per CTA
+// and CTAs per SM, back-to-back launches with early start; the sweep summary is
+// in profiles/).  First match wins.
 const Entry kTable[] = {
-    {-1, 0, 0, 0, 0, {}},   // sentinel
+    // Q8_0, n_in 2560: LM heads
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 1, {4, 3, 12, 2}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 2, {4, 2, 16, 1}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 0, {4, 5, 16, 1}},
+    // Q8_0, n_in 2560: 9000..65535 rows (the 10240 / 12288 projections)
+    {QG_Q8_0, 11264, 65535, 2560, 1, {4, 3, 8, 3}},
+    {QG_Q8_0, 11264, 65535, 2560, 2, {4, 5, 4, 3}},
+    {QG_Q8_0, 11264, 65535, 2560, 3, {4, 7, 12, 1}},
+    {QG_Q8_0, 11264, 65535, 2560, 4, {4, 2, 12, 1}},
+    {QG_Q8_0, 9000, 11263, 2560, 1, {4, 3, 12, 2}},
+    {QG_Q8_0, 9000, 11263, 2560, 0, {4, 7, 12, 1}},
+    // Q8_0, n_in 2560: 4096..8999 rows (the 6144 projection)
+    {QG_Q8_0, 4096, 8999, 2560, 1, {4, 5, 4, 3}},
+    {QG_Q8_0, 4096, 8999, 2560, 2, {4, 5, 8, 2}},
+    {QG_Q8_0, 4096, 8999, 2560, 0, {4, 2, 12, 1}},
+    // Q8_0, n_in 2560: up to 4095 rows (2560 x 2560)
+    {QG_Q8_0, 1, 4095, 2560, 1, {1, 5, 12, 2}},
+    {QG_Q8_0, 1, 4095, 2560, 2, {4, 5, 8, 2}},
+    {QG_Q8_0, 1, 4095, 2560, 0, {2, 5, 12, 1}},
+    // Q8_0, n_in 6144, few rows (6144 -> 2560)
+    {QG_Q8_0, 1, 8191, 6144, 1, {1, 8, 12, 2}},
+    {QG_Q8_0, 1, 8191, 6144, 0, {2, 8, 12, 1}},
+    // Q4_0 and BF16, 8192 x 2560
+    {QG_Q4_0, 4096, 65535, 2560, 1, {4, 5, 8, 2}},
+    {QG_Q4_0, 4096, 65535, 2560, 2, {4, 2, 8, 2}},
+    {QG_Q4_0, 4096, 65535, 2560, 3, {4, 3, 8, 2}},
+    {QG_Q4_0, 4096, 65535, 2560, 4, {4, 3, 16, 1}},
+    {QG_BF16, 4096, 65535, 2560, 1, {4, 5, 8, 2}},
+    {QG_BF16, 4096, 65535, 2560, 2, {4, 5, 8, 2}},
+    {QG_BF16, 4096, 65535, 2560, 3, {4, 3, 8, 2}},
+    {QG_BF16, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
+    // affine 4-bit LM head
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {4, 5, 16, 1}},
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {4, 2, 16, 1}},
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 0, {4, 3, 16, 1}},
 };
 
 }  // namespace
@@ -45,13 +82,20 @@ Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
         if (e.ntok && e.ntok != ntok) continue;
         return e.tile;
     }
+    // Heuristic for unmeasured shapes: many rows stream 4 per warp in one 16-warp
+    // CTA per SM with a shallow ring (bandwidth-bound); few rows use fewer rows per
+    // warp, deeper rings and 12-warp CTAs so the short kernel still fills the GPU.
     Tile t;
-    // Many rows: 4 rows per warp amortise x reads; few rows: spread them thinner.
-    t.rpw = n_out >= 8192 ? 4 : 2;
-    t.depth = 2;
-    t.warps = 16;
-    t.ctas = 1;
-    (void)fmt; (void)n_in; (void)ntok;
+    if (n_out >= 65536) {
+        t = {4, 2, 16, 1};
+    } else if (n_out >= 8192) {
+        t = {4, 3, 12, 1};
+    } else if (n_out >= 4096) {
+        t = {2, 5, 12, 1};
+    } else {
+        t = {1, 6, 12, 2};
+    }
+    (void)n_in; (void)ntok;
     return t;
 }
 

@@ -182,6 +182,20 @@ qg_status qg_set_tile_override(const char* spec);
 qg_status qg_describe_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, int ntok,
                            char* buf, size_t len);
 
+/* ------------------------------------------------------------- launch options
+ * QG_LAUNCH_EARLY_START: launch with programmatic dependent launch.  Each kernel
+ * lets the next kernel in the stream start as soon as SMs free up, and a kernel
+ * that starts early begins copying its weights W before the previous kernel
+ * has finished; it waits for that kernel to complete before it reads x or
+ * writes y, argmax or the workspace.  So back-to-back calls (a decode chain of
+ * projections) overlap one call's weight stream with the previous call's tail.
+ * Enable it only when W is not written by work still in flight in the stream
+ * (model weights are written once, before decoding).  Process-wide; default
+ * off; the environment variable QGEMV_EARLY_START=1 turns it on at first use.
+ * Unknown flags give QG_EINVAL. */
+#define QG_LAUNCH_EARLY_START 1u
+qg_status qg_set_launch_options(unsigned int flags);
+
 /* ------------------------------------------------------------ device status
  * Every wait inside the kernels (on the mbarrier that counts a bulk copy into
  * shared memory) is bounded.  If a wait gives up, the kernel sets

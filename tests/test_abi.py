@@ -77,3 +77,11 @@ def test_tile_override_grammar():
                 b"rpw=-1", b"pf=2"):
         assert lib.qg_set_tile_override(bad) == -1, bad
     assert lib.qg_set_tile_override(None) == 0
+
+
+def test_launch_options():
+    lib = qg.load_library()
+    assert lib.qg_set_launch_options(1) == 0
+    assert lib.qg_set_launch_options(0) == 0
+    assert lib.qg_set_launch_options(2) == -1
+    assert lib.qg_set_launch_options(0xFFFF) == -1
