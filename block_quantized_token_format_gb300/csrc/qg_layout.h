@@ -2,8 +2,9 @@
 // CUDA launch code.  Canonical layout = the formats' stored bytes; device
 // layout = rows one after the other, each row a run of 16-byte-aligned steps
 // of [512 B of codes][their scales][pad], so every row starts on a 16-byte
-// boundary, one step of one row is one contiguous bulk copy, and a row prefix
-// of a packed matrix is a packed matrix.
+// boundary, step k of RPW consecutive rows is one box of a 2-D tensor copy
+// ([n_out][row stride / 8] elements of 8 bytes), and a row prefix of a packed
+// matrix is a packed matrix.
 #pragma once
 
 #include <cstdint>

@@ -1,5 +1,6 @@
 // C ABI entry points of the mat-vec: validation, tile selection, launch.
 // The operation and every argument rule are documented in include/qgemv.h.
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
@@ -163,10 +164,10 @@ qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argma
     const int threads = 32 * t.warps;
     const int occ = blocks_per_sm(fn, dev, optin, threads, smem);
     if (occ < 1) return QG_EUNSUPPORTED;
+    // Groups are dealt to CTAs round-robin: every CTA up to one per group has work.
     const int64_t ngroups = (n_out + t.rpw - 1) / t.rpw;
-    const int64_t need = (ngroups + t.warps - 1) / t.warps;
     int64_t grid = int64_t(sms) * std::min(t.ctas, occ);
-    if (need < grid) grid = need;
+    if (ngroups < grid) grid = ngroups;
     if (grid > kMaxGrid) grid = kMaxGrid;
     if (grid < 1) grid = 1;
     plan->fn = fn;
@@ -179,13 +180,66 @@ qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argma
     return QG_OK;
 }
 
-void fill_common(KernelArgs& a, const Plan& p, int fmt, const void* W, int64_t n_out, int64_t n_in,
-                 const float* x, float* y) {
-    a.W = static_cast<const uint8_t*>(W);
+// cuTensorMapEncodeTiled, fetched from the driver through the runtime once
+// (the library links only the runtime).  Encoding is a host-only computation.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return EncodeTiledFn(nullptr);
+        }
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// The packed matrix as a 2-D tensor of 8-byte elements: dim 0 = one row
+// (row stride / 8 elements), dim 1 = the n_out rows; one box = one full step of
+// rpw rows, so the box's rows land in shared memory one full step apart.
+// Elements outside the tensor (rows >= n_out, bytes past a row's short last
+// step, or past a row shorter than one step) are not read and arrive as zeros.
+// The last map built on this thread is reused when the same matrix and box come again.
+qg_status encode_weight_map(CUtensorMap* map, int fmt, const void* W, int64_t n_out, int64_t n_in, int rpw) {
+    struct Key {
+        const void* W; int64_t n_out, n_in; int fmt, rpw;
+        bool operator==(const Key& o) const {
+            return W == o.W && n_out == o.n_out && n_in == o.n_in && fmt == o.fmt && rpw == o.rpw;
+        }
+    };
+    thread_local Key last{nullptr, 0, 0, -1, 0};
+    thread_local CUtensorMap last_map;
+    const Key k{W, n_out, n_in, fmt, rpw};
+    if (k == last) { *map = last_map; return QG_OK; }
+    const EncodeTiledFn enc = encode_tiled();
+    if (!enc) return QG_ECUDA;
+    const int64_t stride = row_stride(fmt, n_in);
+    const cuuint64_t dims[2] = {cuuint64_t(stride / 8), cuuint64_t(n_out)};
+    const cuuint64_t strides[1] = {cuuint64_t(stride)};
+    const cuuint32_t box[2] = {cuuint32_t(full_step_bytes(fmt) / 8), cuuint32_t(rpw)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(W), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return QG_ECUDA;
+    last = k;
+    last_map = *map;
+    return QG_OK;
+}
+
+qg_status fill_common(KernelArgs& a, const Plan& p, int fmt, const void* W, int64_t n_out, int64_t n_in,
+                      const float* x, float* y) {
+    const qg_status st = encode_weight_map(&a.wmap, fmt, W, n_out, n_in, p.tile.rpw);
+    if (st != QG_OK) return st;
     a.x = x;
     a.y = y;
     a.status = p.status;
-    a.stride = row_stride(fmt, n_in);
     a.n_out = int(n_out);
     a.n_in = int(n_in);
     a.depth = p.tile.depth;
@@ -193,6 +247,8 @@ void fill_common(KernelArgs& a, const Plan& p, int fmt, const void* W, int64_t n
     a.drain_limit = std::max<uint32_t>(a.wait_limit, 1u << 16);
     a.test_extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
     a.fmagic = 0x4B000000u;
+    a.stage_tx = uint32_t(p.tile.rpw * full_step_bytes(fmt));
+    return QG_OK;
 }
 
 qg_status check_common(int fmt, const void* W, int64_t n_out, int64_t n_in, const float* x, int ntok) {
@@ -266,7 +322,8 @@ qg_status qgemv(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, const fl
     st = plan_launch(fmt, n_out, n_in, ntok, false, &p);
     if (st != QG_OK) return st;
     KernelArgs a{};
-    fill_common(a, p, fmt, W, n_out, n_in, x, y);
+    st = fill_common(a, p, fmt, W, n_out, n_in, x, y);
+    if (st != QG_OK) return st;
     return launch(p, a, stream);
 }
 
@@ -287,7 +344,8 @@ qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, c
     st = plan_launch(fmt, n_out, n_in, ntok, true, &p);
     if (st != QG_OK) return st;
     KernelArgs a{};
-    fill_common(a, p, fmt, W, n_out, n_in, x, y);
+    st = fill_common(a, p, fmt, W, n_out, n_in, x, y);
+    if (st != QG_OK) return st;
     a.argmax = argmax;
     a.ticket = static_cast<unsigned int*>(workspace);
     a.partials = reinterpret_cast<ArgmaxPartial*>(static_cast<uint8_t*>(workspace) + 16);
@@ -397,13 +455,14 @@ extern "C" qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_o
     const size_t need = 16 + size_t(p.grid) * size_t(ntok) * sizeof(ArgmaxPartial);
     if (need > kNoAllocScratchBytes) return QG_EWORKSPACE;
 
+    KernelArgs a{};
+    st = fill_common(a, p, fmt, W, n_out, n_in, x, y);
+    if (st != QG_OK) return st;
     // The array keeps whatever the last call left; the ticket must start at zero.
     if (cudaMemsetAsync(scratch, 0, 16, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return QG_ECUDA;
     }
-    KernelArgs a{};
-    fill_common(a, p, fmt, W, n_out, n_in, x, y);
     a.argmax = argmax;
     a.ticket = static_cast<unsigned int*>(scratch);
     a.partials = reinterpret_cast<ArgmaxPartial*>(static_cast<uint8_t*>(scratch) + 16);

@@ -10,13 +10,17 @@
 //  * Persistent grid (a few CTAs per SM).  Each CTA stages x once, in fp32,
 //    in shared memory with an XOR swizzle that makes the lanes' reads
 //    conflict-free, so x never costs HBM traffic after the first read.
-//  * Weights move HBM -> shared memory by TMA bulk copies
-//    (cp.async.bulk, completion counted on an mbarrier), never through
-//    registers: each warp owns a ring of `depth` stages, a stage holds one
-//    512-byte code step (plus its scales) of each of the warp's RPW rows, so
-//    the bytes in flight per SM are set by shared memory, not by registers.
-//    Every weight byte is copied exactly once.  One flat pipeline runs across
-//    row-group boundaries, so the copies never drain between groups.
+//  * Weights move HBM -> shared memory by TMA tensor copies
+//    (cp.async.bulk.tensor.2d, completion counted on an mbarrier), never
+//    through registers: each warp owns a ring of `depth` stages, a stage holds
+//    one 512-byte code step (plus its scales) of each of the warp's RPW rows,
+//    fetched as ONE box of RPW rows x one step (the tensor map views the packed
+//    matrix as [n_out][row stride / 8] 8-byte elements), so one thread issues
+//    one copy per step whatever RPW is.  Rows past n_out and the bytes past a
+//    short last step are outside the tensor and arrive as zeros without being
+//    read.  The bytes in flight per SM are set by shared memory, not by
+//    registers, and every weight byte is read exactly once.  One flat pipeline
+//    runs across row-group boundaries, so the copies never drain between groups.
 //  * Dequantization in registers without I2F: a code is placed in the
 //    mantissa of 2^23 (byte permute or mask) and the offset is removed with an
 //    exact packed FADD (add.rn.f32x2).  4-bit codes at nibble position 4m of a
@@ -42,6 +46,7 @@
 //    copies it already issued, and the kernel runs to its normal exit.
 #pragma once
 
+#include <cuda.h>            // CUtensorMap (type only; the library does not link the driver API)
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -59,14 +64,14 @@ constexpr unsigned kStatusWaitTimeout = 1u;
 struct ArgmaxPartial { float v; int i; };
 
 struct KernelArgs {
-    const uint8_t* W;          // device layout, rows of `stride` bytes
+    CUtensorMap wmap;          // the packed weights as a 2-D tensor [n_out][stride / 8] of 8-byte
+                               // elements, box = one full step x RPW rows, zero fill outside
     const float* x;            // [ntok][n_in]
     float* y;                  // [ntok][n_out], may be null for argmax-only
     int* argmax;               // [ntok] (argmax kernels)
     ArgmaxPartial* partials;   // [gridDim.x][ntok] (argmax kernels)
     unsigned int* ticket;      // zero on entry, left zero on exit (argmax kernels)
     unsigned int* status;      // device status word (bit 0: a bounded wait gave up)
-    long long stride;
     int n_out;
     int n_in;
     int depth;                 // ring stages per warp
@@ -74,6 +79,7 @@ struct KernelArgs {
     uint32_t drain_limit;      // polls per wait while draining after giving up
     uint32_t test_extra_tx;    // test hook: bytes added to the first expected transaction of
                                // every warp, so that wait can never complete (0 = off)
+    uint32_t stage_tx;         // bytes one box delivers: RPW x full step (zero fill included)
     uint32_t fmagic;           // 0x4B000000, the bits of 2^23; passed in so that the nibble
                                // extraction (h & mask) | magic is one LOP3 with the mask as
                                // its only immediate
@@ -112,10 +118,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
     return false;
 }
 
-// Bulk copy global -> this CTA's shared memory, completion counted on `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+// Tensor copy of the box at element coordinates (x, y) of the 2-D tensor map at
+// `map` (a kernel parameter) into this CTA's shared memory, completion counted
+// on `bar`.  x * 8 bytes is a multiple of 16 (x is a multiple of a step's
+// element count, and steps are multiples of 16 bytes).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
@@ -270,6 +280,13 @@ struct SmemPlan {
     int x_bytes, bar_off, ring_off, total;
 };
 
+// One ring stage: RPW rows of one full step, rounded up to 128 bytes (tensor
+// copies land on 128-byte boundaries).
+__host__ __device__ constexpr int full_step(int fmt) {
+    return int(kStepCodeBytes) + (fmt == QG_Q8_0 ? 32 : fmt == QG_BF16 ? 0 : 64);
+}
+__host__ __device__ constexpr int stage_bytes(int fmt, int rpw) { return (rpw * full_step(fmt) + 127) / 128 * 128; }
+
 __host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int rpw, int depth, int warps) {
     SmemPlan p;
     const int w = fmt == QG_Q8_0 ? 16 : fmt == QG_BF16 ? 8 : 32;
@@ -277,15 +294,16 @@ __host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int r
     p.x_bytes = (n_in / w) * (ntok * slots + 1) * 16;
     p.bar_off = (p.x_bytes + 15) / 16 * 16;
     p.ring_off = (p.bar_off + warps * depth * 8 + 127) / 128 * 128;
-    const int step = int(kStepCodeBytes) + (fmt == QG_Q8_0 ? 32 : fmt == QG_BF16 ? 0 : 64);
-    p.total = p.ring_off + warps * depth * rpw * step;
+    // + 128: the kernel rounds the ring's shared-memory ADDRESS up to 128 bytes
+    // (the dynamic shared memory base itself may be less aligned).
+    p.total = p.ring_off + warps * depth * stage_bytes(fmt, rpw) + 128;
     return p;
 }
 
 // ------------------------------------------------------------------------------ kernel
 
 template <int FMT, int NTOK, int RPW, bool ARGMAX>
-__global__ void __launch_bounds__(512, 1) qgemv_kernel(const KernelArgs a) {
+__global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ KernelArgs a) {
     using F = Fmt<FMT>;
     constexpr int S = F::kW / 4;                    // x float4 slots per chunk
     constexpr int V = RPW * NTOK;                   // outputs per row group
@@ -293,6 +311,9 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const KernelArgs a) {
     constexpr int LG = Log2<VP>::value;
     constexpr int SPAN = 32 / VP;                   // lanes sharing one reduced value
     constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
+    constexpr int kStage = stage_bytes(FMT, RPW);   // ring stage: RPW rows of one step
+    constexpr int kBoxX = kFullStep / 8;            // 8-byte tensor elements per step
+    static_assert(kFullStep == full_step(FMT) && kFullStep % 16 == 0, "step size");
 
     extern __shared__ __align__(128) unsigned char smem[];
     const int n_in = a.n_in;
@@ -301,14 +322,16 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const KernelArgs a) {
     const int codes = FMT == QG_Q8_0 ? n_in : FMT == QG_BF16 ? 2 * n_in : n_in / 2;
     const int spr = (codes + 511) >> 9;             // steps per row
     const int last_codes = codes - 512 * (spr - 1);
-    const int last_bytes = (last_codes + last_codes * F::kStepScale / 512 + 15) & ~15;
     const int depth = a.depth;
     const uint32_t limit = a.wait_limit;
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    const int gw = blockIdx.x * nwarps + warp;
+    // Row groups go round-robin over the CTAs first (group g -> CTA g mod grid), so
+    // every SM gets an equal share (within one group) even when the groups do not
+    // fill the warps evenly; warp w of CTA b takes groups b + grid * (w + nwarps * k).
+    const int gw = blockIdx.x + gridDim.x * warp;
     const int GW = gridDim.x * nwarps;
     const int ngroups = (a.n_out + RPW - 1) / RPW;
 
@@ -317,26 +340,23 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const KernelArgs a) {
     float4* xs = reinterpret_cast<float4*>(smem);   // [nchunks][kCS]
     const uint32_t xs_base = smem_addr(smem);
     const uint32_t bars = smem_addr(smem + plan.bar_off) + warp * depth * 8;
-    const uint32_t ring = smem_addr(smem + plan.ring_off) + warp * depth * RPW * kFullStep;
+    const uint32_t ring = ((smem_addr(smem + plan.ring_off) + 127u) & ~127u) + uint32_t(warp * depth * kStage);
 
     // ---- issue side of the warp's ring: runs `depth` steps ahead of the compute side
     int gi = gw, ki = 0, si = 0;                   // group, step in row, stage
     uint32_t issued = 0;
     bool failed = false;
-    // Lane 0 announces the step's bytes on the stage's mbarrier, then lanes
-    // 0..RPW-1 each start the bulk copy of one row in the same instruction.
+    // Lane 0 announces the stage's bytes on its mbarrier and starts one tensor
+    // copy of the box (RPW rows x one step).  A box always completes in full:
+    // rows past n_out and the bytes past a short last step arrive as zeros.
+    // (gi * RPW < n_out <= 2^31 - 1 for every issued group, so it fits an int.)
     auto issue = [&]() {
         if (gi < ngroups && !failed) {
-            const uint32_t bar = bars + si * 8;
-            const int bytes = (ki == spr - 1) ? last_bytes : kFullStep;
-            const long long row0 = (long long)gi * RPW;
-            const int nrows = (a.n_out - row0) < RPW ? int(a.n_out - row0) : RPW;
-            if (lane == 0)
-                mbar_arrive_expect_tx(bar, uint32_t(bytes * nrows) + (issued == 0 ? a.test_extra_tx : 0u));
-            __syncwarp();
-            if (lane < nrows)
-                bulk_g2s(ring + (si * RPW + lane) * kFullStep,
-                         a.W + (row0 + lane) * a.stride + (long long)ki * kFullStep, uint32_t(bytes), bar);
+            if (lane == 0) {
+                const uint32_t bar = bars + si * 8;
+                mbar_arrive_expect_tx(bar, a.stage_tx + (issued == 0 ? a.test_extra_tx : 0u));
+                tma_load_2d(ring + uint32_t(si * kStage), &a.wmap, ki * kBoxX, gi * RPW, bar);
+            }
             ++issued;
         }
         if (++ki == spr) { ki = 0; gi += GW; }
@@ -427,7 +447,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const KernelArgs a) {
         const int codes_k = (kc == spr - 1) ? last_codes : 512;
         if (16 * lane < codes_k) {
             const uint32_t xr = x_lane + uint32_t(kc) * (32u * kCS * 16u);
-            const uint32_t stage = uint32_t(sc) * (RPW * kFullStep);
+            const uint32_t stage = uint32_t(sc) * uint32_t(kStage);
             uint4 qv[RPW];
             uint32_t sv[RPW];
 #pragma unroll
@@ -534,7 +554,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const KernelArgs a) {
 
     if (failed) {
         // Report, then drain (bounded) every copy this warp issued but did not consume,
-        // so no bulk copy is still writing this CTA's shared memory when it exits.
+        // so no TMA copy is still writing this CTA's shared memory when it exits.
         if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
         for (uint32_t f = consumed; f < issued; ++f) {
             mbar_wait(bars + sc * 8, phase, a.drain_limit);

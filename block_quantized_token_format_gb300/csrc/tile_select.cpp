@@ -18,7 +18,7 @@
 
 namespace qg {
 
-bool rpw_ok(int v) { return v == 1 || v == 2 || v == 4; }
+bool rpw_ok(int v) { return v == 1 || v == 2 || v == 4 || v == 8; }
 bool depth_ok(int v) { return v >= 2 && v <= 16; }
 
 namespace {
@@ -36,38 +36,41 @@ struct Entry {
 // in profiles/).  First match wins.
 const Entry kTable[] = {
     // Q8_0, n_in 2560: LM heads
-    {QG_Q8_0, 65536, INT64_MAX, 2560, 1, {4, 3, 12, 2}},
-    {QG_Q8_0, 65536, INT64_MAX, 2560, 2, {4, 2, 16, 1}},
-    {QG_Q8_0, 65536, INT64_MAX, 2560, 0, {4, 5, 16, 1}},
-    // Q8_0, n_in 2560: 9000..65535 rows (the 10240 / 12288 projections)
-    {QG_Q8_0, 11264, 65535, 2560, 1, {4, 3, 8, 3}},
-    {QG_Q8_0, 11264, 65535, 2560, 2, {4, 5, 4, 3}},
-    {QG_Q8_0, 11264, 65535, 2560, 3, {4, 7, 12, 1}},
-    {QG_Q8_0, 11264, 65535, 2560, 4, {4, 2, 12, 1}},
-    {QG_Q8_0, 9000, 11263, 2560, 1, {4, 3, 12, 2}},
-    {QG_Q8_0, 9000, 11263, 2560, 0, {4, 7, 12, 1}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 1, {8, 5, 8, 1}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 2, {8, 2, 16, 1}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 3, {4, 3, 16, 1}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 4, {4, 2, 16, 1}},
+    // Q8_0, n_in 2560: 11264..65535 rows (the 12288 projection)
+    {QG_Q8_0, 11264, 65535, 2560, 1, {4, 2, 12, 2}},
+    {QG_Q8_0, 11264, 65535, 2560, 2, {8, 2, 4, 3}},
+    {QG_Q8_0, 11264, 65535, 2560, 0, {4, 2, 12, 1}},
+    // Q8_0, n_in 2560: 9000..11263 rows (the 10240 projection)
+    {QG_Q8_0, 9000, 11263, 2560, 1, {8, 2, 4, 3}},
+    {QG_Q8_0, 9000, 11263, 2560, 2, {8, 2, 8, 2}},
+    {QG_Q8_0, 9000, 11263, 2560, 0, {4, 2, 12, 1}},
     // Q8_0, n_in 2560: 4096..8999 rows (the 6144 projection)
-    {QG_Q8_0, 4096, 8999, 2560, 1, {4, 5, 4, 3}},
-    {QG_Q8_0, 4096, 8999, 2560, 2, {4, 5, 8, 2}},
+    {QG_Q8_0, 4096, 8999, 2560, 1, {4, 2, 16, 1}},
+    {QG_Q8_0, 4096, 8999, 2560, 4, {4, 2, 16, 1}},
     {QG_Q8_0, 4096, 8999, 2560, 0, {4, 2, 12, 1}},
     // Q8_0, n_in 2560: up to 4095 rows (2560 x 2560)
-    {QG_Q8_0, 1, 4095, 2560, 1, {1, 5, 12, 2}},
-    {QG_Q8_0, 1, 4095, 2560, 2, {4, 5, 8, 2}},
-    {QG_Q8_0, 1, 4095, 2560, 0, {2, 5, 12, 1}},
+    {QG_Q8_0, 1, 4095, 2560, 1, {2, 5, 16, 1}},
+    {QG_Q8_0, 1, 4095, 2560, 2, {2, 2, 16, 1}},
+    {QG_Q8_0, 1, 4095, 2560, 0, {2, 3, 16, 1}},
     // Q8_0, n_in 6144, few rows (6144 -> 2560)
-    {QG_Q8_0, 1, 8191, 6144, 1, {1, 8, 12, 2}},
-    {QG_Q8_0, 1, 8191, 6144, 0, {2, 8, 12, 1}},
+    {QG_Q8_0, 1, 8191, 6144, 1, {2, 5, 12, 2}},
+    {QG_Q8_0, 1, 8191, 6144, 4, {2, 5, 16, 1}},
+    {QG_Q8_0, 1, 8191, 6144, 0, {2, 5, 12, 1}},
     // Q4_0 and BF16, 8192 x 2560
-    {QG_Q4_0, 4096, 65535, 2560, 1, {4, 5, 8, 2}},
+    {QG_Q4_0, 4096, 65535, 2560, 1, {8, 5, 4, 3}},
     {QG_Q4_0, 4096, 65535, 2560, 2, {4, 2, 8, 2}},
-    {QG_Q4_0, 4096, 65535, 2560, 3, {4, 3, 8, 2}},
-    {QG_Q4_0, 4096, 65535, 2560, 4, {4, 3, 16, 1}},
-    {QG_BF16, 4096, 65535, 2560, 1, {4, 5, 8, 2}},
+    {QG_Q4_0, 4096, 65535, 2560, 3, {4, 2, 8, 2}},
+    {QG_Q4_0, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
+    {QG_BF16, 4096, 65535, 2560, 1, {8, 5, 8, 1}},
     {QG_BF16, 4096, 65535, 2560, 2, {4, 5, 8, 2}},
-    {QG_BF16, 4096, 65535, 2560, 3, {4, 3, 8, 2}},
+    {QG_BF16, 4096, 65535, 2560, 3, {4, 3, 16, 1}},
     {QG_BF16, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
     // affine 4-bit LM head
-    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {4, 5, 16, 1}},
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {8, 2, 16, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {4, 2, 16, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 0, {4, 3, 16, 1}},
 };
@@ -82,20 +85,22 @@ Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
         if (e.ntok && e.ntok != ntok) continue;
         return e.tile;
     }
-    // Heuristic for unmeasured shapes: many rows stream 4 per warp in one 16-warp
-    // CTA per SM with a shallow ring (bandwidth-bound); few rows use fewer rows per
-    // warp, deeper rings and 12-warp CTAs so the short kernel still fills the GPU.
+    // Heuristic for unmeasured shapes: many rows stream 4 per warp (8 at ntok 1) in
+    // one 12- or 16-warp CTA per SM with a shallow ring; few rows use 2 rows per warp
+    // so that the row groups still spread over every SM.
     Tile t;
-    if (n_out >= 65536) {
+    if (n_out >= 65536 && ntok == 1) {
+        t = {8, 2, 16, 1};
+    } else if (n_out >= 65536) {
         t = {4, 2, 16, 1};
     } else if (n_out >= 8192) {
-        t = {4, 3, 12, 1};
+        t = {4, 2, 12, 1};
     } else if (n_out >= 4096) {
-        t = {2, 5, 12, 1};
+        t = {4, 2, 16, 1};
     } else {
-        t = {1, 6, 12, 2};
+        t = {2, 3, 16, 1};
     }
-    (void)n_in; (void)ntok;
+    (void)n_in;
     return t;
 }
 

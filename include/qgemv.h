@@ -169,7 +169,8 @@ qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t
  * rules are the prior art).  The reduction order never depends on this choice.
  *
  * qg_set_tile_override: force a geometry for later calls, e.g.
- * "rpw=4,depth=4,warps=8,ctas=2" (any subset of the keys; rpw in {1,2,4},
+ * "rpw=4,depth=4,warps=8,ctas=2" (any subset of the keys; rpw in {1,2,4,8}, 8 only
+ * for ntok = 1, or ntok = 2 with Q8_0 and BF16 (QG_EUNSUPPORTED otherwise),
  * depth in {2..16}, warps in {1..16}, ctas in {1..8}; the ring depth and then
  * the warp count are lowered if the CTA would not fit in shared memory).
  * NULL or "" clears it.  The environment variable QGEMV_TILE, read at the
@@ -197,7 +198,7 @@ qg_status qg_describe_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, int ntok,
 qg_status qg_set_launch_options(unsigned int flags);
 
 /* ------------------------------------------------------------ device status
- * Every wait inside the kernels (on the mbarrier that counts a bulk copy into
+ * Every wait inside the kernels (on the mbarrier that counts a TMA copy into
  * shared memory) is bounded.  If a wait gives up, the kernel sets
  * QG_DEVICE_WAIT_TIMEOUT in a per-device status word, stops issuing copies,
  * drains the copies it already issued (again bounded) and exits normally; its

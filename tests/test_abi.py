@@ -71,7 +71,7 @@ def test_argmax_rejects_before_launch():
 
 def test_tile_override_grammar():
     lib = qg.load_library()
-    for good in (b"rpw=4", b"depth=2,rpw=1", b"rpw=2,depth=4,warps=8,ctas=2", b"", None, b"rpw=1,"):
+    for good in (b"rpw=4", b"depth=2,rpw=1", b"rpw=2,depth=4,warps=8,ctas=2", b"", None, b"rpw=1,", b"rpw=8"):
         assert lib.qg_set_tile_override(good) == 0, good
     for bad in (b"rpw=3", b"depth=1", b"depth=17", b"warps=0", b"warps=17", b"ctas=0", b"foo=1", b"rpw", b"rpw=x",
                 b"rpw=-1", b"pf=2"):

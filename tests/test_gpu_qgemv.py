@@ -135,11 +135,43 @@ def test_tile_choice_does_not_change_bits(fmt):
     base = {ntok: gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok]) for ntok in (1, 3)}
     try:
         for spec in ["rpw=1,depth=2", "rpw=1,depth=4,warps=4", "rpw=2,depth=2,warps=2,ctas=1",
-                     "rpw=2,depth=8", "rpw=4,depth=3,warps=8,ctas=2", "rpw=4,depth=16,warps=1"]:
+                     "rpw=2,depth=8", "rpw=4,depth=3,warps=8,ctas=2", "rpw=4,depth=16,warps=1",
+                     "rpw=8,depth=2", "rpw=8,depth=5,warps=4,ctas=3"]:
             qg.qg_set_tile_override(spec)
-            for ntok in (1, 3):
+            for ntok in ((1,) if "rpw=8" in spec else (1, 3)):   # 8 rows per warp: ntok 1 (and 2)
                 y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
                 assert np.array_equal(y.view(np.uint32), base[ntok].view(np.uint32)), (fmt, spec, ntok)
+    finally:
+        qg.qg_set_tile_override(None)
+
+
+RPW8_NTOKS = {"q8_0": (1, 2), "q4_0": (1,), "affine4_g64": (1,), "bf16": (1, 2)}
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n_out,n_in_base", [(1, 64), (13, 320), (1537, 2560), (64, 12288)])
+def test_multi_row_boxes_ragged(fmt, n_out, n_in_base):
+    """rpw = 2, 4, 8: one tensor-copy box of rpw rows per step, partly past n_out
+    (zero filled) and, for rows shorter than a step or a short last step, partly
+    past the row's bytes; the rows must still land one full step apart."""
+    n_in = n_in_for(fmt, n_in_base)
+    W = workloads.gaussian(n_out * 11 + n_in, (n_out, n_in), 0.02)
+    x = workloads.gaussian(n_out + 3 * n_in, (4, n_in))
+    canon = ORC.quantize(fmt, W)
+    packed = upload(fmt, canon, n_out, n_in)
+    ref = ORC.gemv(fmt, canon, n_out, n_in, x)
+    den = ORC.gemv_abs(fmt, canon, n_out, n_in, x)
+    try:
+        for spec in ("rpw=2,depth=3,warps=1", "rpw=4,depth=2,warps=3", "rpw=8,depth=2,warps=1",
+                     "rpw=8,depth=4,warps=16,ctas=1"):
+            qg.qg_set_tile_override(spec)
+            for ntok in (RPW8_NTOKS[fmt] if "rpw=8" in spec else (1, 2, 3, 4)):
+                y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
+                check_close(y, ref[:ntok], den[:ntok], f"{fmt} {n_out}x{n_in} ntok={ntok} {spec}")
+        qg.qg_set_tile_override("rpw=8")
+        with pytest.raises(qg.QGError) as e:       # not instantiated: refused, nothing launched
+            gpu_qgemv(fmt, packed, n_out, n_in, np.repeat(x[:1], 3, axis=0))
+        assert e.value.status == -3
     finally:
         qg.qg_set_tile_override(None)
 
