@@ -26,6 +26,9 @@
 //    exact packed FADD (add.rn.f32x2).  4-bit codes at nibble position 4m of a
 //    half-word come out as q*16^m; x is stored pre-multiplied by 16^-m (exact),
 //    so the products are q*x exactly.  Block scales are applied once per chunk.
+//    (A magic of 2^(23-4m) per nibble position would give q directly without
+//    the x pre-scale, but measured ~4% slower on the affine head: two more
+//    constant pairs and three more magic registers in the inner loop.)
 //  * FP32 math in packed pairs: per (row, token) a pair of partial sums (even
 //    and odd columns) advanced by fma.rn.f32x2, added and scaled once per
 //    chunk.  On GB300 the packed FMA does not raise the FP32 rate, but it
@@ -200,7 +203,6 @@ template <int FMT> struct Fmt;
 
 template <> struct Fmt<QG_Q8_0> {
     static constexpr int kW = 16;
-    static constexpr bool kFour = false;
     static constexpr int kStepScale = 32;
     static __device__ __forceinline__ uint32_t scale_off(int j) { return 2u * uint32_t(j >> 1); }
     static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds16(a); }
@@ -215,7 +217,6 @@ template <> struct Fmt<QG_Q8_0> {
 
 template <> struct Fmt<QG_Q4_0> {
     static constexpr int kW = 32;
-    static constexpr bool kFour = true;
     static constexpr int kStepScale = 64;
     static __device__ __forceinline__ uint32_t scale_off(int j) { return 2u * uint32_t(j); }
     static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds16(a); }
@@ -232,7 +233,6 @@ template <> struct Fmt<QG_Q4_0> {
 
 template <> struct Fmt<QG_AFFINE4_G64> {
     static constexpr int kW = 32;
-    static constexpr bool kFour = true;
     static constexpr int kStepScale = 64;
     static __device__ __forceinline__ uint32_t scale_off(int j) { return 4u * uint32_t(j >> 1); }
     static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds32(a); }
@@ -248,7 +248,6 @@ template <> struct Fmt<QG_AFFINE4_G64> {
 
 template <> struct Fmt<QG_BF16> {
     static constexpr int kW = 8;
-    static constexpr bool kFour = false;
     static constexpr int kStepScale = 0;
     static __device__ __forceinline__ uint32_t scale_off(int) { return 0u; }
     static __device__ __forceinline__ uint32_t scale(uint32_t) { return 0u; }
@@ -366,6 +365,8 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
     // Programmatic dependent launch: let the next kernel in the stream start its
     // own weight copies as soon as SMs free up (a no-op without that launch mode).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (lane == 0)   // the weight tensor map is read by this warp's first copy below
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&a.wmap)) : "memory");
 
     if (lane == 0)
         for (int s = 0; s < depth; ++s) mbar_init(bars + s * 8, 1);
@@ -379,35 +380,57 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
     // argmax workspace): wait for it to complete (a no-op without the early start).
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // ---- stage x (overlaps the first copies)
+    // ---- stage x (overlaps the first copies).  Each thread issues all its loads
+    // of a batch before its first store, so staging costs about one L2 round trip,
+    // not one per float4; token and chunk indices come from the loop structure and
+    // shifts (S is a power of two), not from divisions.
     {
         const float4* x4 = reinterpret_cast<const float4*>(a.x);
-        for (int i = threadIdx.x; i < NTOK * n4; i += blockDim.x) {
-            const int t = i / n4;
-            const int g = i - t * n4;
-            float4 v = __ldg(x4 + i);
-            if constexpr (F::kFour) {   // column j is used as q*16^(j%4): store x * 16^-(j%4)
-                v.y *= 0.0625f;
-                v.z *= 0.00390625f;
-                v.w *= 0.000244140625f;
+        constexpr int kXG = NTOK >= 8 ? 1 : 8 / NTOK;   // float4 columns per thread and batch
+        const int nt = int(blockDim.x);
+        for (int g0 = threadIdx.x; g0 < n4; g0 += kXG * nt) {
+            float4 v[kXG][NTOK];
+#pragma unroll
+            for (int j = 0; j < kXG; ++j) {
+                const int g = g0 + j * nt;
+#pragma unroll
+                for (int t = 0; t < NTOK; ++t)
+                    if (g < n4) v[j][t] = __ldg(x4 + t * n4 + g);
             }
-            const int c = g / S;
-            xs[c * kCS + t * S + (g - c * S)] = v;
+#pragma unroll
+            for (int j = 0; j < kXG; ++j) {
+                const int g = g0 + j * nt;
+                if (g < n4) {
+                    float4* dst = xs + (g / S) * kCS + (g % S);
+#pragma unroll
+                    for (int t = 0; t < NTOK; ++t) {
+                        float4 w = v[j][t];
+                        if constexpr (FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64) {
+                            // column j is used as q*16^(j%4): store x * 16^-(j%4) (exact)
+                            w.y *= 0.0625f;
+                            w.z *= 0.00390625f;
+                            w.w *= 0.000244140625f;
+                        }
+                        dst[t * S] = w;
+                    }
+                }
+            }
         }
         if constexpr (FMT == QG_AFFINE4_G64) {
             float* xf = reinterpret_cast<float*>(smem);
-            for (int i = threadIdx.x; i < NTOK * nchunks; i += blockDim.x) {
-                const int t = i / nchunks;
-                const int c = i - t * nchunks;
-                const float4* src = x4 + t * n4 + S * c;
-                float sum = 0.f;
+            for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
+#pragma unroll 1
+                for (int t = 0; t < NTOK; ++t) {
+                    const float4* src = x4 + t * n4 + S * c;
+                    float sum = 0.f;
 #pragma unroll
-                for (int q = 0; q < S; ++q) {
-                    const float4 v = __ldg(src + q);
-                    sum = __fadd_rn(sum, v.x); sum = __fadd_rn(sum, v.y);
-                    sum = __fadd_rn(sum, v.z); sum = __fadd_rn(sum, v.w);
+                    for (int q = 0; q < S; ++q) {
+                        const float4 v = __ldg(src + q);
+                        sum = __fadd_rn(sum, v.x); sum = __fadd_rn(sum, v.y);
+                        sum = __fadd_rn(sum, v.z); sum = __fadd_rn(sum, v.w);
+                    }
+                    xf[(c * kCS + NTOK * S) * 4 + t] = sum;
                 }
-                xf[(c * kCS + NTOK * S) * 4 + t] = sum;
             }
         }
     }
