@@ -14,17 +14,17 @@
 
 namespace qg {
 
-const void* kernel_lookup_fmt0(int, int, bool);
-const void* kernel_lookup_fmt1(int, int, bool);
-const void* kernel_lookup_fmt2(int, int, bool);
-const void* kernel_lookup_fmt3(int, int, bool);
+const void* kernel_lookup_fmt0(int, int, bool, bool);
+const void* kernel_lookup_fmt1(int, int, bool, bool);
+const void* kernel_lookup_fmt2(int, int, bool, bool);
+const void* kernel_lookup_fmt3(int, int, bool, bool);
 
-const void* kernel_lookup(int fmt, int ntok, int rpw, bool argmax) {
+const void* kernel_lookup(int fmt, int ntok, int rpw, bool argmax, bool split) {
     switch (fmt) {
-        case 0: return kernel_lookup_fmt0(ntok, rpw, argmax);
-        case 1: return kernel_lookup_fmt1(ntok, rpw, argmax);
-        case 2: return kernel_lookup_fmt2(ntok, rpw, argmax);
-        case 3: return kernel_lookup_fmt3(ntok, rpw, argmax);
+        case 0: return kernel_lookup_fmt0(ntok, rpw, argmax, split);
+        case 1: return kernel_lookup_fmt1(ntok, rpw, argmax, split);
+        case 2: return kernel_lookup_fmt2(ntok, rpw, argmax, split);
+        case 3: return kernel_lookup_fmt3(ntok, rpw, argmax, split);
         default: return nullptr;
     }
 }
@@ -138,6 +138,7 @@ struct Plan {
     int threads = 0;
     size_t smem = 0;
     unsigned int* status = nullptr;
+    int seg_len = 0;
 };
 
 constexpr size_t kStaticSmemReserve = 1024;   // the argmax kernels' static shared memory
@@ -149,17 +150,37 @@ qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argma
     qg_status st = device_info(&dev, &sms, &optin, &status);
     if (st != QG_OK) return st;
     Tile t = apply_override(select_tile(fmt, n_out, n_in, ntok), current_override());
-    if (!rpw_ok(t.rpw) || !depth_ok(t.depth) || t.warps < 1 || t.warps > kMaxWarps || t.ctas < 1)
+    if (!rpw_ok(t.rpw) || !depth_ok(t.depth) || t.warps < 1 || t.warps > kMaxWarps || t.ctas < 1 ||
+        t.split < 0 || t.split > kMaxSplit)
         return QG_EINVAL;
-    // Shrink the ring until the CTA fits in shared memory; x alone must fit.
+    // Split: the shape's default unless overridden, at most one segment per step;
+    // segments of L steps (the last may be shorter), none empty.  The warps of a CTA
+    // are a whole number of teams.
+    // The split is lowered until one team fits in shared memory in the worst case
+    // (ntok 4, one row per warp, a 2-stage ring), so it is the same for every ntok.
+    const int spr = int(steps_per_row(fmt, n_in));
+    int P = t.split > 0 ? t.split : select_split(fmt, n_out, n_in);
+    if (P > spr) P = spr;
+    while (P > 1 && size_t(smem_plan(fmt, kMaxNtok, int(n_in), 1, 2, P, P).total) + kStaticSmemReserve >
+                        size_t(optin))
+        --P;
+    const int L = (spr + P - 1) / P;
+    P = (spr + L - 1) / L;
+    t.split = P;
+    if (t.warps < P) t.warps = P;
+    t.warps -= t.warps % P;
+    // Shrink the ring, then the warps (whole teams), then the rows per warp until
+    // the CTA fits in shared memory; x alone must fit.
     auto total = [&](int depth, int warps) {
-        return size_t(smem_plan(fmt, ntok, int(n_in), t.rpw, depth, warps).total);
+        return size_t(smem_plan(fmt, ntok, int(n_in), t.rpw, depth, warps, P).total);
     };
-    while (total(t.depth, t.warps) + kStaticSmemReserve > size_t(optin) && t.depth > 2) --t.depth;
-    while (total(t.depth, t.warps) + kStaticSmemReserve > size_t(optin) && t.warps > 1) --t.warps;
+    auto fits = [&]() { return total(t.depth, t.warps) + kStaticSmemReserve <= size_t(optin); };
+    while (!fits() && t.depth > 2) --t.depth;
+    while (!fits() && t.warps > P) t.warps -= P;
+    while (!fits() && t.rpw > 1) t.rpw /= 2;
     const size_t smem = total(t.depth, t.warps);
     if (smem + kStaticSmemReserve > size_t(optin)) return QG_EUNSUPPORTED;
-    const void* fn = kernel_lookup(fmt, ntok, t.rpw, argmax);
+    const void* fn = kernel_lookup(fmt, ntok, t.rpw, argmax, P > 1);
     if (!fn) return QG_EUNSUPPORTED;
     const int threads = 32 * t.warps;
     const int occ = blocks_per_sm(fn, dev, optin, threads, smem);
@@ -177,6 +198,7 @@ qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argma
     plan->threads = threads;
     plan->smem = smem;
     plan->status = status;
+    plan->seg_len = L;
     return QG_OK;
 }
 
@@ -243,6 +265,8 @@ qg_status fill_common(KernelArgs& a, const Plan& p, int fmt, const void* W, int6
     a.n_out = int(n_out);
     a.n_in = int(n_in);
     a.depth = p.tile.depth;
+    a.split = p.tile.split;
+    a.seg_len = p.seg_len;
     a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
     a.drain_limit = std::max<uint32_t>(a.wait_limit, 1u << 16);
     a.test_extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);

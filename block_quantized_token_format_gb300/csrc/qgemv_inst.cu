@@ -12,11 +12,11 @@
 
 namespace qg {
 
-const void* QG_CAT(kernel_lookup_fmt, QG_INST_FMT)(int ntok, int rpw, bool argmax) {
-#define QG_E(NT, R)                                                                      \
-    if (ntok == NT && rpw == R)                                                          \
-        return argmax ? (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, true>             \
-                      : (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, false>;
+const void* QG_CAT(kernel_lookup_fmt, QG_INST_FMT)(int ntok, int rpw, bool argmax, bool split) {
+#define QG_K(NT, R, A) (split ? (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, A, true>       \
+                              : (const void*)&qgemv_kernel<QG_INST_FMT, NT, R, A, false>)
+#define QG_E(NT, R) \
+    if (ntok == NT && rpw == R) return argmax ? QG_K(NT, R, true) : QG_K(NT, R, false);
 #define QG_E_NT(NT) QG_E(NT, 1) QG_E(NT, 2) QG_E(NT, 4)
     QG_E_NT(1) QG_E_NT(2) QG_E_NT(3) QG_E_NT(4)
     QG_E(1, 8)                 // 8 rows per warp: ntok 1, and ntok 2 where it does not spill
@@ -25,6 +25,7 @@ const void* QG_CAT(kernel_lookup_fmt, QG_INST_FMT)(int ntok, int rpw, bool argma
 #endif
 #undef QG_E_NT
 #undef QG_E
+#undef QG_K
     return nullptr;
 }
 

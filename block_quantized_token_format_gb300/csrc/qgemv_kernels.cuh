@@ -78,6 +78,9 @@ struct KernelArgs {
     int n_out;
     int n_in;
     int depth;                 // ring stages per warp
+    int split;                 // warps per team: a row group's steps are split into this many
+                               // segments, one per team warp (1 = no split)
+    int seg_len;               // steps per segment (the last one may be shorter)
     uint32_t wait_limit;       // polls per mbarrier wait before giving up
     uint32_t drain_limit;      // polls per wait while draining after giving up
     uint32_t test_extra_tx;    // test hook: bytes added to the first expected transaction of
@@ -100,6 +103,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 
 __device__ __forceinline__ void mbar_fence_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -276,7 +283,7 @@ template <> struct Log2<1> { static constexpr int value = 0; };
 // NTOK*S+1 slots is odd, so the 8 lanes of a 128-byte shared-memory phase hit 8
 // distinct 16-byte bank groups, and every load offset is a compile-time constant.
 struct SmemPlan {
-    int x_bytes, bar_off, ring_off, total;
+    int x_bytes, bar_off, tbar_off, xch_off, ring_off, total;
 };
 
 // One ring stage: RPW rows of one full step, rounded up to 128 bytes (tensor
@@ -286,13 +293,20 @@ __host__ __device__ constexpr int full_step(int fmt) {
 }
 __host__ __device__ constexpr int stage_bytes(int fmt, int rpw) { return (rpw * full_step(fmt) + 127) / 128 * 128; }
 
-__host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int rpw, int depth, int warps) {
+// With a split of P > 1, each team of P warps also has four mbarriers (full and
+// empty, two parities) and an exchange area of 2 x (P - 1) x 32 floats for the
+// reduced values of its segments.
+__host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int rpw, int depth, int warps,
+                                              int split) {
     SmemPlan p;
     const int w = fmt == QG_Q8_0 ? 16 : fmt == QG_BF16 ? 8 : 32;
     const int slots = w / 4;
+    const int teams = split > 1 ? warps / split : 0;
     p.x_bytes = (n_in / w) * (ntok * slots + 1) * 16;
     p.bar_off = (p.x_bytes + 15) / 16 * 16;
-    p.ring_off = (p.bar_off + warps * depth * 8 + 127) / 128 * 128;
+    p.tbar_off = p.bar_off + warps * depth * 8;
+    p.xch_off = p.tbar_off + teams * 32;
+    p.ring_off = (p.xch_off + teams * 2 * (split - 1) * 32 * 4 + 127) / 128 * 128;
     // + 128: the kernel rounds the ring's shared-memory ADDRESS up to 128 bytes
     // (the dynamic shared memory base itself may be less aligned).
     p.total = p.ring_off + warps * depth * stage_bytes(fmt, rpw) + 128;
@@ -301,7 +315,7 @@ __host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int r
 
 // ------------------------------------------------------------------------------ kernel
 
-template <int FMT, int NTOK, int RPW, bool ARGMAX>
+template <int FMT, int NTOK, int RPW, bool ARGMAX, bool SPLIT>
 __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ KernelArgs a) {
     using F = Fmt<FMT>;
     constexpr int S = F::kW / 4;                    // x float4 slots per chunk
@@ -327,22 +341,33 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
+    // Split: the warps form teams of P; warp `seg` of a team streams steps
+    // [seg * L, min(spr, (seg + 1) * L)) of every row of the team's groups, and the
+    // team adds the segments' reduced values in segment order.  P depends only on
+    // (fmt, n_out, n_in), so the arithmetic never depends on ntok or the tile.
+    // (SPLIT = false: the kernel for P = 1, without the team exchange's registers.)
+    const int P = SPLIT ? a.split : 1, L = SPLIT ? a.seg_len : spr;
+    const int team = warp / P, seg = warp - team * P, nteams = nwarps / P;
+    const int k0 = seg * L;
+    const int k1 = (k0 + L < spr) ? k0 + L : spr;
     // Row groups go round-robin over the CTAs first (group g -> CTA g mod grid), so
     // every SM gets an equal share (within one group) even when the groups do not
-    // fill the warps evenly; warp w of CTA b takes groups b + grid * (w + nwarps * k).
-    const int gw = blockIdx.x + gridDim.x * warp;
-    const int GW = gridDim.x * nwarps;
+    // fill the teams evenly; team m of CTA b takes groups b + grid * (m + nteams * k).
+    const int gw = blockIdx.x + gridDim.x * team;
+    const int GW = gridDim.x * nteams;
     const int ngroups = (a.n_out + RPW - 1) / RPW;
 
     constexpr int kCS = NTOK * S + 1;               // float4 slots per chunk in staged x
-    const SmemPlan plan = smem_plan(FMT, NTOK, n_in, RPW, depth, nwarps);
+    const SmemPlan plan = smem_plan(FMT, NTOK, n_in, RPW, depth, nwarps, P);
     float4* xs = reinterpret_cast<float4*>(smem);   // [nchunks][kCS]
     const uint32_t xs_base = smem_addr(smem);
     const uint32_t bars = smem_addr(smem + plan.bar_off) + warp * depth * 8;
     const uint32_t ring = ((smem_addr(smem + plan.ring_off) + 127u) & ~127u) + uint32_t(warp * depth * kStage);
+    const uint32_t tbar = smem_addr(smem + plan.tbar_off) + uint32_t(team * 32);   // full[2], empty[2]
+    float* xch = reinterpret_cast<float*>(smem + plan.xch_off) + team * 2 * (P - 1) * 32;
 
     // ---- issue side of the warp's ring: runs `depth` steps ahead of the compute side
-    int gi = gw, ki = 0, si = 0;                   // group, step in row, stage
+    int gi = gw, ki = k0, si = 0;                  // group, step in row, stage
     uint32_t issued = 0;
     bool failed = false;
     // Lane 0 announces the stage's bytes on its mbarrier and starts one tensor
@@ -358,7 +383,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
             }
             ++issued;
         }
-        if (++ki == spr) { ki = 0; gi += GW; }
+        if (++ki == k1) { ki = k0; gi += GW; }
         if (++si == depth) si = 0;
     };
 
@@ -368,8 +393,15 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
     if (lane == 0)   // the weight tensor map is read by this warp's first copy below
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&a.wmap)) : "memory");
 
-    if (lane == 0)
+    if (lane == 0) {
         for (int s = 0; s < depth; ++s) mbar_init(bars + s * 8, 1);
+        if (SPLIT && P > 1 && seg == 0) {   // the team's exchange barriers; first used after __syncthreads
+            mbar_init(tbar, uint32_t(P - 1));
+            mbar_init(tbar + 8, uint32_t(P - 1));
+            mbar_init(tbar + 16, 1);
+            mbar_init(tbar + 24, 1);
+        }
+    }
     mbar_fence_init();
     __syncwarp();
     // The first copies read only W, which no earlier kernel writes (the caller's
@@ -458,8 +490,8 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
 #pragma unroll
         for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = 0ull;
 
-    int gc = gw, kc = 0, sc = 0;
-    uint32_t consumed = 0, phase = 0;
+    int gc = gw, kc = k0, sc = 0;
+    uint32_t consumed = 0, phase = 0, jg = 0;       // jg: row groups this warp has finished
     while (gc < ngroups) {
         // The decision to give up is warp-uniform: every lane leaves together.
         if (!__all_sync(kFull, mbar_wait(bars + sc * 8, phase, limit))) {
@@ -529,7 +561,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
         __syncwarp();          // every lane has read this stage before it is refilled
         issue();
         if (++sc == depth) { sc = 0; phase ^= 1u; }
-        if (++kc == spr) {
+        if (++kc == k1) {
             // ---- finish the row group: transposed warp reduction
             float v[VP];
 #pragma unroll
@@ -554,7 +586,34 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
 #pragma unroll
             for (int mask = 16 >> LG; mask >= 1; mask >>= 1) v[0] += __shfl_xor_sync(kFull, v[0], mask);
             const int vi = lane / SPAN;                       // value index this lane holds
-            if (vi < V && (lane % SPAN) == 0) {
+            const bool holder = vi < V && (lane % SPAN) == 0;
+            if (SPLIT && P > 1) {
+                // Team exchange (double-buffered by group parity, bounded waits):
+                // segments 1..P-1 publish their values, segment 0 adds them in order.
+                const int par = int(jg & 1u);
+                const uint32_t use = jg >> 1;
+                float* slot = xch + par * (P - 1) * 32;
+                if (seg > 0) {
+                    if (jg >= 2 && !__all_sync(kFull, mbar_wait(tbar + 16 + 8 * par, (use - 1) & 1u, limit))) {
+                        failed = true;
+                        break;
+                    }
+                    if (holder) slot[(seg - 1) * 32 + vi] = v[0];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tbar + 8 * par);
+                } else {
+                    if (!__all_sync(kFull, mbar_wait(tbar + 8 * par, use & 1u, limit))) {
+                        failed = true;
+                        break;
+                    }
+                    if (holder)
+                        for (int q = 0; q < P - 1; ++q) v[0] += slot[q * 32 + vi];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tbar + 16 + 8 * par);
+                }
+                ++jg;
+            }
+            if (holder && seg == 0) {
                 const int r = vi / NTOK, t = vi - r * NTOK;
                 const long long row = (long long)gc * RPW + r;
                 if (row < a.n_out) {
@@ -570,7 +629,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
             for (int r = 0; r < (kPairAcc ? RPW : 1); ++r)
 #pragma unroll
                 for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = 0ull;
-            kc = 0;
+            kc = k0;
             gc += GW;
         }
     }
@@ -639,6 +698,6 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
 }
 
 // Lookup of an instantiated kernel (defined in the per-format instantiation units).
-const void* kernel_lookup(int fmt, int ntok, int rpw, bool argmax);
+const void* kernel_lookup(int fmt, int ntok, int rpw, bool argmax, bool split);
 
 }  // namespace qg

@@ -56,10 +56,8 @@ const Entry kTable[] = {
     {QG_Q8_0, 1, 4095, 2560, 1, {2, 5, 16, 1}},
     {QG_Q8_0, 1, 4095, 2560, 2, {2, 2, 16, 1}},
     {QG_Q8_0, 1, 4095, 2560, 0, {2, 3, 16, 1}},
-    // Q8_0, n_in 6144, few rows (6144 -> 2560)
-    {QG_Q8_0, 1, 8191, 6144, 1, {2, 5, 12, 2}},
-    {QG_Q8_0, 1, 8191, 6144, 4, {2, 5, 16, 1}},
-    {QG_Q8_0, 1, 8191, 6144, 0, {2, 5, 12, 1}},
+    // Q8_0, n_in 6144, few rows (6144 -> 2560; split 3: 15 warps = 5 teams)
+    {QG_Q8_0, 1, 8191, 6144, 0, {4, 2, 16, 1}},
     // Q4_0 and BF16, 8192 x 2560
     {QG_Q4_0, 4096, 65535, 2560, 1, {8, 5, 4, 3}},
     {QG_Q4_0, 4096, 65535, 2560, 2, {4, 2, 8, 2}},
@@ -104,11 +102,26 @@ Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
     return t;
 }
 
+int select_split(int fmt, int64_t n_out, int64_t n_in) {
+    // Matrices with 8192 rows or more have row groups for every warp of the GPU
+    // (at 4 rows per warp) and short rows gain nothing from a team (measured on
+    // GB300: a split of 2-3 costs 5-20% on 6144-12288 x 2560).  Few long rows
+    // (2560 x 6144: 12 steps a row, 640 groups for 2280 warps) leave most warps
+    // idle while each active one walks its steps alone; a team of about one warp
+    // per 4 steps gains ~20% there (split 3 on 2560 x 6144).
+    const int64_t spr = steps_per_row(fmt, n_in);
+    if (n_out >= 8192 || spr <= 6) return 1;
+    int64_t p = (spr + 3) / 4;
+    if (p > kMaxSplit) p = kMaxSplit;
+    return int(p);
+}
+
 Tile apply_override(Tile t, const TileOverride& o) {
     if (o.rpw > 0) t.rpw = o.rpw;
     if (o.depth > 0) t.depth = o.depth;
     if (o.warps > 0) t.warps = o.warps;
     if (o.ctas > 0) t.ctas = o.ctas;
+    if (o.split > 0) t.split = o.split;
     return t;
 }
 
@@ -133,6 +146,7 @@ bool parse_tile_spec(const char* spec, TileOverride* out) {
         else if (key == "depth") { if (!depth_ok(v)) return false; o.depth = v; }
         else if (key == "warps") { if (v < 1 || v > 16) return false; o.warps = v; }
         else if (key == "ctas") { if (v < 1 || v > 8) return false; o.ctas = v; }
+        else if (key == "split") { if (v < 1 || v > kMaxSplit) return false; o.split = v; }
         else return false;
     }
     *out = o;
@@ -141,7 +155,8 @@ bool parse_tile_spec(const char* spec, TileOverride* out) {
 
 std::string tile_to_string(const Tile& t) {
     char b[96];
-    std::snprintf(b, sizeof b, "rpw=%d,depth=%d,warps=%d,ctas=%d", t.rpw, t.depth, t.warps, t.ctas);
+    std::snprintf(b, sizeof b, "rpw=%d,depth=%d,warps=%d,ctas=%d,split=%d", t.rpw, t.depth, t.warps, t.ctas,
+                  t.split);
     return b;
 }
 

@@ -168,17 +168,30 @@ qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t
  * with a heuristic fallback (the Track 2 audit's per-shape, per-ntok tile
  * rules are the prior art).  The reduction order never depends on this choice.
  *
+ * The split P (1..4) is chosen per (fmt, n_out, n_in) only: a row's steps are
+ * cut into P segments, one per warp of a team, and the segments' sums are added
+ * in segment order.  P fixes the reduction order, so it never depends on ntok
+ * or the geometry: for a given matrix every ntok and every geometry give
+ * bitwise the same rows.  (Vocabulary-sized heads use P = 1; projections with a
+ * few row groups per warp use about one segment per three steps.)
+ *
  * qg_set_tile_override: force a geometry for later calls, e.g.
- * "rpw=4,depth=4,warps=8,ctas=2" (any subset of the keys; rpw in {1,2,4,8}, 8 only
- * for ntok = 1, or ntok = 2 with Q8_0 and BF16 (QG_EUNSUPPORTED otherwise),
- * depth in {2..16}, warps in {1..16}, ctas in {1..8}; the ring depth and then
- * the warp count are lowered if the CTA would not fit in shared memory).
+ * "rpw=4,depth=4,warps=8,ctas=2,split=2" (any subset of the keys; rpw in
+ * {1,2,4,8}, 8 only for ntok = 1, or ntok = 2 with Q8_0 and BF16
+ * (QG_EUNSUPPORTED otherwise), depth in {2..16}, warps in {1..16}, ctas in
+ * {1..8}, split in {1..4}).  The split is capped at one segment per step and
+ * lowered until one team fits in shared memory at ntok = 4 (so it stays the
+ * same for every ntok); warps are rounded to whole teams; the ring depth, then
+ * the warp count, then the rows per warp are lowered if the CTA would not fit
+ * in shared memory.  Forcing a split changes the reduction order of that
+ * matrix (results stay within rounding of the default).
  * NULL or "" clears it.  The environment variable QGEMV_TILE, read at the
  * first call, sets the same override.  Returns QG_EINVAL on a malformed spec
  * (the override is unchanged).
  *
  * qg_describe_tile: writes the geometry a call would use into buf as
- * "rpw=..,depth=..,warps=..,ctas=..,grid=.." (NUL-terminated, truncated to len). */
+ * "rpw=..,depth=..,warps=..,ctas=..,split=..,grid=.." (NUL-terminated,
+ * truncated to len). */
 qg_status qg_set_tile_override(const char* spec);
 qg_status qg_describe_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, int ntok,
                            char* buf, size_t len);

@@ -163,7 +163,9 @@ def test_multi_row_boxes_ragged(fmt, n_out, n_in_base):
     den = ORC.gemv_abs(fmt, canon, n_out, n_in, x)
     try:
         for spec in ("rpw=2,depth=3,warps=1", "rpw=4,depth=2,warps=3", "rpw=8,depth=2,warps=1",
-                     "rpw=8,depth=4,warps=16,ctas=1"):
+                     "rpw=8,depth=4,warps=16,ctas=1", "rpw=1,depth=2,warps=1,split=1",
+                     "rpw=2,depth=3,warps=4,split=2", "rpw=4,depth=2,warps=9,split=3",
+                     "rpw=1,depth=3,warps=16,ctas=2,split=4"):
             qg.qg_set_tile_override(spec)
             for ntok in (RPW8_NTOKS[fmt] if "rpw=8" in spec else (1, 2, 3, 4)):
                 y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
@@ -172,6 +174,37 @@ def test_multi_row_boxes_ragged(fmt, n_out, n_in_base):
         with pytest.raises(qg.QGError) as e:       # not instantiated: refused, nothing launched
             gpu_qgemv(fmt, packed, n_out, n_in, np.repeat(x[:1], 3, axis=0))
         assert e.value.status == -3
+    finally:
+        qg.qg_set_tile_override(None)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_split_is_fixed_per_shape_and_token_invariant(fmt):
+    """A row's steps may be split over a team of warps.  The split is chosen from
+    (fmt, n_out, n_in) only, so every ntok gives the ntok=1 bits; a forced split
+    changes the addition order (close to the oracle), never correctness."""
+    n_out, n_in = 777, n_in_for(fmt, 6144)
+    W = workloads.gaussian(31, (n_out, n_in), 0.02)
+    x = workloads.activations(31, n_in, 4)
+    canon = ORC.quantize(fmt, W)
+    packed = upload(fmt, canon, n_out, n_in)
+    ref = ORC.gemv(fmt, canon, n_out, n_in, x)
+    den = ORC.gemv_abs(fmt, canon, n_out, n_in, x)
+    assert ",split=" in qg.qg_describe_tile(fmt, n_out, n_in, 1)
+    splits = {qg.qg_describe_tile(fmt, n_out, n_in, t).split("split=")[1].split(",")[0] for t in (1, 2, 3, 4)}
+    assert len(splits) == 1, splits
+    singles = [gpu_qgemv(fmt, packed, n_out, n_in, x[t:t + 1])[0] for t in range(4)]
+    y4 = gpu_qgemv(fmt, packed, n_out, n_in, x)
+    for t in range(4):
+        assert np.array_equal(y4[t].view(np.uint32), singles[t].view(np.uint32)), (fmt, t)
+    check_close(y4, ref, den, f"{fmt} default split")
+    try:
+        for p in (1, 2, 3, 4):
+            qg.qg_set_tile_override(f"split={p}")
+            y = gpu_qgemv(fmt, packed, n_out, n_in, x)
+            check_close(y, ref, den, f"{fmt} split={p}")
+            y1 = gpu_qgemv(fmt, packed, n_out, n_in, x[:1])
+            assert np.array_equal(y1[0].view(np.uint32), y[0].view(np.uint32)), (fmt, p)
     finally:
         qg.qg_set_tile_override(None)
 
