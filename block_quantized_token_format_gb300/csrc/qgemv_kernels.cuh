@@ -302,7 +302,9 @@ __host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int r
     const int w = fmt == QG_Q8_0 ? 16 : fmt == QG_BF16 ? 8 : 32;
     const int slots = w / 4;
     const int teams = split > 1 ? warps / split : 0;
-    p.x_bytes = (n_in / w) * (ntok * slots + 1) * 16;
+    // x holds whole steps of chunks (32 per step), zero past n_in.
+    const int codes = fmt == QG_Q8_0 ? n_in : fmt == QG_BF16 ? 2 * n_in : n_in / 2;
+    p.x_bytes = (codes + 511) / 512 * 32 * (ntok * slots + 1) * 16;
     p.bar_off = (p.x_bytes + 15) / 16 * 16;
     p.tbar_off = p.bar_off + warps * depth * 8;
     p.xch_off = p.tbar_off + teams * 32;
@@ -450,7 +452,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
         }
         if constexpr (FMT == QG_AFFINE4_G64) {
             float* xf = reinterpret_cast<float*>(smem);
-            for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {
+            for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {   // (padding chunks stay 0)
 #pragma unroll 1
                 for (int t = 0; t < NTOK; ++t) {
                     const float4* src = x4 + t * n4 + S * c;
@@ -465,6 +467,9 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
                 }
             }
         }
+        // Chunks past n_in (the lanes past a row's short last step) read as zero.
+        for (int i = nchunks * kCS + int(threadIdx.x); i < spr * 32 * kCS; i += int(blockDim.x))
+            xs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
 
@@ -490,17 +495,20 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
 #pragma unroll
         for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = 0ull;
 
-    int gc = gw, kc = k0, sc = 0;
+    int gc = gw, sc = 0;
     uint32_t consumed = 0, phase = 0, jg = 0;       // jg: row groups this warp has finished
-    while (gc < ngroups) {
+    for (; gc < ngroups; gc += GW) {
+      for (int kc = k0; kc < k1; ++kc) {
         // The decision to give up is warp-uniform: every lane leaves together.
         if (!__all_sync(kFull, mbar_wait(bars + sc * 8, phase, limit))) {
             failed = true;
             break;
         }
         ++consumed;
+        // In a row's short last step the lanes past its codes read zero-filled or
+        // scale bytes with a zero scale, against zero-padded x: they add exact zeros.
         const int codes_k = (kc == spr - 1) ? last_codes : 512;
-        if (16 * lane < codes_k) {
+        {
             const uint32_t xr = x_lane + uint32_t(kc) * (32u * kCS * 16u);
             const uint32_t stage = uint32_t(sc) * uint32_t(kStage);
             uint4 qv[RPW];
@@ -561,7 +569,9 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
         __syncwarp();          // every lane has read this stage before it is refilled
         issue();
         if (++sc == depth) { sc = 0; phase ^= 1u; }
-        if (++kc == k1) {
+      }
+      if (failed) break;
+        {
             // ---- finish the row group: transposed warp reduction
             float v[VP];
 #pragma unroll
@@ -629,8 +639,6 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
             for (int r = 0; r < (kPairAcc ? RPW : 1); ++r)
 #pragma unroll
                 for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = 0ull;
-            kc = k0;
-            gc += GW;
         }
     }
 
