@@ -84,6 +84,23 @@ def csrc_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time (all-reduce MAX); every rank gets the same value."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(step_bytes: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every replica streams step_bytes per step; the job
+    takes the slowest rank's time."""
+    return step_bytes * steps * world / (max_ms * 1e-3) / 1e9
+
+
 def algo_bytes(fmt, n_out, n_in, ntok, argmax=False):
     b = workloads_bytes(fmt, n_out, n_in) + 4 * ntok * (n_in + n_out)
     return b + (4 * ntok if argmax else 0)
@@ -311,13 +328,9 @@ def main_gpu(args, rank, world, local_rank):
     with ClockSampler(gpu_id) as clk:
         total_ms, t_wall0, t_wall1 = run(graphs, K, Wm)
     clocks = clk.summary(t_wall0, t_wall1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / K
-    value = step_bytes * K * world / (total_ms * 1e-3) / 1e9
+    value = job_gbs(step_bytes, K, world, total_ms)
 
     # --- roofline of the dominant kernel.  Every launch of the step is qgemv_kernel
     # (100% of the step's GPU time), so its average launch duration is the step time
