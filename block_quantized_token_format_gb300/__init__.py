@@ -21,7 +21,7 @@ __all__ = [
     "qg_quantize", "qg_to_device_layout", "qg_pack", "qgemv", "qgemv_argmax_workspace_bytes",
     "qgemv_argmax", "qg_set_tile_override", "qg_describe_tile", "weight_bytes", "qg_device_status",
     "qg_set_wait_limit", "QG_DEVICE_WAIT_TIMEOUT", "qgemv_argmax_noalloc", "qg_set_launch_options",
-    "QG_LAUNCH_EARLY_START",
+    "QG_LAUNCH_EARLY_START", "current_stream_handle",
 ]
 
 QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
@@ -104,6 +104,12 @@ def _stream(stream) -> int | None:
     return stream.cuda_stream or None
 
 
+def current_stream_handle() -> int:
+    """torch's current CUDA stream as a raw ``cudaStream_t`` (0 = the legacy default stream)."""
+    import torch
+    return int(torch.cuda.current_stream().cuda_stream)
+
+
 def _check(status: int, what: str) -> None:
     if status != 0:
         raise QGError(status, what)
@@ -178,11 +184,16 @@ def qg_pack(fmt, W, out: np.ndarray | None = None) -> np.ndarray:
 # ----------------------------------------------------------------------------- the mat-vec
 
 def qgemv(fmt, W, n_out: int, n_in: int, x, y, ntok: int | None = None, stream=None) -> None:
-    """Enqueue ``y[t, o] = sum_i dequant(W)[o, i] * x[t, i]`` on ``stream`` (default: torch's current)."""
+    """Enqueue ``y[t, o] = sum_i dequant(W)[o, i] * x[t, i]`` on ``stream`` (default: torch's
+    current).  ``stream`` may be a torch stream or a raw ``cudaStream_t`` as an int; passing
+    the int saves a torch lookup per call in launch-bound loops."""
     if ntok is None:
         ntok = x.shape[0] if getattr(x, "dim", lambda: 1)() == 2 else 1
-    st = load_library().qgemv(_fmt(fmt), _ptr(W), n_out, n_in, _ptr(x), _ptr(y), int(ntok), _stream(stream))
-    _check(st, "qgemv")
+    lib = _lib if _lib is not None else load_library()
+    st = lib.qgemv(FORMATS[fmt] if isinstance(fmt, str) else int(fmt), _ptr(W), n_out, n_in, _ptr(x), _ptr(y),
+                   int(ntok), stream if isinstance(stream, int) else _stream(stream))
+    if st != 0:
+        raise QGError(st, "qgemv")
 
 
 def qgemv_argmax_workspace_bytes(n_out: int, ntok: int) -> int:

@@ -51,6 +51,7 @@ std::atomic<uint32_t> g_test_extra_tx{0};
 
 // Tile override: QGEMV_TILE at first use, or qg_set_tile_override.
 std::mutex g_override_mu;
+std::atomic<uint64_t> g_override_gen{1};   // bumped whenever the override changes (plan cache key)
 TileOverride g_override;
 std::once_flag g_env_once;
 
@@ -202,6 +203,34 @@ qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argma
     return QG_OK;
 }
 
+// Plans cached per thread (a call's plan depends on the device, the shape, ntok,
+// argmax and the override; the override's generation is part of the key), so a
+// repeated call skips tile selection and the occupancy lookup.
+struct PlanKey {
+    int dev, fmt, ntok; int64_t n_out, n_in; bool argmax; uint64_t gen;
+    bool operator==(const PlanKey& o) const {
+        return dev == o.dev && fmt == o.fmt && ntok == o.ntok && n_out == o.n_out && n_in == o.n_in &&
+               argmax == o.argmax && gen == o.gen;
+    }
+};
+
+qg_status plan_launch_cached(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argmax, Plan* plan) {
+    constexpr int kSlots = 64;
+    struct Slot { bool used = false; PlanKey key; Plan plan; };
+    thread_local Slot cache[kSlots];
+    read_env_override();
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
+    const PlanKey key{dev, fmt, ntok, n_out, n_in, argmax, g_override_gen.load(std::memory_order_acquire)};
+    const uint64_t h = (uint64_t(n_out) * 0x9E3779B97F4A7C15ull) ^ (uint64_t(n_in) * 0xC2B2AE3D27D4EB4Full) ^
+                       uint64_t(fmt * 31 + ntok * 7 + (argmax ? 3 : 0) + dev * 131);
+    Slot& sl = cache[(h ^ (h >> 29)) % kSlots];
+    if (sl.used && sl.key == key) { *plan = sl.plan; return QG_OK; }
+    const qg_status st = plan_launch(fmt, n_out, n_in, ntok, argmax, plan);
+    if (st == QG_OK) { sl.used = true; sl.key = key; sl.plan = *plan; }
+    return st;
+}
+
 // cuTensorMapEncodeTiled, fetched from the driver through the runtime once
 // (the library links only the runtime).  Encoding is a host-only computation.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -227,7 +256,7 @@ EncodeTiledFn encode_tiled() {
 // rpw rows, so the box's rows land in shared memory one full step apart.
 // Elements outside the tensor (rows >= n_out, bytes past a row's short last
 // step, or past a row shorter than one step) are not read and arrive as zeros.
-// The last map built on this thread is reused when the same matrix and box come again.
+// Maps are cached per thread (32 slots) and reused when the same matrix and box come again.
 qg_status encode_weight_map(CUtensorMap* map, int fmt, const void* W, int64_t n_out, int64_t n_in, int rpw) {
     struct Key {
         const void* W; int64_t n_out, n_in; int fmt, rpw;
@@ -235,10 +264,14 @@ qg_status encode_weight_map(CUtensorMap* map, int fmt, const void* W, int64_t n_
             return W == o.W && n_out == o.n_out && n_in == o.n_in && fmt == o.fmt && rpw == o.rpw;
         }
     };
-    thread_local Key last{nullptr, 0, 0, -1, 0};
-    thread_local CUtensorMap last_map;
+    constexpr int kSlots = 32;
+    struct Slot { Key key{nullptr, 0, 0, -1, 0}; CUtensorMap map; };
+    thread_local Slot cache[kSlots];
     const Key k{W, n_out, n_in, fmt, rpw};
-    if (k == last) { *map = last_map; return QG_OK; }
+    const uint64_t h = (reinterpret_cast<uintptr_t>(W) >> 8) * 0x9E3779B97F4A7C15ull ^
+                       uint64_t(n_out) * 0xC2B2AE3D27D4EB4Full ^ uint64_t(n_in * 13 + fmt * 7 + rpw);
+    Slot& sl = cache[(h ^ (h >> 31)) % kSlots];
+    if (sl.key == k) { *map = sl.map; return QG_OK; }
     const EncodeTiledFn enc = encode_tiled();
     if (!enc) return QG_ECUDA;
     const int64_t stride = row_stride(fmt, n_in);
@@ -250,8 +283,8 @@ qg_status encode_weight_map(CUtensorMap* map, int fmt, const void* W, int64_t n_
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return QG_ECUDA;
-    last = k;
-    last_map = *map;
+    sl.key = k;
+    sl.map = *map;
     return QG_OK;
 }
 
@@ -343,7 +376,7 @@ qg_status qgemv(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, const fl
     if (!y) return QG_EINVAL;
     if (!aligned(y, 4)) return QG_EALIGN;
     Plan p;
-    st = plan_launch(fmt, n_out, n_in, ntok, false, &p);
+    st = plan_launch_cached(fmt, n_out, n_in, ntok, false, &p);
     if (st != QG_OK) return st;
     KernelArgs a{};
     st = fill_common(a, p, fmt, W, n_out, n_in, x, y);
@@ -365,7 +398,7 @@ qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, c
     if (!workspace || workspace_bytes < qgemv_argmax_workspace_bytes(n_out, ntok)) return QG_EWORKSPACE;
     if (!aligned(workspace, 16)) return QG_EALIGN;
     Plan p;
-    st = plan_launch(fmt, n_out, n_in, ntok, true, &p);
+    st = plan_launch_cached(fmt, n_out, n_in, ntok, true, &p);
     if (st != QG_OK) return st;
     KernelArgs a{};
     st = fill_common(a, p, fmt, W, n_out, n_in, x, y);
@@ -382,6 +415,7 @@ qg_status qg_set_tile_override(const char* spec) {
     if (!parse_tile_spec(spec, &o)) return QG_EINVAL;
     std::lock_guard<std::mutex> lk(g_override_mu);
     g_override = o;
+    g_override_gen.fetch_add(1);
     return QG_OK;
 }
 
@@ -472,7 +506,7 @@ extern "C" qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_o
     }
 
     Plan p;
-    st = plan_launch(fmt, n_out, n_in, ntok, true, &p);
+    st = plan_launch_cached(fmt, n_out, n_in, ntok, true, &p);
     if (st != QG_OK) return st;
     // The launch needs a ticket plus one partial per CTA and token; refuse a launch
     // geometry (possible only through a tile override) that the array cannot hold.

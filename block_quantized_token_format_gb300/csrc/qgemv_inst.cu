@@ -19,10 +19,8 @@ const void* QG_CAT(kernel_lookup_fmt, QG_INST_FMT)(int ntok, int rpw, bool argma
     if (ntok == NT && rpw == R) return argmax ? QG_K(NT, R, true) : QG_K(NT, R, false);
 #define QG_E_NT(NT) QG_E(NT, 1) QG_E(NT, 2) QG_E(NT, 4)
     QG_E_NT(1) QG_E_NT(2) QG_E_NT(3) QG_E_NT(4)
-    QG_E(1, 8)                 // 8 rows per warp: ntok 1, and ntok 2 where it does not spill
-#if QG_INST_FMT == 0 || QG_INST_FMT == 3      // Q8_0, BF16
+    QG_E(1, 8)                 // 8 rows per warp: ntok 1 and 2
     QG_E(2, 8)
-#endif
 #undef QG_E_NT
 #undef QG_E
 #undef QG_K

@@ -69,7 +69,7 @@ const Entry kTable[] = {
     {QG_BF16, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
     // affine 4-bit LM head
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {8, 2, 16, 1}},
-    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {4, 2, 16, 1}},
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {8, 2, 16, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 0, {4, 3, 16, 1}},
 };
 

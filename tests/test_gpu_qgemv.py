@@ -145,7 +145,7 @@ def test_tile_choice_does_not_change_bits(fmt):
         qg.qg_set_tile_override(None)
 
 
-RPW8_NTOKS = {"q8_0": (1, 2), "q4_0": (1,), "affine4_g64": (1,), "bf16": (1, 2)}
+RPW8_NTOKS = {"q8_0": (1, 2), "q4_0": (1, 2), "affine4_g64": (1, 2), "bf16": (1, 2)}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
