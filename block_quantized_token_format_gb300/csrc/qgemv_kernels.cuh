@@ -272,7 +272,10 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
-template <int V> struct Pow2Up { static constexpr int value = V <= 1 ? 1 : V <= 2 ? 2 : V <= 4 ? 4 : V <= 8 ? 8 : 16; };
+template <int V> struct Pow2Up {
+    static_assert(V >= 1 && V <= 32, "a warp reduces at most 32 outputs per row group");
+    static constexpr int value = V <= 1 ? 1 : V <= 2 ? 2 : V <= 4 ? 4 : V <= 8 ? 8 : V <= 16 ? 16 : 32;
+};
 template <int V> struct Log2 { static constexpr int value = V <= 1 ? 0 : 1 + Log2<V / 2>::value; };
 template <> struct Log2<1> { static constexpr int value = 0; };
 
@@ -323,6 +326,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_kernel(const __grid_constant__ K
     constexpr int S = F::kW / 4;                    // x float4 slots per chunk
     constexpr int V = RPW * NTOK;                   // outputs per row group
     constexpr int VP = Pow2Up<V>::value;
+    static_assert(VP >= V && VP <= 32, "butterfly width");
     constexpr int LG = Log2<VP>::value;
     constexpr int SPAN = 32 / VP;                   // lanes sharing one reduced value
     constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;

@@ -138,14 +138,15 @@ def test_tile_choice_does_not_change_bits(fmt):
                      "rpw=2,depth=8", "rpw=4,depth=3,warps=8,ctas=2", "rpw=4,depth=16,warps=1",
                      "rpw=8,depth=2", "rpw=8,depth=5,warps=4,ctas=3"]:
             qg.qg_set_tile_override(spec)
-            for ntok in ((1,) if "rpw=8" in spec else (1, 3)):   # 8 rows per warp: ntok 1 (and 2)
+            for ntok in ((1,) if "rpw=8" in spec else (1, 3)):   # 8 rows per warp: ntok <= 2
                 y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
                 assert np.array_equal(y.view(np.uint32), base[ntok].view(np.uint32)), (fmt, spec, ntok)
     finally:
         qg.qg_set_tile_override(None)
 
 
-RPW8_NTOKS = {"q8_0": (1, 2), "q4_0": (1, 2), "affine4_g64": (1, 2), "bf16": (1, 2)}
+# (rows per warp, ntok) pairs the library instantiates
+RPW_NTOKS = {(r, t) for r in (1, 2, 4) for t in (1, 2, 3, 4)} | {(8, 1), (8, 2), (6, 2), (6, 3), (5, 4), (3, 4)}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -163,11 +164,15 @@ def test_multi_row_boxes_ragged(fmt, n_out, n_in_base):
     den = ORC.gemv_abs(fmt, canon, n_out, n_in, x)
     try:
         for spec in ("rpw=2,depth=3,warps=1", "rpw=4,depth=2,warps=3", "rpw=8,depth=2,warps=1",
-                     "rpw=8,depth=4,warps=16,ctas=1", "rpw=1,depth=2,warps=1,split=1",
+                     "rpw=8,depth=4,warps=16,ctas=1", "rpw=3,depth=2,warps=5", "rpw=5,depth=3,warps=7",
+                     "rpw=6,depth=2,warps=11,ctas=2", "rpw=1,depth=2,warps=1,split=1",
                      "rpw=2,depth=3,warps=4,split=2", "rpw=4,depth=2,warps=9,split=3",
                      "rpw=1,depth=3,warps=16,ctas=2,split=4"):
             qg.qg_set_tile_override(spec)
-            for ntok in (RPW8_NTOKS[fmt] if "rpw=8" in spec else (1, 2, 3, 4)):
+            rpw = int(spec.split("rpw=")[1].split(",")[0])
+            for ntok in (1, 2, 3, 4):
+                if (rpw, ntok) not in RPW_NTOKS:
+                    continue
                 y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
                 check_close(y, ref[:ntok], den[:ntok], f"{fmt} {n_out}x{n_in} ntok={ntok} {spec}")
         qg.qg_set_tile_override("rpw=8")
