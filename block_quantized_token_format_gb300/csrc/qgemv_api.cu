@@ -130,6 +130,19 @@ int blocks_per_sm(const void* fn, int dev, int optin, int threads, size_t smem) 
     return n;
 }
 
+// Threads per block a kernel allows (its launch bound), cached per kernel.
+int max_threads(const void* fn) {
+    static std::mutex mu;
+    static std::map<const void*, int> cache;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(fn);
+    if (it != cache.end()) return it->second;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) { cudaGetLastError(); return 0; }
+    cache[fn] = fa.maxThreadsPerBlock;
+    return fa.maxThreadsPerBlock;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 struct Plan {
@@ -170,19 +183,34 @@ qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argma
     t.split = P;
     if (t.warps < P) t.warps = P;
     t.warps -= t.warps % P;
-    // Shrink the ring, then the warps (whole teams), then the rows per warp until
-    // the CTA fits in shared memory; x alone must fit.
+    const void* fn = kernel_lookup(fmt, ntok, t.rpw, argmax, P > 1);
+    if (!fn) return QG_EUNSUPPORTED;
+    // The kernel's thread limit (12 warps where a warp keeps more than 16 outputs).
+    auto cap_warps = [&]() {
+        const int mw = max_threads(fn) / 32;
+        if (mw < 1) return false;
+        if (t.warps > mw) t.warps = mw - mw % P;
+        return t.warps >= P;
+    };
+    if (!cap_warps()) return QG_EUNSUPPORTED;
+    // Shrink the ring, then the warps (whole teams), then the rows per warp (to the
+    // next smaller instantiated value) until the CTA fits in shared memory; x alone
+    // must fit.
     auto total = [&](int depth, int warps) {
         return size_t(smem_plan(fmt, ntok, int(n_in), t.rpw, depth, warps, P).total);
     };
     auto fits = [&]() { return total(t.depth, t.warps) + kStaticSmemReserve <= size_t(optin); };
     while (!fits() && t.depth > 2) --t.depth;
     while (!fits() && t.warps > P) t.warps -= P;
-    while (!fits() && t.rpw > 1) t.rpw /= 2;
+    while (!fits() && t.rpw > 1) {
+        int r = t.rpw - 1;
+        while (r > 1 && !kernel_lookup(fmt, ntok, r, argmax, P > 1)) --r;
+        t.rpw = r;
+        fn = kernel_lookup(fmt, ntok, t.rpw, argmax, P > 1);
+        if (!fn || !cap_warps()) return QG_EUNSUPPORTED;
+    }
     const size_t smem = total(t.depth, t.warps);
     if (smem + kStaticSmemReserve > size_t(optin)) return QG_EUNSUPPORTED;
-    const void* fn = kernel_lookup(fmt, ntok, t.rpw, argmax, P > 1);
-    if (!fn) return QG_EUNSUPPORTED;
     const int threads = 32 * t.warps;
     const int occ = blocks_per_sm(fn, dev, optin, threads, smem);
     if (occ < 1) return QG_EUNSUPPORTED;

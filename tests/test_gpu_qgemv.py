@@ -146,7 +146,8 @@ def test_tile_choice_does_not_change_bits(fmt):
 
 
 # (rows per warp, ntok) pairs the library instantiates
-RPW_NTOKS = {(r, t) for r in (1, 2, 4) for t in (1, 2, 3, 4)} | {(8, 1), (8, 2), (6, 2), (6, 3), (5, 4), (3, 4)}
+RPW_NTOKS = ({(r, t) for r in (1, 2, 4) for t in (1, 2, 3, 4)} |
+             {(8, 1), (8, 2), (8, 3), (6, 2), (6, 3), (6, 4), (5, 4), (3, 4)})
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -165,7 +166,8 @@ def test_multi_row_boxes_ragged(fmt, n_out, n_in_base):
     try:
         for spec in ("rpw=2,depth=3,warps=1", "rpw=4,depth=2,warps=3", "rpw=8,depth=2,warps=1",
                      "rpw=8,depth=4,warps=16,ctas=1", "rpw=3,depth=2,warps=5", "rpw=5,depth=3,warps=7",
-                     "rpw=6,depth=2,warps=11,ctas=2", "rpw=1,depth=2,warps=1,split=1",
+                     "rpw=6,depth=2,warps=11,ctas=2", "rpw=6,depth=2,warps=16", "rpw=8,depth=3,warps=16",
+                     "rpw=1,depth=2,warps=1,split=1",
                      "rpw=2,depth=3,warps=4,split=2", "rpw=4,depth=2,warps=9,split=3",
                      "rpw=1,depth=3,warps=16,ctas=2,split=4"):
             qg.qg_set_tile_override(spec)
@@ -177,7 +179,7 @@ def test_multi_row_boxes_ragged(fmt, n_out, n_in_base):
                 check_close(y, ref[:ntok], den[:ntok], f"{fmt} {n_out}x{n_in} ntok={ntok} {spec}")
         qg.qg_set_tile_override("rpw=8")
         with pytest.raises(qg.QGError) as e:       # not instantiated: refused, nothing launched
-            gpu_qgemv(fmt, packed, n_out, n_in, np.repeat(x[:1], 3, axis=0))
+            gpu_qgemv(fmt, packed, n_out, n_in, np.repeat(x[:1], 4, axis=0))
         assert e.value.status == -3
     finally:
         qg.qg_set_tile_override(None)
