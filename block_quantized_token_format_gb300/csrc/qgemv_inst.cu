@@ -23,7 +23,7 @@ const void* QG_CAT(kernel_lookup_fmt, QG_INST_FMT)(int ntok, int rpw, bool argma
     QG_E(2, 8)
     QG_E(2, 6) QG_E(3, 6)      // 6 rows per warp: ntok 2-3
     QG_E(4, 3) QG_E(4, 5)      // 3 and 5 rows per warp: ntok 4
-    QG_E(3, 8) QG_E(4, 6)      // more than 16 outputs: at most 12 warps, 168 registers
+    QG_E(3, 8) QG_E(4, 6)      // more than 20 outputs: at most 12 warps, 168 registers
 #undef QG_E_NT
 #undef QG_E
 #undef QG_K

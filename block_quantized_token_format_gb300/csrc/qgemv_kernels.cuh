@@ -321,13 +321,17 @@ __host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int r
 // ------------------------------------------------------------------------------ kernel
 
 // Threads per CTA a kernel allows: 512 (16 warps), or 384 (12 warps) where a warp
-// keeps more than 20 outputs per row group (8 rows at ntok 3, 6 rows at ntok 4), so
-// that each thread may hold up to 168 registers instead of 128 and the extra rows'
+// keeps more than 20 outputs per row group (8 rows at ntok 3, 6 rows at ntok 4), or
+// 16 with 4-bit codes at ntok >= 2 (whose decode needs more registers), so that each
+// thread may hold up to 168 registers instead of 128 and the extra rows'
 // accumulators do not spill.  Kernels that fit in 128 keep 16 warps.
-template <int NTOK, int RPW> struct MaxThreads { static constexpr int value = RPW * NTOK > 20 ? 384 : 512; };
+template <int FMT, int NTOK, int RPW> struct MaxThreads {
+    static constexpr bool kFourBit = FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64;
+    static constexpr int value = (RPW * NTOK > 20 || (kFourBit && RPW * NTOK >= 16 && NTOK >= 2)) ? 384 : 512;
+};
 
 template <int FMT, int NTOK, int RPW, bool ARGMAX, bool SPLIT>
-__global__ void __launch_bounds__(MaxThreads<NTOK, RPW>::value, 1) qgemv_kernel(const __grid_constant__ KernelArgs a) {
+__global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_kernel(const __grid_constant__ KernelArgs a) {
     using F = Fmt<FMT>;
     constexpr int S = F::kW / 4;                    // x float4 slots per chunk
     constexpr int V = RPW * NTOK;                   // outputs per row group

@@ -65,7 +65,7 @@ const Entry kTable[] = {
     {QG_Q8_0, 1, 8191, 6144, 0, {4, 2, 16, 1}},
     // Q4_0 and BF16, 8192 x 2560
     {QG_Q4_0, 4096, 65535, 2560, 1, {4, 2, 12, 2}},
-    {QG_Q4_0, 4096, 65535, 2560, 2, {4, 2, 8, 2}},
+    {QG_Q4_0, 4096, 65535, 2560, 2, {8, 2, 6, 2}},
     {QG_Q4_0, 4096, 65535, 2560, 3, {8, 2, 6, 2}},
     {QG_Q4_0, 4096, 65535, 2560, 4, {5, 2, 16, 1}},
     {QG_BF16, 4096, 65535, 2560, 1, {4, 5, 8, 2}},
@@ -74,7 +74,7 @@ const Entry kTable[] = {
     {QG_BF16, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
     // affine 4-bit LM head
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {8, 2, 16, 1}},
-    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {6, 2, 16, 1}},
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {8, 2, 12, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 3, {8, 2, 12, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 4, {6, 2, 12, 1}},
 };

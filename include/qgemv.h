@@ -178,8 +178,9 @@ qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t
  * qg_set_tile_override: force a geometry for later calls, e.g.
  * "rpw=4,depth=4,warps=8,ctas=2,split=2" (any subset of the keys; rpw in
  * {1,2,3,4,5,6,8}: 1, 2, 4 for every ntok, 8 for ntok <= 3, 6 for ntok 2-4,
- * 3 and 5 for ntok 4 (QG_EUNSUPPORTED otherwise); where rpw * ntok > 20 a CTA
- * has at most 12 warps; depth in {2..16}, warps in {1..16}, ctas in
+ * 3 and 5 for ntok 4 (QG_EUNSUPPORTED otherwise); where rpw * ntok > 20 (or
+ * >= 16 with 4-bit codes at ntok >= 2) a CTA has at most 12 warps; depth in
+ * {2..16}, warps in {1..16}, ctas in
  * {1..8}, split in {1..4}).  The split is capped at one segment per step and
  * lowered until one team fits in shared memory at ntok = 4 (so it stays the
  * same for every ntok); warps are rounded to whole teams; the ring depth, then
