@@ -132,10 +132,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 // `map` (a kernel parameter) into this CTA's shared memory, completion counted
 // on `bar`.  x * 8 bytes is a multiple of 16 (x is a multiple of a step's
 // element count, and steps are multiples of 16 bytes).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x, int y, uint32_t bar) {
+// The weights are read once per call: the copy carries an L2 evict-first policy so
+// that the stream does not push x, y and other recently written data out of L2.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x, int y, uint32_t bar,
+                                            uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy) : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
@@ -384,6 +394,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
 
     // ---- issue side of the warp's ring: runs `depth` steps ahead of the compute side
     int gi = gw, ki = k0, si = 0;                  // group, step in row, stage
+    const uint64_t wpolicy = l2_evict_first_policy();
     uint32_t issued = 0;
     bool failed = false;
     // Lane 0 announces the stage's bytes on its mbarrier and starts one tensor
@@ -395,7 +406,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
             if (lane == 0) {
                 const uint32_t bar = bars + si * 8;
                 mbar_arrive_expect_tx(bar, a.stage_tx + (issued == 0 ? a.test_extra_tx : 0u));
-                tma_load_2d(ring + uint32_t(si * kStage), &a.wmap, ki * kBoxX, gi * RPW, bar);
+                tma_load_2d(ring + uint32_t(si * kStage), &a.wmap, ki * kBoxX, gi * RPW, bar, wpolicy);
             }
             ++issued;
         }
