@@ -216,6 +216,26 @@ def test_split_is_fixed_per_shape_and_token_invariant(fmt):
         qg.qg_set_tile_override(None)
 
 
+def test_plan_cache_follows_the_override():
+    """Launch plans are cached per thread; every override change must reach the next
+    call.  A forced split changes the addition order (and so, here, some bits);
+    clearing the override restores the default bits exactly."""
+    fmt, n_out, n_in = "q8_0", 777, 6144          # default split 3 (12 steps a row)
+    W = workloads.gaussian(41, (n_out, n_in), 0.02)
+    x = workloads.activations(41, n_in, 4)
+    packed = upload(fmt, ORC.quantize(fmt, W), n_out, n_in)
+    base = gpu_qgemv(fmt, packed, n_out, n_in, x)
+    try:
+        qg.qg_set_tile_override("split=1")
+        forced = gpu_qgemv(fmt, packed, n_out, n_in, x)
+        assert not np.array_equal(forced.view(np.uint32), base.view(np.uint32))
+        qg.qg_set_tile_override("split=1,rpw=2")
+        assert np.array_equal(gpu_qgemv(fmt, packed, n_out, n_in, x).view(np.uint32), forced.view(np.uint32))
+    finally:
+        qg.qg_set_tile_override(None)
+    assert np.array_equal(gpu_qgemv(fmt, packed, n_out, n_in, x).view(np.uint32), base.view(np.uint32))
+
+
 def test_deterministic_and_prefix_rows():
     n_out, n_in = 4099, 2560
     W = workloads.gaussian(9, (n_out, n_in), 0.02)
