@@ -318,3 +318,40 @@ def qgemv_argmax(fmt, packed, n_out, n_in, x):
     """The fused LM-head call: fp64 logits plus first-index argmax per token."""
     y = gemv(fmt, packed, n_out, n_in, x)
     return y, argmax_first(y)
+
+
+# ----------------------------------------------------------------------------- draft vocabulary by id list
+
+def gather_rows(fmt, packed: np.ndarray, n_out: int, n_in: int, ids) -> np.ndarray:
+    """Canonical bytes of the small head made of rows ``ids`` (in that order).
+
+    [M2Max] "MTP draft vocabulary subset": the draft head scores only the listed
+    rows of the LM head, copied once into a small head.  Ids repeat freely; every
+    id must lie in ``[0, n_out)``.
+    """
+    f = fmt_id(fmt)
+    ids = np.asarray(ids, dtype=np.int64)
+    if ids.size and (ids.min() < 0 or ids.max() >= n_out):
+        raise IndexError("row id outside the head")
+    if f == AFFINE4_G64:
+        nw = n_out * n_in // 8
+        ng = n_out * n_in // 64
+        w = packed[: nw * 4].reshape(n_out, n_in // 2)[ids]
+        s = packed[nw * 4: nw * 4 + ng * 2].reshape(n_out, n_in // 32)[ids]
+        b = packed[nw * 4 + ng * 2:].reshape(n_out, n_in // 32)[ids]
+        return np.concatenate([w.reshape(-1), s.reshape(-1), b.reshape(-1)])
+    per_row = weight_bytes(f, 1, n_in)
+    return np.ascontiguousarray(packed.reshape(n_out, per_row)[ids]).reshape(-1)
+
+
+def qgemv_argmax_ids(fmt, packed, n_out, n_in, x, ids):
+    """The draft head over an id list: fp64 logits of the small head (``[ntok, len(ids)]``,
+    column j = row ``ids[j]``) and, per token, the full-vocabulary id of its first-index
+    argmax, ``ids[j*]`` ([Issue] Phase 2b: a reduced draft vocabulary plus a d2t index
+    mapping back to target ids).  Ties go to the lowest position j in the list."""
+    ids = np.asarray(ids, dtype=np.int64)
+    small = gather_rows(fmt, packed, n_out, n_in, ids)
+    y = gemv(fmt, small, ids.size, n_in, x)
+    j = argmax_first(y)
+    return y, ids[j].astype(np.int32)
+

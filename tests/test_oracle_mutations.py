@@ -37,6 +37,9 @@ MUTATIONS = {
     "gemv wrong token": ("y[t, r0:r1] = deq @ x64[t]", "y[t, r0:r1] = deq @ x64[0]"),
     "argmax last index": ("return np.argmax(yy, axis=1).astype(np.int32)",
                           "return (yy.shape[1] - 1 - np.argmax(yy[:, ::-1], axis=1)).astype(np.int32)"),
+    "draft argmax not mapped": ("return y, ids[j].astype(np.int32)", "return y, j.astype(np.int32)"),
+    "draft gather ignores affine scales": ("s = packed[nw * 4: nw * 4 + ng * 2].reshape(n_out, n_in // 32)[ids]",
+                                           "s = packed[nw * 4: nw * 4 + ng * 2].reshape(n_out, n_in // 32)[:ids.size]"),
 }
 
 

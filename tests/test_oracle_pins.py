@@ -342,10 +342,42 @@ def check_fp16_bf16_rounding(orc):
     assert list(r) == [1, 2, 3, -1, -3, 0, 8388608, -3]
 
 
+def check_draft_ids(orc):
+    """The draft head over an id list ([M2Max] "MTP draft vocabulary subset": the listed
+    rows copied once into a small head; [Issue] Phase 2b: the d2t map back to full ids)."""
+    n_out, n_in = 50, 128
+    x = workloads.gaussian(71, (2, n_in))
+    W = workloads.gaussian(72, (n_out, n_in), 0.02)
+    W[31] = np.float32(0.05) * np.sign(x[0])        # token 0's maximum, in the list
+    W[44] = np.float32(0.06) * np.sign(x[1])        # token 1's overall maximum, NOT in the list
+    W[12] = np.float32(0.04) * np.sign(x[1])        # token 1's maximum within the list
+    ids = np.array([40, 31, 3, 12, 7, 31, 0], dtype=np.int32)   # unsorted, with a repeat
+    for fmt in ("q8_0", "q4_0", "affine4_g64", "bf16"):
+        raw = orc.quantize(fmt, W)
+        full = orc.gemv(fmt, raw, n_out, n_in, x)
+        y, am = orc.qgemv_argmax_ids(fmt, raw, n_out, n_in, x, ids)
+        assert y.shape == (2, ids.size)
+        assert np.allclose(y, full[:, ids], rtol=1e-13, atol=1e-15), fmt    # column j is row ids[j]
+        assert list(am) == [31, 12], (fmt, list(am))                        # mapped back to full ids
+        # the gathered bytes decode to exactly the listed rows, in list order
+        deq = orc.dequantize(fmt, orc.gather_rows(fmt, raw, n_out, n_in, ids), ids.size, n_in)
+        assert np.array_equal(deq, orc.dequantize(fmt, raw, n_out, n_in)[ids]), fmt
+    raw = orc.quantize("q8_0", W)
+    y0, a0 = orc.qgemv_argmax("q8_0", raw, n_out, n_in, x)           # the identity list is the full head
+    y1, a1 = orc.qgemv_argmax_ids("q8_0", raw, n_out, n_in, x, np.arange(n_out, dtype=np.int32))
+    assert np.allclose(y0, y1, rtol=1e-13, atol=1e-15) and list(a0) == list(a1)
+    try:
+        orc.gather_rows("q8_0", raw, n_out, n_in, [n_out])
+        raise AssertionError("an id past the head was accepted")
+    except IndexError:
+        pass
+
+
 ALL_CHECKS = [check_page_byte_counts, check_golden_q8_0, check_golden_q4_0, check_golden_affine4,
               check_golden_bf16, check_rounding, check_brute_force, check_idempotence,
               check_affine_constructed_roundtrip, check_linearity, check_token_independence,
-              check_cross_format, check_argmax, check_quant_error_band, check_fp16_bf16_rounding]
+              check_cross_format, check_argmax, check_quant_error_band, check_fp16_bf16_rounding,
+              check_draft_ids]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)

@@ -56,6 +56,10 @@ WORKLOADS: dict[str, Workload] = {w.name: w for w in [
     Workload("affine4_head_248320x5120", "affine4_g64", 248320, 5120, 140, argmax=True),
 ]}
 
+# A draft vocabulary given as an id list (not a row prefix): 106,299 ids of the
+# 248,320-row Q8_0 head, drawn without replacement and sorted, from this seed.
+DRAFT_IDS = {"q8_0_head_248320x2560": (106299, 131)}
+
 # The dense projection set timed as one step by bench.py.
 DENSE_SET = ["q8_0_6144x2560", "q8_0_10240x2560", "q8_0_12288x2560", "q8_0_2560x6144"]
 
@@ -108,3 +112,9 @@ def gaussian(seed: int, shape, scale: float = 1.0) -> np.ndarray:
     """A generic seeded fp32 normal array for small test cases."""
     g = np.random.Generator(np.random.PCG64(seed))
     return g.standard_normal(shape, dtype=np.float32) * np.float32(scale)
+
+
+def draft_ids(seed: int, n_full: int, k: int) -> np.ndarray:
+    """k distinct row ids of an n_full-row head, drawn without replacement and sorted (int32)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    return np.sort(g.choice(n_full, size=k, replace=False)).astype(np.int32)
