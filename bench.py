@@ -486,9 +486,68 @@ def detail_table(args, qg, torch, dev, l2, peak):
         table[name] = {"fmt": w.fmt, "n_out": w.n_out, "n_in": w.n_in, "weight_bytes": wbytes,
                        "call": "qgemv_argmax" if w.argmax else "qgemv", "copies": copies, "ntok": row}
         del pool
+        if name in workloads.DRAFT_IDS:
+            table[f"{w.fmt}_draft_ids_{workloads.DRAFT_IDS[name][0]}_of_{w.n_out}x{w.n_in}"] = \
+                draft_ids_detail(qg, torch, dev, l2, peak, w, base)
     cache.clear()
     torch.cuda.empty_cache()
     return table
+
+
+def draft_ids_detail(qg, torch, dev, l2, peak, w, head):
+    """The id-list draft head: gather the listed rows once (timed: bytes read + written),
+    then qgemv_argmax_ids on the small head per ntok (timed like every other workload)."""
+    k, seed = workloads.DRAFT_IDS[w.name]
+    ids = torch.from_numpy(workloads.draft_ids(seed, w.n_out, k)).to(dev)
+    small = torch.empty(qg.qg_packed_bytes(w.fmt, k, w.n_in), dtype=torch.uint8, device=dev)
+    qg.qg_gather_rows(w.fmt, head, w.n_out, w.n_in, ids, small)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        qg.qg_gather_rows(w.fmt, head, w.n_out, w.n_in, ids, small)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e3)
+    g_us = statistics.median(times)
+    moved = 2 * small.numel()
+    wbytes = workloads_bytes(w.fmt, k, w.n_in)
+    copies = max(1, math.ceil(4 * l2 / small.numel()))
+    pool = [small] + [small.clone() for _ in range(copies - 1)]
+    x = torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).to(dev)
+    y = torch.empty((4, k), dtype=torch.float32, device=dev)
+    am = torch.empty(4, dtype=torch.int32, device=dev)
+    wsp = torch.zeros(qg.qgemv_argmax_workspace_bytes(k, 4), dtype=torch.uint8, device=dev)
+    row = {}
+    for ntok in NTOKS:
+        n = 50
+        for i in range(copies + 2):
+            qg.qgemv_argmax_ids(w.fmt, pool[i % copies], k, w.n_in, x, y, am, ids, wsp, ntok)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, capture_error_mode="thread_local"):
+            for i in range(n):
+                qg.qgemv_argmax_ids(w.fmt, pool[i % copies], k, w.n_in, x, y, am, ids, wsp, ntok)
+        gr.replay()
+        ts = []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gr.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / n * 1e3)
+        us = statistics.median(ts)
+        gbs = wbytes / (us * 1e-6) / 1e9
+        row[str(ntok)] = {"us": round(us, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                          "tile": qg.qg_describe_tile(w.fmt, k, w.n_in, ntok)}
+        del gr
+    return {"fmt": w.fmt, "n_out": k, "n_in": w.n_in, "weight_bytes": wbytes, "call": "qgemv_argmax_ids",
+            "ids": f"{k} ids of the {w.n_out}-row head (seeded, sorted)", "copies": copies,
+            "gather": {"us": round(g_us, 1), "bytes_moved": moved, "gbs": round(moved / (g_us * 1e-6) / 1e9, 1),
+                       "frac": round(moved / (g_us * 1e-6) / 1e9 / peak, 4)},
+            "ntok": row}
 
 
 # ----------------------------------------------------------------------------- reference arm

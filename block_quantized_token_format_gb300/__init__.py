@@ -21,7 +21,8 @@ __all__ = [
     "qg_quantize", "qg_to_device_layout", "qg_pack", "qgemv", "qgemv_argmax_workspace_bytes",
     "qgemv_argmax", "qg_set_tile_override", "qg_describe_tile", "weight_bytes", "qg_device_status",
     "qg_set_wait_limit", "QG_DEVICE_WAIT_TIMEOUT", "qgemv_argmax_noalloc", "qg_set_launch_options",
-    "QG_LAUNCH_EARLY_START", "current_stream_handle",
+    "QG_LAUNCH_EARLY_START", "current_stream_handle", "qg_gather_rows", "qgemv_argmax_ids",
+    "QG_DEVICE_BAD_ROW_ID",
 ]
 
 QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
@@ -75,6 +76,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "qg_set_wait_limit": (i32, [ctypes.c_uint, ctypes.c_uint]),
         "qgemv_argmax_noalloc": (i32, [i32, vp, i64, i64, vp, vp, vp, i32, vp]),
         "qg_set_launch_options": (i32, [ctypes.c_uint]),
+        "qg_gather_rows": (i32, [i32, vp, i64, i64, vp, i64, vp, vp]),
+        "qgemv_argmax_ids": (i32, [i32, vp, i64, i64, vp, vp, vp, i32, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -221,6 +224,30 @@ def qgemv_argmax_noalloc(fmt, W, n_out: int, n_in: int, x, y, argmax, ntok: int 
     st = load_library().qgemv_argmax_noalloc(_fmt(fmt), _ptr(W), n_out, n_in, _ptr(x), _ptr(y), _ptr(argmax),
                                              int(ntok), _stream(stream))
     _check(st, "qgemv_argmax_noalloc")
+
+
+def qg_gather_rows(fmt, W, n_out: int, n_in: int, ids, out, n_ids: int | None = None, stream=None) -> None:
+    """Enqueue the copy of rows ``ids`` (device int32) of the packed matrix ``W`` into ``out``
+    (a packed ``n_ids``-row matrix): the small head of a draft vocabulary."""
+    if n_ids is None:
+        n_ids = ids.numel()
+    _check(load_library().qg_gather_rows(_fmt(fmt), _ptr(W), n_out, n_in, _ptr(ids), int(n_ids), _ptr(out),
+                                         _stream(stream)), "qg_gather_rows")
+
+
+def qgemv_argmax_ids(fmt, W_sub, n_sub: int, n_in: int, x, y, argmax, ids, workspace, ntok: int | None = None,
+                     workspace_bytes: int | None = None, stream=None) -> None:
+    """qgemv_argmax over a gathered head; argmax[t] is written as ids[winning row] (full-vocab id)."""
+    if ntok is None:
+        ntok = x.shape[0] if getattr(x, "dim", lambda: 1)() == 2 else 1
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+    st = load_library().qgemv_argmax_ids(_fmt(fmt), _ptr(W_sub), n_sub, n_in, _ptr(x), _ptr(y), _ptr(argmax),
+                                         int(ntok), _ptr(ids), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "qgemv_argmax_ids")
+
+
+QG_DEVICE_BAD_ROW_ID = 2
 
 
 def qg_set_tile_override(spec: str | None) -> None:

@@ -417,12 +417,18 @@ size_t qgemv_argmax_workspace_bytes(int64_t n_out, int ntok) {
     return 16 + size_t(kMaxGrid) * size_t(ntok) * sizeof(ArgmaxPartial);
 }
 
-qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, const float* x, float* y,
-                       int32_t* argmax, int ntok, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace qg {
+namespace {
+
+qg_status argmax_call(int fmt, const void* W, int64_t n_out, int64_t n_in, const float* x, float* y,
+                      int32_t* argmax, int ntok, const int32_t* row_ids, void* workspace, size_t workspace_bytes,
+                      void* stream) {
     qg_status st = check_common(fmt, W, n_out, n_in, x, ntok);
     if (st != QG_OK) return st;
     if (!argmax) return QG_EINVAL;
-    if ((y && !aligned(y, 4)) || !aligned(argmax, 4)) return QG_EALIGN;
+    if ((y && !aligned(y, 4)) || !aligned(argmax, 4) || (row_ids && !aligned(row_ids, 4))) return QG_EALIGN;
     if (!workspace || workspace_bytes < qgemv_argmax_workspace_bytes(n_out, ntok)) return QG_EWORKSPACE;
     if (!aligned(workspace, 16)) return QG_EALIGN;
     Plan p;
@@ -432,9 +438,63 @@ qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, c
     st = fill_common(a, p, fmt, W, n_out, n_in, x, y);
     if (st != QG_OK) return st;
     a.argmax = argmax;
+    a.row_ids = row_ids;
     a.ticket = static_cast<unsigned int*>(workspace);
     a.partials = reinterpret_cast<ArgmaxPartial*>(static_cast<uint8_t*>(workspace) + 16);
     return launch(p, a, stream);
+}
+
+// Row gather: block-strided over the listed rows, each row copied as 16-byte words.
+// An id outside [0, n_out) gets a zero row and sets kStatusBadRowId (no access
+// outside the source).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                          const int32_t* __restrict__ ids, long long n_ids,
+                                                          long long n_out, int row16, unsigned int* status) {
+    for (long long j = blockIdx.x; j < n_ids; j += gridDim.x) {
+        const int id = __ldg(ids + j);
+        uint4* d = dst + j * row16;
+        if (id < 0 || id >= n_out) {
+            for (int k = threadIdx.x; k < row16; k += blockDim.x) d[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (threadIdx.x == 0) atomicOr(status, kStatusBadRowId);
+        } else {
+            const uint4* r = src + (long long)id * row16;
+            for (int k = threadIdx.x; k < row16; k += blockDim.x) d[k] = __ldg(r + k);
+        }
+    }
+}
+
+}  // namespace
+}  // namespace qg
+
+extern "C" {
+
+qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, const float* x, float* y,
+                       int32_t* argmax, int ntok, void* workspace, size_t workspace_bytes, void* stream) {
+    return argmax_call(fmt, W, n_out, n_in, x, y, argmax, ntok, nullptr, workspace, workspace_bytes, stream);
+}
+
+qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t n_in, const float* x, float* y,
+                           int32_t* argmax, int ntok, const int32_t* ids, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    if (!ids) return QG_EINVAL;
+    return argmax_call(fmt, W_sub, n_sub, n_in, x, y, argmax, ntok, ids, workspace, workspace_bytes, stream);
+}
+
+qg_status qg_gather_rows(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in, const int32_t* ids, int64_t n_ids,
+                         void* W_out, void* stream) {
+    if (!shape_valid(fmt, n_out, n_in)) return QG_EINVAL;
+    if (!W || !ids || !W_out || n_ids < 1 || n_ids > (int64_t(1) << 31) - 1) return QG_EINVAL;
+    if (!aligned(W, 16) || !aligned(W_out, 16) || !aligned(ids, 4)) return QG_EALIGN;
+    int dev = 0, sms = 0, optin = 0;
+    unsigned int* status = nullptr;
+    qg_status st = device_info(&dev, &sms, &optin, &status);
+    if (st != QG_OK) return st;
+    const int64_t stride = row_stride(fmt, n_in);
+    const long long grid = std::min<long long>(n_ids, (long long)sms * 8);
+    gather_rows_kernel<<<unsigned(grid), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(W), static_cast<uint4*>(W_out), ids, n_ids, n_out, int(stride / 16), status);
+    if (cudaGetLastError() != cudaSuccess) return QG_ECUDA;
+    return QG_OK;
 }
 
 qg_status qg_set_tile_override(const char* spec) {

@@ -63,6 +63,7 @@ constexpr int kMaxWarps = 16;             // warps per CTA (launch bound 512 thr
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr uint32_t kWaitLimit = 1u << 22; // mbarrier polls before a wait is declared failed
 constexpr unsigned kStatusWaitTimeout = 1u;
+constexpr unsigned kStatusBadRowId = 2u;    // a row gather met an id outside the head
 
 struct ArgmaxPartial { float v; int i; };
 
@@ -72,6 +73,8 @@ struct KernelArgs {
     const float* x;            // [ntok][n_in]
     float* y;                  // [ntok][n_out], may be null for argmax-only
     int* argmax;               // [ntok] (argmax kernels)
+    const int32_t* row_ids;    // optional [n_out]: the argmax is written as row_ids[winning row]
+                               // (a draft head gathered from a full head: back to full ids)
     ArgmaxPartial* partials;   // [gridDim.x][ntok] (argmax kernels)
     unsigned int* ticket;      // zero on entry, left zero on exit (argmax kernels)
     unsigned int* status;      // device status word (bit 0: a bounded wait gave up)
@@ -723,7 +726,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
                     const int oi = __shfl_xor_sync(kFull, bi, mask);
                     if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
                 }
-                if (lane == 0) a.argmax[t] = (bi == 0x7FFFFFFF) ? -1 : bi;
+                if (lane == 0) a.argmax[t] = (bi == 0x7FFFFFFF) ? -1 : (a.row_ids ? a.row_ids[bi] : bi);
             }
             if (threadIdx.x == 0) *a.ticket = 0u;   // ready for the next call on this workspace
         }

@@ -138,6 +138,39 @@ qg_status qgemv_argmax(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
                        const float* x, float* y, int32_t* argmax, int ntok,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------ draft vocabulary given as an id list
+ * A drafter may score only a listed subset of the LM head's rows ("Where the
+ * time goes on an M2 Max", section "MTP draft vocabulary subset": the listed rows
+ * are copied once into a small head) and map its argmax back to full-vocabulary
+ * ids ("perf(speculative): cut the MTP drafter's per-step cost", Phase 2 item 2b:
+ * a reduced draft vocabulary plus a d2t index mapping).  A list that is a row
+ * prefix needs neither call: pass the first rows of the head to qgemv_argmax.
+ *
+ * qg_gather_rows: W_out (device layout, n_ids rows, qg_packed_bytes(fmt, n_ids,
+ *   n_in) bytes, caller-allocated, 16-byte aligned, not overlapping W) receives
+ *   row ids[j] of W (device layout, n_out rows, 16-byte aligned) as its row j.
+ *   ids: n_ids int32 in device memory (4-byte aligned), any order, repeats
+ *   allowed.  An id outside [0, n_out) gives a zero row and sets
+ *   QG_DEVICE_BAD_ROW_ID in the device status word (qg_device_status); nothing
+ *   outside W is read.  Asynchronous on `stream`; run it once per list, off the
+ *   per-token path.  Errors: QG_EINVAL (format, shape, null pointer, n_ids < 1 or
+ *   >= 2^31), QG_EALIGN, QG_ECUDA.
+ *
+ * qgemv_argmax_ids: qgemv_argmax over the gathered head W_sub (n_sub rows):
+ *   y, if not NULL, receives the small head's logits [ntok][n_sub]; argmax[t]
+ *   receives ids[j*], the full-vocabulary id of the winning row j* (the lowest j
+ *   on ties; -1 when every logit is NaN).  ids: the n_sub int32 ids W_sub was
+ *   gathered with, in device memory, read once per token at the end.  Workspace,
+ *   ownership and errors as qgemv_argmax, plus QG_EINVAL for ids == NULL and
+ *   QG_EALIGN for misaligned ids. */
+#define QG_DEVICE_BAD_ROW_ID 2u
+qg_status qg_gather_rows(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
+                         const int32_t* ids, int64_t n_ids, void* W_out, void* stream);
+qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t n_in,
+                           const float* x, float* y, int32_t* argmax, int ntok,
+                           const int32_t* ids, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
 /* ------------------------------------------------------- qgemv_argmax_noalloc
  * No counterpart on the source pages: an addition for callers that cannot call
  * cudaMalloc, such as a plugin inside a host framework that owns every device
@@ -217,7 +250,8 @@ qg_status qg_set_launch_options(unsigned int flags);
  * shared memory) is bounded.  If a wait gives up, the kernel sets
  * QG_DEVICE_WAIT_TIMEOUT in a per-device status word, stops issuing copies,
  * drains the copies it already issued (again bounded) and exits normally; its
- * outputs are then not valid.  qg_device_status copies the current device's
+ * outputs are then not valid.  qg_gather_rows sets QG_DEVICE_BAD_ROW_ID when a
+ * listed id is outside the head.  qg_device_status copies the current device's
  * word into *status (synchronously: it waits for the device) and, if `clear`,
  * resets it to 0. */
 #define QG_DEVICE_WAIT_TIMEOUT 1u

@@ -69,6 +69,27 @@ def test_argmax_rejects_before_launch():
     assert lib.qgemv_argmax(0, A, 100, 256, A, A, A, 4, A + 8, ws, None) == -2
 
 
+def test_draft_ids_calls_reject_before_launch():
+    lib = qg.load_library()
+    ws = qg.qgemv_argmax_workspace_bytes(100, 4)
+    # qg_gather_rows(fmt, W, n_out, n_in, ids, n_ids, W_out, stream)
+    assert lib.qg_gather_rows(9, A, 100, 256, A, 10, A, None) == -1          # bad format
+    assert lib.qg_gather_rows(0, A, 100, 48, A, 10, A, None) == -1           # bad n_in
+    assert lib.qg_gather_rows(0, None, 100, 256, A, 10, A, None) == -1       # null W
+    assert lib.qg_gather_rows(0, A, 100, 256, None, 10, A, None) == -1       # null ids
+    assert lib.qg_gather_rows(0, A, 100, 256, A, 10, None, None) == -1       # null out
+    assert lib.qg_gather_rows(0, A, 100, 256, A, 0, A, None) == -1           # no ids
+    assert lib.qg_gather_rows(0, A, 100, 256, A, 1 << 31, A, None) == -1     # too many ids
+    assert lib.qg_gather_rows(0, A + 8, 100, 256, A, 10, A, None) == -2      # W misaligned
+    assert lib.qg_gather_rows(0, A, 100, 256, A, 10, A + 8, None) == -2      # out misaligned
+    assert lib.qg_gather_rows(0, A, 100, 256, A + 2, 10, A, None) == -2      # ids misaligned
+    # qgemv_argmax_ids(fmt, W, n_sub, n_in, x, y, argmax, ntok, ids, ws, ws_bytes, stream)
+    assert lib.qgemv_argmax_ids(0, A, 100, 256, A, A, A, 4, None, A, ws, None) == -1     # null ids
+    assert lib.qgemv_argmax_ids(0, A, 100, 256, A, A, A, 4, A + 2, A, ws, None) == -2    # ids misaligned
+    assert lib.qgemv_argmax_ids(0, A, 100, 256, A, A, A, 4, A, None, ws, None) == -4     # no workspace
+    assert lib.qgemv_argmax_ids(0, A, 100, 256, A, A, A, 5, A, A, ws, None) == -1        # ntok 5
+
+
 def test_tile_override_grammar():
     lib = qg.load_library()
     for good in (b"rpw=4", b"depth=2,rpw=1", b"rpw=2,depth=4,warps=8,ctas=2", b"", None, b"rpw=1,", b"rpw=8", b"split=3,rpw=2", b"rpw=3", b"rpw=5", b"rpw=6"):
