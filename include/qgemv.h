@@ -113,8 +113,10 @@ qg_status qg_pack(qg_fmt fmt, const float* W_host, int64_t n_out, int64_t n_in,
  *   ntok  1..4.   n_out >= 1.   n_in a positive multiple of the block (as above)
  *         and small enough that ntok*n_in fp32 values fit in one SM's shared
  *         memory (QG_EUNSUPPORTED otherwise; n_in <= 12288 always fits at ntok 4).
- * Each output is an fp32 sum over n_in whose order depends only on (fmt, n_in):
- * row t of an ntok=k call is bitwise equal to the ntok=1 call on x[t].
+ * Each output is an fp32 sum over n_in whose order depends only on the matrix
+ * (fmt, n_out, n_in; see the split under tile selection): row t of an ntok=k
+ * call is bitwise equal to the ntok=1 call on x[t], for every geometry, grid
+ * and launch option (a forced split override changes the order).
  * Asynchronous on `stream`; returns QG_ECUDA if the launch is rejected. */
 qg_status qgemv(qg_fmt fmt, const void* W, int64_t n_out, int64_t n_in,
                 const float* x, float* y, int ntok, void* stream);
