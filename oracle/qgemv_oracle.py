@@ -18,6 +18,10 @@ Sources (the web pages this library is built from; short tags used below):
   "The cost model" (the affine 4-bit LM head: weight 635.7 + scales 39.7 +
   biases 39.7 MB) and "Phase 2" item 2a (fuse the LM-head projection and its
   argmax) and 2b (reduced draft vocabulary).
+* [Track2] also section 1 item 2 (``moe_plan`` groups a step's (token, expert)
+  pairs by expert; ``moe_gu`` / ``moe_down`` run each group with its own token
+  count ne = 1..4, reading each unique expert once) and table 2.2 (routed
+  experts at ntok 1, 3, 4: 10.0, 18.1 and 21.3 unique groups at share 0.65).
 * [Track1]  "opus-mtp-turbo: Track 1 report", item 3 (Q4_0 / Q8_0 draft weights;
   one row's sum is independent of the token count).
 
@@ -354,4 +358,88 @@ def qgemv_argmax_ids(fmt, packed, n_out, n_in, x, ids):
     y = gemv(fmt, small, ids.size, n_in, x)
     j = argmax_first(y)
     return y, ids[j].astype(np.int32)
+
+
+# ----------------------------------------------------------------------------- routed experts
+
+MAX_GROUP_SLOTS = 4     # tokens per expert group: ne = 1..4
+
+
+def expert_plan(ids, n_experts: int):
+    """Group a step's routed (token, choice) pairs by expert ([Track2] section 1 item 2).
+
+    ``ids[t, j]`` is the expert of token t's j-th choice; pair ``i = t * topk + j``.
+    Reading of the plan: groups in increasing expert id; within a group the pairs in
+    increasing i; an expert with more than four pairs (a token listing it twice, or
+    more than four tokens) continues in the next group, four pairs at a time.  The
+    pairs laid out group after group are the *slots*.
+
+    Returns a dict of int arrays: ``group_start`` (n_groups + 1 entries, last =
+    n_slots), ``group_expert``, ``slot_pair`` (the pair i held by each slot),
+    ``slot_token`` (= slot_pair // topk) and ``pair_slot`` (the inverse of slot_pair).
+    """
+    ids = np.asarray(ids)
+    if ids.ndim != 2 or ids.size == 0:
+        raise ValueError("ids must be [ntok, topk]")
+    topk = ids.shape[1]
+    flat = [int(v) for v in ids.reshape(-1)]
+    if any(not 0 <= e < n_experts for e in flat):
+        raise ValueError("expert id out of range")
+    group_start, group_expert, slot_pair = [], [], []
+    for e in range(n_experts):
+        pairs = [i for i, v in enumerate(flat) if v == e]
+        for c in range(0, len(pairs), MAX_GROUP_SLOTS):
+            group_start.append(len(slot_pair))
+            group_expert.append(e)
+            slot_pair.extend(pairs[c:c + MAX_GROUP_SLOTS])
+    group_start.append(len(slot_pair))
+    pair_slot = [0] * len(flat)
+    for s, i in enumerate(slot_pair):
+        pair_slot[i] = s
+    return {"group_start": np.array(group_start, dtype=np.int64),
+            "group_expert": np.array(group_expert, dtype=np.int64),
+            "slot_pair": np.array(slot_pair, dtype=np.int64),
+            "slot_token": np.array(slot_pair, dtype=np.int64) // topk,
+            "pair_slot": np.array(pair_slot, dtype=np.int64)}
+
+
+def experts_gemv_slots(fmt, packed, n_experts: int, n_out: int, n_in: int, x, plan, x_by_slot: bool):
+    """The expert-grouped mat-vec over a plan's slots: fp64 ``y[s, o]`` for slot s of
+    group g = ``deq(W_e)[o] . x_row(s)`` with e = group_expert[g] and x_row(s) =
+    ``x[slot_token[s]]`` (the gate / up projection reads the step's token rows) or
+    ``x[s]`` (the down projection reads one activation row per slot).  [Track2]
+    section 1 item 2."""
+    starts = [int(v) for v in plan["group_start"]]
+    n_slots = starts[-1]
+    y = np.empty((n_slots, n_out))
+    for g, e in enumerate(plan["group_expert"]):
+        slots = list(range(starts[g], starts[g + 1]))
+        rows = slots if x_by_slot else [int(plan["slot_token"][s]) for s in slots]
+        y[slots] = experts_gemv(fmt, packed, n_experts, n_out, n_in, x, [e], [rows])[0, :len(slots)]
+    return y
+
+
+def experts_gemv(fmt, packed, n_experts: int, n_out: int, n_in: int, x, group_expert, group_tokens):
+    """Expert-grouped multi-token mat-vec.
+
+    [Track2] section 1 item 2 (``moe_plan`` groups the tokens by expert id; ``moe_gu`` /
+    ``moe_down`` then run each group with its own token count ne = 1..4, reading each
+    unique expert's weights once).  ``packed`` holds the experts' matrices stacked
+    (expert e = rows ``[e * n_out, (e + 1) * n_out)``); group g multiplies expert
+    ``group_expert[g]`` by the tokens ``group_tokens[g]`` (1..4 indices into x).
+    Returns fp64 ``y[g, k, o]`` for the k-th token of group g (``[n_groups, 4, n_out]``;
+    slots k >= ne are NaN).
+    """
+    f = fmt_id(fmt)
+    x = np.asarray(x, dtype=np.float32)
+    ng = len(group_expert)
+    y = np.full((ng, 4, n_out), np.nan)
+    for g in range(ng):
+        e = int(group_expert[g])
+        toks = [int(t) for t in group_tokens[g]]
+        if not 0 <= e < n_experts or not 1 <= len(toks) <= 4:
+            raise ValueError("bad group")
+        sub = row_slice(f, packed, n_experts * n_out, n_in, e * n_out, (e + 1) * n_out)
+        y[g, :len(toks)] = gemv(f, sub, n_out, n_in, x[toks])
+    return y
 

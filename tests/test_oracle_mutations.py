@@ -38,6 +38,17 @@ MUTATIONS = {
     "argmax last index": ("return np.argmax(yy, axis=1).astype(np.int32)",
                           "return (yy.shape[1] - 1 - np.argmax(yy[:, ::-1], axis=1)).astype(np.int32)"),
     "draft argmax not mapped": ("return y, ids[j].astype(np.int32)", "return y, j.astype(np.int32)"),
+    "experts wrong expert rows": ("sub = row_slice(f, packed, n_experts * n_out, n_in, e * n_out, (e + 1) * n_out)",
+                                  "sub = row_slice(f, packed, n_experts * n_out, n_in, 0, n_out)"),
+    "experts tokens reversed": ("y[g, :len(toks)] = gemv(f, sub, n_out, n_in, x[toks])",
+                                "y[g, :len(toks)] = gemv(f, sub, n_out, n_in, x[toks[::-1]])"),
+    "plan pairs by token not by expert": ("pairs = [i for i, v in enumerate(flat) if v == e]",
+                                          "pairs = [i for i, v in enumerate(flat) if v == e][::-1]"),
+    "plan groups of five": ("MAX_GROUP_SLOTS = 4     # tokens", "MAX_GROUP_SLOTS = 5     # tokens"),
+    "plan slot_token off by one": ('"slot_token": np.array(slot_pair, dtype=np.int64) // topk,',
+                                   '"slot_token": np.array(slot_pair, dtype=np.int64) // max(topk - 1, 1),'),
+    "slots read token rows in down mode": ("rows = slots if x_by_slot else",
+                                           "rows = slots if not x_by_slot else"),
     "draft gather ignores affine scales": ("s = packed[nw * 4: nw * 4 + ng * 2].reshape(n_out, n_in // 32)[ids]",
                                            "s = packed[nw * 4: nw * 4 + ng * 2].reshape(n_out, n_in // 32)[:ids.size]"),
 }

@@ -373,11 +373,102 @@ def check_draft_ids(orc):
         pass
 
 
+def check_experts(orc):
+    """Expert-grouped mat-vec ([Track2] section 1 item 2: tokens grouped by expert,
+    each group run with its own token count): every group equals the plain mat-vec
+    of its expert's rows on its tokens, and grouping all tokens under one expert
+    equals the stacked matrix's rows of that expert."""
+    n_experts, n_out, n_in = 5, 24, 128
+    W = workloads.gaussian(81, (n_experts * n_out, n_in), 0.02)
+    x = workloads.gaussian(82, (4, n_in))
+    for fmt in ("q8_0", "q4_0", "affine4_g64", "bf16"):
+        raw = orc.quantize(fmt, W)
+        ge = [3, 0, 4, 3]
+        gt = [[2], [0, 1, 3], [3, 2, 1, 0], [1, 0]]
+        y = orc.experts_gemv(fmt, raw, n_experts, n_out, n_in, x, ge, gt)
+        full = orc.gemv(fmt, raw, n_experts * n_out, n_in, x)          # every token x every stacked row
+        for g, (e, toks) in enumerate(zip(ge, gt)):
+            for k, t in enumerate(toks):
+                assert np.allclose(y[g, k], full[t, e * n_out:(e + 1) * n_out], rtol=1e-13, atol=1e-15), (fmt, g, k)
+            assert np.all(np.isnan(y[g, len(toks):]))
+        # hand check of one output: expert 4, token 1 (slot 2 of group 2), row 5
+        deq = orc.dequantize(fmt, raw, n_experts * n_out, n_in)
+        assert np.isclose(y[2, 2, 5], float(deq[4 * n_out + 5] @ x[1].astype(np.float64)), rtol=1e-13, atol=1e-15)
+    try:
+        orc.experts_gemv("q8_0", orc.quantize("q8_0", W), n_experts, n_out, n_in, x, [n_experts], [[0]])
+        raise AssertionError("an expert past the stack was accepted")
+    except ValueError:
+        pass
+
+
+def check_expert_plan(orc):
+    """The routed-expert plan ([Track2] section 1 item 2: moe_plan groups the pairs by
+    expert).  A hand-worked case, the invariants of the grouping on random routing,
+    the four-pair chunking, and the unique-expert count."""
+    # ids[t][j]: pairs i = 0..5 -> experts 3,1 | 1,0 | 3,2.  By expert, then i:
+    # e0: [3]   e1: [1, 2]   e2: [5]   e3: [0, 4]
+    p = orc.expert_plan([[3, 1], [1, 0], [3, 2]], 4)
+    assert p["group_start"].tolist() == [0, 1, 3, 4, 6]
+    assert p["group_expert"].tolist() == [0, 1, 2, 3]
+    assert p["slot_pair"].tolist() == [3, 1, 2, 5, 0, 4]
+    assert p["slot_token"].tolist() == [1, 0, 1, 2, 0, 2]
+    assert p["pair_slot"].tolist() == [4, 1, 2, 0, 5, 3]
+    # one expert taken by six pairs: groups of 4 then 2, both for that expert
+    p = orc.expert_plan([[7, 7, 7], [7, 7, 7]], 8)
+    assert p["group_start"].tolist() == [0, 4, 6] and p["group_expert"].tolist() == [7, 7]
+    assert p["slot_pair"].tolist() == [0, 1, 2, 3, 4, 5]
+    rng = np.random.default_rng(5)
+    for trial in range(60):
+        ntok, topk, n_exp = int(rng.integers(1, 6)), int(rng.integers(1, 11)), int(rng.integers(1, 40))
+        ids = rng.integers(0, n_exp, size=(ntok, topk))
+        p = orc.expert_plan(ids, n_exp)
+        gs, ge, sp = p["group_start"], p["group_expert"], p["slot_pair"]
+        n = ntok * topk
+        assert gs[0] == 0 and gs[-1] == n and np.all(np.diff(gs) >= 1) and np.all(np.diff(gs) <= 4)
+        assert sorted(sp.tolist()) == list(range(n))                       # every pair exactly once
+        assert np.all(p["pair_slot"][sp] == np.arange(n))
+        assert np.all(p["slot_token"] == sp // topk)
+        flat = ids.reshape(-1)
+        for g in range(len(ge)):
+            sl = sp[gs[g]:gs[g + 1]]
+            assert np.all(flat[sl] == ge[g]) and np.all(np.diff(sl) > 0)
+        assert np.all(np.diff(ge) >= 0)
+        for g in range(1, len(ge)):             # a repeated expert only after a full group
+            if ge[g] == ge[g - 1]:
+                assert gs[g] - gs[g - 1] == 4
+        counts = np.bincount(flat, minlength=n_exp)
+        assert len(ge) == int(np.sum((counts + 3) // 4))
+    for bad in ([[0, 4]], [[-1, 0]]):
+        try:
+            orc.expert_plan(bad, 4)
+            raise AssertionError("an expert id outside the stack was accepted")
+        except ValueError:
+            pass
+    # the slot form of the mat-vec is the group form laid out by slot
+    n_experts, n_out, n_in = 6, 16, 64
+    W = workloads.gaussian(83, (n_experts * n_out, n_in), 0.02)
+    raw = orc.quantize("q8_0", W)
+    ids = [[5, 2, 0], [2, 1, 5]]
+    p = orc.expert_plan(ids, n_experts)
+    xt = workloads.gaussian(84, (2, n_in))
+    y = orc.experts_gemv_slots("q8_0", raw, n_experts, n_out, n_in, xt, p, False)
+    full = orc.gemv("q8_0", raw, n_experts * n_out, n_in, xt)
+    for i in range(6):
+        t, e, s = i // 3, ids[i // 3][i % 3], int(p["pair_slot"][i])
+        assert np.allclose(y[s], full[t, e * n_out:(e + 1) * n_out], rtol=1e-13, atol=1e-15)
+    xs = workloads.gaussian(85, (6, n_in))
+    y = orc.experts_gemv_slots("q8_0", raw, n_experts, n_out, n_in, xs, p, True)
+    full = orc.gemv("q8_0", raw, n_experts * n_out, n_in, xs)
+    for s in range(6):
+        e = int(p["group_expert"][np.searchsorted(p["group_start"], s, side="right") - 1])
+        assert np.allclose(y[s], full[s, e * n_out:(e + 1) * n_out], rtol=1e-13, atol=1e-15)
+
+
 ALL_CHECKS = [check_page_byte_counts, check_golden_q8_0, check_golden_q4_0, check_golden_affine4,
               check_golden_bf16, check_rounding, check_brute_force, check_idempotence,
               check_affine_constructed_roundtrip, check_linearity, check_token_independence,
               check_cross_format, check_argmax, check_quant_error_band, check_fp16_bf16_rounding,
-              check_draft_ids]
+              check_draft_ids, check_experts, check_expert_plan]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)

@@ -118,3 +118,32 @@ def draft_ids(seed: int, n_full: int, k: int) -> np.ndarray:
     """k distinct row ids of an n_full-row head, drawn without replacement and sorted (int32)."""
     g = np.random.Generator(np.random.PCG64(seed))
     return np.sort(g.choice(n_full, size=k, replace=False)).astype(np.int32)
+
+
+def routing(seed: int, ntok: int, topk: int, n_experts: int, share: float) -> np.ndarray:
+    """Synthetic top-k routing ``ids[ntok, topk]`` (int32), distinct experts per token.
+
+    Token 0 draws topk experts uniformly.  Each later token's choice j repeats, with
+    probability ``share``, an expert that an earlier token chose (uniform among those
+    this token has not taken yet), otherwise draws one that no token has chosen yet;
+    so about ``topk + (ntok - 1) * topk * (1 - share)`` experts are active in a step.
+    """
+    g = np.random.Generator(np.random.PCG64(seed))
+    ids = np.zeros((ntok, topk), dtype=np.int32)
+    used: list[int] = []
+    for t in range(ntok):
+        mine: list[int] = []
+        for _ in range(topk):
+            old = [e for e in used if e not in mine]
+            if t > 0 and old and g.random() < share:
+                e = old[int(g.integers(len(old)))]
+            else:
+                free = np.setdiff1d(np.arange(n_experts), np.array(used + mine, dtype=np.int64))
+                e = int(free[int(g.integers(len(free)))])
+            mine.append(e)
+        for e in mine:
+            if e not in used:
+                used.append(e)
+        ids[t] = mine
+    return ids
+
