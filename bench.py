@@ -491,7 +491,99 @@ def detail_table(args, qg, torch, dev, l2, peak):
                 draft_ids_detail(qg, torch, dev, l2, peak, w, base)
     cache.clear()
     torch.cuda.empty_cache()
+    if not args.detail_only or any(n in workloads.EXPERT_LAYERS for n in names):
+        for name in workloads.EXPERT_LAYERS:
+            table[name] = experts_detail(qg, torch, dev, peak, workloads.EXPERT_LAYERS[name])
+            torch.cuda.empty_cache()
     return table
+
+
+def experts_detail(qg, torch, dev, peak, layer, unique=32, routings=64):
+    """Routed experts, one layer: the plan, the gate/up projection (token rows) and the
+    down projection (one activation row per slot) per ntok, each step with its own
+    seeded routing (64 routings in turn), timed as 64-step graphs.  Bytes = the
+    active experts' weight bytes (each read once per projection).  The stack holds
+    n_experts experts at their own addresses; their contents repeat every `unique`
+    experts (the data does not change the timing; the addresses do)."""
+    E, dm, ff = layer.n_experts, layer.d_model, layer.d_ff
+    shapes = {"gu": (2 * ff, dm, layer.seed), "dn": (dm, ff, layer.seed + 1)}
+    stacks = {}
+    for key, (n_out, n_in, seed) in shapes.items():
+        stride = qg.qg_row_stride(layer.fmt, n_in)
+        host = np.empty(unique * n_out * stride, dtype=np.uint8)
+
+        def one(k, n_out=n_out, n_in=n_in, seed=seed, stride=stride, host=host):
+            qg.qg_pack(layer.fmt, workloads.expert_matrix(seed, k, n_out, n_in),
+                       out=host[k * n_out * stride:(k + 1) * n_out * stride])
+
+        with ThreadPoolExecutor(16) as ex:
+            list(ex.map(one, range(unique)))
+        stacks[key] = torch.from_numpy(host).to(dev).repeat(E // unique)
+    bytes_e = {k: workloads_bytes(layer.fmt, n_out, n_in) for k, (n_out, n_in, _) in shapes.items()}
+    out = {"fmt": layer.fmt, "n_experts": E, "gate_up": f"{2 * ff}x{dm} per expert", "down": f"{dm}x{ff} per expert",
+           "topk": layer.topk, "share": layer.share, "routings": routings,
+           "bytes_per_expert": bytes_e["gu"] + bytes_e["dn"],
+           "tile": {k: qg.qg_describe_expert_tile(layer.fmt, n_out, n_in) for k, (n_out, n_in, _) in shapes.items()},
+           "ntok": {}}
+    for ntok in NTOKS:
+        G = ntok * layer.topk
+        ids_np = [workloads.routing(layer.seed * 100 + 17 * ntok + r, ntok, layer.topk, E, layer.share)
+                  for r in range(routings)]
+        unique_e = float(np.mean([len(np.unique(i)) for i in ids_np]))
+        ids = [torch.from_numpy(i).to(dev) for i in ids_np]
+        plans = [torch.empty(qg.qg_expert_plan_ints(G), dtype=torch.int32, device=dev) for _ in range(routings)]
+        x = torch.from_numpy(workloads.activations(layer.seed, dm, ntok)).to(dev)
+        h = torch.from_numpy(workloads.gaussian(layer.seed + 3, (G, ff))).to(dev)
+        y_gu = torch.empty((G, 2 * ff), dtype=torch.float32, device=dev)
+        y_dn = torch.empty((G, dm), dtype=torch.float32, device=dev)
+
+        def plan(r):
+            qg.qg_expert_plan(ids[r], E, plans[r])
+
+        def gu(r):
+            qg.qgemv_experts(layer.fmt, stacks["gu"], E, 2 * ff, dm, x, plans[r], G, y_gu)
+
+        def dn(r):
+            qg.qgemv_experts(layer.fmt, stacks["dn"], E, dm, ff, h, plans[r], G, y_dn, x_by_slot=True)
+
+        def layer_step(r):
+            plan(r)
+            gu(r)
+            dn(r)
+
+        for r in range(routings):
+            plan(r)
+        torch.cuda.synchronize()
+        row = {"pairs": G, "unique_experts": round(unique_e, 2),
+               "grouping_saves": round(1.0 - unique_e / G, 3)}
+        for key, fn in (("plan", plan), ("gate_up", gu), ("down", dn), ("layer", layer_step)):
+            for r in range(3):
+                fn(r)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                for r in range(routings):
+                    fn(r)
+            g.replay()
+            ts = []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b) / routings * 1e3)
+            us = statistics.median(ts)
+            nbytes = unique_e * {"plan": 0, "gate_up": bytes_e["gu"], "down": bytes_e["dn"],
+                                 "layer": bytes_e["gu"] + bytes_e["dn"]}[key]
+            row[key] = {"us": round(us, 3)}
+            if nbytes:
+                gbs = nbytes / (us * 1e-6) / 1e9
+                row[key].update({"gbs": round(gbs, 1), "frac": round(gbs / peak, 4)})
+            del g
+        out["ntok"][str(ntok)] = row
+    del stacks
+    return out
 
 
 def draft_ids_detail(qg, torch, dev, l2, peak, w, head):

@@ -22,7 +22,8 @@ __all__ = [
     "qgemv_argmax", "qg_set_tile_override", "qg_describe_tile", "weight_bytes", "qg_device_status",
     "qg_set_wait_limit", "QG_DEVICE_WAIT_TIMEOUT", "qgemv_argmax_noalloc", "qg_set_launch_options",
     "QG_LAUNCH_EARLY_START", "current_stream_handle", "qg_gather_rows", "qgemv_argmax_ids",
-    "QG_DEVICE_BAD_ROW_ID",
+    "QG_DEVICE_BAD_ROW_ID", "qg_expert_plan_ints", "qg_expert_plan", "qgemv_experts", "qg_describe_expert_tile",
+    "QG_DEVICE_BAD_PLAN",
 ]
 
 QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
@@ -78,6 +79,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "qg_set_launch_options": (i32, [ctypes.c_uint]),
         "qg_gather_rows": (i32, [i32, vp, i64, i64, vp, i64, vp, vp]),
         "qgemv_argmax_ids": (i32, [i32, vp, i64, i64, vp, vp, vp, i32, vp, vp, sz, vp]),
+        "qg_expert_plan_ints": (sz, [i64]),
+        "qg_expert_plan": (i32, [vp, i32, i32, i32, vp, vp]),
+        "qgemv_experts": (i32, [i32, vp, i64, i64, i64, vp, i64, i32, vp, i64, vp, vp]),
+        "qg_describe_expert_tile": (i32, [i32, i64, i64, ctypes.c_char_p, sz]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -248,6 +253,35 @@ def qgemv_argmax_ids(fmt, W_sub, n_sub: int, n_in: int, x, y, argmax, ids, works
 
 
 QG_DEVICE_BAD_ROW_ID = 2
+QG_DEVICE_BAD_PLAN = 4
+
+
+def qg_expert_plan_ints(n_pairs: int) -> int:
+    """int32 entries of the plan of ``n_pairs`` routed (token, choice) pairs (0 if out of range)."""
+    return int(load_library().qg_expert_plan_ints(int(n_pairs)))
+
+
+def qg_expert_plan(ids, n_experts: int, plan, stream=None) -> None:
+    """Enqueue the plan of the routing ``ids`` (device int32 ``[ntok, topk]``) into ``plan``
+    (device int32, ``qg_expert_plan_ints(ntok * topk)`` entries)."""
+    ntok, topk = int(ids.shape[0]), int(ids.shape[1])
+    _check(load_library().qg_expert_plan(_ptr(ids), ntok, topk, int(n_experts), _ptr(plan), _stream(stream)),
+           "qg_expert_plan")
+
+
+def qgemv_experts(fmt, W, n_experts: int, n_out: int, n_in: int, x, plan, n_slots: int, y,
+                  x_by_slot: bool = False, stream=None) -> None:
+    """Enqueue the expert-grouped mat-vec: ``y[s] = W_e . x_row(s)`` for every slot s of the
+    plan (``x_row(s) = x[slot_token[s]]``, or ``x[s]`` with ``x_by_slot``)."""
+    _check(load_library().qgemv_experts(_fmt(fmt), _ptr(W), int(n_experts), int(n_out), int(n_in), _ptr(x),
+                                        int(x.shape[0]), 1 if x_by_slot else 0, _ptr(plan), int(n_slots), _ptr(y),
+                                        _stream(stream)), "qgemv_experts")
+
+
+def qg_describe_expert_tile(fmt, n_out: int, n_in: int) -> str:
+    buf = ctypes.create_string_buffer(128)
+    _check(load_library().qg_describe_expert_tile(_fmt(fmt), n_out, n_in, buf, 128), "qg_describe_expert_tile")
+    return buf.value.decode()
 
 
 def qg_set_tile_override(spec: str | None) -> None:

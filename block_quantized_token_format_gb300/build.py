@@ -47,6 +47,8 @@ def _units():
         units.append((os.path.join(BUILD, f"qgemv_inst_fmt{f}.o"),
                       [nvcc, *ARCH, *NVCC_FLAGS, f"-DQG_INST_FMT={f}", "-c",
                        os.path.join(CSRC, "qgemv_inst.cu")]))
+    units.append((os.path.join(BUILD, "qgemv_experts.o"),
+                  [nvcc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, "qgemv_experts.cu")]))
     units.append((os.path.join(BUILD, "qgemv_api.o"),
                   [nvcc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, "qgemv_api.cu")]))
     for src in ("pack.cpp", "tile_select.cpp"):

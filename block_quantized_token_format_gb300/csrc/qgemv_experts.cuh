@@ -1,0 +1,264 @@
+// Expert-grouped multi-token mat-vec for sm_103a (routed experts at ntok <= 4).
+//
+// The operator of the Track 2 Audit & Optimization Report (M5 Metal kernels),
+// section 1 item 2: a plan groups a step's (token, expert) pairs by expert, and
+// the gate/up and down projections run every group with its own token count
+// ne = 1..4, reading each active expert's weights from memory once.  Here the
+// experts' matrices are stacked ([n_experts * n_out][n_in], expert e = rows
+// e * n_out ..), one tensor map covers the stack, and the plan sits in device
+// memory, written by the plan kernel (or the caller), so no host round trip
+// separates routing from the projections.
+//
+// GB300 design, on the pieces of the plain mat-vec kernel (stage_x, step_fma,
+// warp_reduce): a persistent grid whose CTAs are dealt to groups in proportion
+// (CTA b of C serves group floor(b * n_groups / C), so every group gets C /
+// n_groups CTAs, rounded down or up); a CTA stages the x rows of its group's ne
+// tokens once and its warps stream the expert's row blocks round-robin through
+// their TMA rings.  ne is a run-time value: the kernel switches to a body
+// compiled for each ne, so a one-token group costs what a one-token mat-vec
+// costs.  The first copies of a group need only the expert id and go out before
+// x is staged.  With more groups than CTAs, a CTA takes groups b, b + C, ...
+// one after the other, restaging x between them.
+//
+// The addition order of an output depends only on (fmt, n_in): it is the order of
+// the plain mat-vec without a split, whatever ne, the group, the tile or the grid.
+#pragma once
+
+#include "qgemv_kernels.cuh"
+
+namespace qg {
+
+constexpr unsigned kStatusBadPlan = 4u;   // a plan entry or a routed expert id out of range
+constexpr int kMaxPlanPairs = 1024;      // (token, choice) pairs one plan can hold
+
+// Offsets (in int32 entries) of the plan's arrays for n_slots = ntok * topk slots.
+__host__ __device__ constexpr int plan_group_start(int) { return 1; }           // n_slots + 1 entries
+__host__ __device__ constexpr int plan_group_expert(int G) { return 2 + G; }    // n_slots entries
+__host__ __device__ constexpr int plan_slot_pair(int G) { return 2 + 2 * G; }
+__host__ __device__ constexpr int plan_slot_token(int G) { return 2 + 3 * G; }
+__host__ __device__ constexpr int plan_pair_slot(int G) { return 2 + 4 * G; }
+__host__ __device__ constexpr int plan_ints(int G) { return 2 + 5 * G; }
+
+struct ExpertArgs {
+    CUtensorMap wmap;          // the stacked experts' packed rows as [n_experts * n_out][stride / 8]
+                               // 8-byte elements, box = one full step x RPW rows, zero fill outside
+    const float* x;            // [n_x][n_in]
+    float* y;                  // [n_slots][n_out]
+    const int32_t* plan;       // the plan (offsets above)
+    unsigned int* status;      // device status word
+    int n_experts;
+    int n_out;
+    int n_in;
+    int n_slots;
+    int n_x;                   // rows of x
+    int x_by_slot;             // 0: slot s reads x[slot_token[s]]; 1: slot s reads x[s]
+    int depth;
+    uint32_t wait_limit, drain_limit, stage_tx, fmagic;
+    uint32_t test_extra_tx;    // test hook: bytes added to every warp's first expected transaction
+};
+
+// One warp's ring over the groups a CTA serves: the issue cursor (row block, step,
+// stage) runs `depth` steps ahead of the consume cursor (stage, phase).  All
+// copies of a group are consumed before the next group's first copy is issued, so
+// the issue stage of a new group starts at the consume stage.
+template <int RPW, int kStage, int kBoxX>
+struct ExpertRing {
+    uint32_t bars, ring;
+    uint64_t policy;
+    int depth, spr, nblk;
+    int sc = 0;
+    uint32_t phase = 0, issued = 0, consumed = 0;
+    bool failed = false;
+    int gi = 0, ki = 0, si = 0, gstride = 1, ebase = 0;
+
+    __device__ __forceinline__ void start_group(int first_block, int stride, int expert_row0) {
+        gi = first_block;
+        ki = 0;
+        si = sc;
+        gstride = stride;
+        ebase = expert_row0;
+    }
+    // Lane 0 announces the stage's bytes and starts one tensor copy of the box
+    // (RPW rows x one step); rows past the stack arrive as zeros.
+    __device__ __forceinline__ void issue(const CUtensorMap* map, uint32_t tx, uint32_t extra, int lane) {
+        if (gi < nblk && !failed) {
+            if (lane == 0) {
+                const uint32_t bar = bars + si * 8;
+                mbar_arrive_expect_tx(bar, tx + (issued == 0 ? extra : 0u));
+                tma_load_2d(ring + uint32_t(si * kStage), map, ki * kBoxX, ebase + gi * RPW, bar, policy);
+            }
+            ++issued;
+        }
+        if (++ki == spr) { ki = 0; gi += gstride; }
+        if (++si == depth) si = 0;
+    }
+};
+
+// One group of NE tokens (x staged in the layout for kMaxNtok tokens): stream this
+// warp's row blocks of the expert and write y[s0 + t][row].
+template <int FMT, int RPW, int NE, class Ring>
+__device__ __forceinline__ void expert_group(const ExpertArgs& a, Ring& R, unsigned char* smem, int s0,
+                                             int first_block, int lane) {
+    using F = Fmt<FMT>;
+    constexpr int S = F::kW / 4;
+    constexpr int kCS = kMaxNtok * S + 1;
+    constexpr int V = RPW * NE;
+    constexpr int SPAN = 32 / Pow2Up<V>::value;
+    constexpr int kStage = stage_bytes(FMT, RPW);
+    const int n_in = a.n_in, n_out = a.n_out;
+    const int codes = FMT == QG_Q8_0 ? n_in : FMT == QG_BF16 ? 2 * n_in : n_in / 2;
+    const int last_codes = codes - 512 * (R.spr - 1);
+    const uint32_t x_lane = smem_addr(smem) + uint32_t(lane) * (kCS * 16);
+    const uint32_t code_lane = R.ring + 16u * uint32_t(lane);
+    const uint32_t scale_lane = R.ring + F::scale_off(lane);
+    Acc<FMT, NE, RPW> acc;
+    acc.clear();
+    for (int gc = first_block; gc < R.nblk; gc += R.gstride) {
+        for (int kc = 0; kc < R.spr; ++kc) {
+            if (!__all_sync(kFull, mbar_wait(R.bars + R.sc * 8, R.phase, a.wait_limit))) {
+                R.failed = true;
+                break;
+            }
+            ++R.consumed;
+            const int codes_k = (kc == R.spr - 1) ? last_codes : 512;
+            const uint32_t stage = uint32_t(R.sc) * uint32_t(kStage);
+            step_fma<FMT, NE, RPW, kMaxNtok>(acc, x_lane + uint32_t(kc) * (32u * kCS * 16u), code_lane + stage,
+                                   scale_lane + stage + uint32_t(codes_k), a.fmagic);
+            __syncwarp();                        // every lane has read this stage before it is refilled
+            R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
+            if (++R.sc == R.depth) { R.sc = 0; R.phase ^= 1u; }
+        }
+        if (R.failed) break;
+        const float v0 = warp_reduce<FMT, NE, RPW>(acc, lane);
+        const int vi = lane / SPAN;
+        if (vi < V && (lane % SPAN) == 0) {
+            const int r = vi / NE, t = vi - r * NE;
+            const int row = gc * RPW + r;
+            if (row < n_out) a.y[(long long)(s0 + t) * n_out + row] = v0;
+        }
+        acc.clear();
+    }
+}
+
+// Threads per CTA: 16 warps up to 2 rows per warp; 12 warps (168 registers a thread)
+// at 4 rows, whose four-token body does not fit in 128 registers beside the group
+// loop's state.
+template <int RPW> struct ExpertThreads { static constexpr int value = RPW >= 4 ? 384 : 512; };
+
+template <int FMT, int RPW>
+__global__ void __launch_bounds__(ExpertThreads<RPW>::value, 1) qgemv_experts_kernel(const __grid_constant__ ExpertArgs a) {
+    using F = Fmt<FMT>;
+    constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
+    constexpr int kStage = stage_bytes(FMT, RPW);
+    constexpr int kBoxX = kFullStep / 8;
+    static_assert(kFullStep == full_step(FMT) && kFullStep % 16 == 0, "step size");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int n_in = a.n_in;
+    const int codes = FMT == QG_Q8_0 ? n_in : FMT == QG_BF16 ? 2 * n_in : n_in / 2;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+
+    const SmemPlan sp = smem_plan(FMT, kMaxNtok, n_in, RPW, a.depth, nwarps, 1);
+    ExpertRing<RPW, kStage, kBoxX> R;
+    R.depth = a.depth;
+    R.spr = (codes + 511) >> 9;
+    R.nblk = (a.n_out + RPW - 1) / RPW;
+    R.bars = smem_addr(smem + sp.bar_off) + warp * R.depth * 8;
+    R.ring = ((smem_addr(smem + sp.ring_off) + 127u) & ~127u) + uint32_t(warp * R.depth * kStage);
+    R.policy = l2_evict_first_policy();
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&a.wmap)) : "memory");
+        for (int s = 0; s < R.depth; ++s) mbar_init(R.bars + s * 8, 1);
+    }
+    mbar_fence_init();
+    __syncwarp();
+    // The plan and x may come from the previous kernel in the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    const int G = a.n_slots;
+    const int32_t* plan = a.plan;
+    int ng = __ldg(plan);
+    if (ng < 0 || ng > G) {
+        if (threadIdx.x == 0) atomicOr(a.status, kStatusBadPlan);
+        ng = 0;
+    }
+    const int C = int(gridDim.x), b = int(blockIdx.x);
+    int g, gstep, ci, cn;
+    if (ng <= C) {   // CTAs in proportion: group g owns CTAs [ceil(g C / ng), ceil((g + 1) C / ng))
+        const int d = ng > 0 ? ng : 1;
+        g = int((long long)b * ng / C);
+        const int b0 = int(((long long)g * C + d - 1) / d);
+        const int b1 = int(((long long)(g + 1) * C + d - 1) / d);
+        ci = b - b0;
+        cn = b1 - b0;
+        gstep = d;
+    } else {         // more groups than CTAs: whole groups b, b + C, ...
+        g = b;
+        ci = 0;
+        cn = 1;
+        gstep = C;
+    }
+
+    for (; g < ng; g += gstep) {
+        // Every thread reads the same plan words, so `ok` and ne are CTA-uniform.
+        const int s0 = __ldg(plan + plan_group_start(G) + g);
+        const int s1 = __ldg(plan + plan_group_start(G) + g + 1);
+        const int e = __ldg(plan + plan_group_expert(G) + g);
+        const int ne = s1 - s0;
+        bool ok = s0 >= 0 && s1 <= G && ne >= 1 && ne <= kMaxNtok && e >= 0 && e < a.n_experts;
+        int xrow[kMaxNtok];
+#pragma unroll
+        for (int k = 0; k < kMaxNtok; ++k) {
+            xrow[k] = 0;
+            if (ok && k < ne) {
+                xrow[k] = a.x_by_slot ? s0 + k : __ldg(plan + plan_slot_token(G) + s0 + k);
+                ok = ok && xrow[k] >= 0 && xrow[k] < a.n_x;
+            }
+        }
+        if (!ok) {
+            if (threadIdx.x == 0) atomicOr(a.status, kStatusBadPlan);
+            continue;
+        }
+        // The group's first copies need only the expert's rows: they go out before
+        // x is staged.  (e * n_out + n_out <= 2^31 - 1, checked at launch.)
+        const int first = ci + cn * warp;
+        R.start_group(first, cn * nwarps, e * a.n_out);
+        for (int s = 0; s < R.depth; ++s) R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
+        __syncthreads();                         // no warp still reads the previous group's x
+        {
+            // One staging path for every ne (the layout for kMaxNtok tokens; slots of
+            // tokens >= ne are never read).
+            const float4* x4 = reinterpret_cast<const float4*>(a.x);
+            const float4* rows[kMaxNtok];
+#pragma unroll
+            for (int k = 0; k < kMaxNtok; ++k) rows[k] = x4 + (long long)xrow[k] * (n_in >> 2);
+            stage_x<FMT, kMaxNtok>(smem, rows, n_in, R.spr, ne);
+        }
+        __syncthreads();
+        if (R.failed) continue;
+        switch (ne) {
+            case 1: expert_group<FMT, RPW, 1>(a, R, smem, s0, first, lane); break;
+            case 2: expert_group<FMT, RPW, 2>(a, R, smem, s0, first, lane); break;
+            case 3: expert_group<FMT, RPW, 3>(a, R, smem, s0, first, lane); break;
+            default: expert_group<FMT, RPW, 4>(a, R, smem, s0, first, lane); break;
+        }
+    }
+
+    if (R.failed) {
+        // Report, then drain (bounded) the copies issued but not consumed.
+        if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+        for (uint32_t f = R.consumed; f < R.issued; ++f) {
+            mbar_wait(R.bars + R.sc * 8, R.phase, a.drain_limit);
+            if (++R.sc == R.depth) { R.sc = 0; R.phase ^= 1u; }
+        }
+    }
+}
+
+// Lookup of an instantiated expert kernel (qgemv_experts.cu).
+const void* expert_kernel_lookup(int fmt, int rpw);
+
+}  // namespace qg

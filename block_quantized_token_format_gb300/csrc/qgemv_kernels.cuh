@@ -331,6 +331,201 @@ __host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int r
     return p;
 }
 
+// ------------------------------------------------------------------------------ kernel pieces
+// Shared by the mat-vec kernel and the expert-grouped kernel.
+
+// Stage x rows[0..live-1] (each n_in fp32, 16-byte aligned) into the chunk-interleaved
+// layout for NTOK tokens at `smem` (see SmemPlan), zero past n_in up to whole steps;
+// the slots of tokens live..NTOK-1 are left as they are.  Each thread issues all its
+// loads of a batch before its first store, so staging costs about one L2 round trip,
+// not one per float4; token and chunk indices come from the loop structure and shifts
+// (S is a power of two), not from divisions.  Ends without a barrier: the caller
+// synchronizes the CTA before the staged x is read.
+template <int FMT, int NTOK>
+__device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const (&rows)[NTOK], int n_in, int spr,
+                                        int live = NTOK) {
+    constexpr int S = Fmt<FMT>::kW / 4;
+    constexpr int kCS = NTOK * S + 1;
+    float4* xs = reinterpret_cast<float4*>(smem);
+    const int n4 = n_in >> 2;
+    const int nchunks = n_in / Fmt<FMT>::kW;
+    constexpr int kXG = NTOK >= 8 ? 1 : 8 / NTOK;   // float4 columns per thread and batch
+    const int nt = int(blockDim.x);
+    for (int g0 = threadIdx.x; g0 < n4; g0 += kXG * nt) {
+        float4 v[kXG][NTOK];
+#pragma unroll
+        for (int j = 0; j < kXG; ++j) {
+            const int g = g0 + j * nt;
+#pragma unroll
+            for (int t = 0; t < NTOK; ++t)
+                if (g < n4 && t < live) v[j][t] = __ldg(rows[t] + g);
+        }
+#pragma unroll
+        for (int j = 0; j < kXG; ++j) {
+            const int g = g0 + j * nt;
+            if (g < n4) {
+                float4* dst = xs + (g / S) * kCS + (g % S);
+#pragma unroll
+                for (int t = 0; t < NTOK; ++t) {
+                    if (t >= live) break;
+                    float4 w = v[j][t];
+                    if constexpr (FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64) {
+                        // column j is used as q*16^(j%4): store x * 16^-(j%4) (exact)
+                        w.y *= 0.0625f;
+                        w.z *= 0.00390625f;
+                        w.w *= 0.000244140625f;
+                    }
+                    dst[t * S] = w;
+                }
+            }
+        }
+    }
+    if constexpr (FMT == QG_AFFINE4_G64) {
+        float* xf = reinterpret_cast<float*>(smem);
+        for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {   // (padding chunks stay 0)
+#pragma unroll 1
+            for (int t = 0; t < live; ++t) {
+                // rows[t] by selects (a rolled loop must not index the array: that
+                // would put it in local memory)
+                const float4* rt = rows[0];
+#pragma unroll
+                for (int u = 1; u < NTOK; ++u) rt = (t == u) ? rows[u] : rt;
+                const float4* src = rt + S * c;
+                float sum = 0.f;
+#pragma unroll
+                for (int q = 0; q < S; ++q) {
+                    const float4 v = __ldg(src + q);
+                    sum = __fadd_rn(sum, v.x); sum = __fadd_rn(sum, v.y);
+                    sum = __fadd_rn(sum, v.z); sum = __fadd_rn(sum, v.w);
+                }
+                xf[(c * kCS + NTOK * S) * 4 + t] = sum;
+            }
+        }
+    }
+    // Chunks past n_in (the lanes past a row's short last step) read as zero.
+    for (int i = nchunks * kCS + int(threadIdx.x); i < spr * 32 * kCS; i += int(blockDim.x))
+        xs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// A lane's accumulators for one row group: per (row, token) one fp32 sum of scaled
+// chunk sums, or (BF16, no scales) a pair of partial sums over the whole row.
+template <int FMT, int NTOK, int RPW> struct Acc {
+    static constexpr bool kPair = (FMT == QG_BF16);
+    float s[RPW][NTOK];
+    f2_t p[kPair ? RPW : 1][kPair ? NTOK : 1];
+    __device__ __forceinline__ void clear() {
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+#pragma unroll
+            for (int t = 0; t < NTOK; ++t) s[r][t] = 0.f;
+#pragma unroll
+        for (int r = 0; r < (kPair ? RPW : 1); ++r)
+#pragma unroll
+            for (int t = 0; t < (kPair ? NTOK : 1); ++t) p[r][t] = 0ull;
+    }
+    // The lane's sum for output j = r * NTOK + t (j < RPW * NTOK).
+    __device__ __forceinline__ float value(int j) const {
+        if constexpr (kPair) return f2_sum(p[j / NTOK][j % NTOK]);
+        else return s[j / NTOK][j % NTOK];
+    }
+};
+
+// One ring stage into the accumulators: the lane's 16-byte code chunk of each of the
+// RPW rows (at `codes` + r * full step), the chunk's scale word (at `scales` + r * full
+// step), the lane's staged x chunk at `xr` (a layout for XT >= NTOK tokens; tokens
+// 0..NTOK-1 are used).  Within the chunk a pair of partial sums (even / odd columns)
+// per (row, token) is advanced by packed FMAs, then added and scaled once.
+template <int FMT, int NTOK, int RPW, int XT = NTOK>
+__device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uint32_t codes, uint32_t scales,
+                                         uint32_t magic) {
+    using F = Fmt<FMT>;
+    constexpr int S = F::kW / 4;
+    constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
+    constexpr bool kPairAcc = Acc<FMT, NTOK, RPW>::kPair;
+    uint4 qv[RPW];
+    uint32_t sv[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        qv[r] = lds128(codes + r * kFullStep);
+        sv[r] = F::scale(scales + r * kFullStep);
+    }
+    f2_t p[kPairAcc ? 1 : RPW][kPairAcc ? 1 : NTOK];
+#pragma unroll
+    for (int r = 0; r < (kPairAcc ? 1 : RPW); ++r)
+#pragma unroll
+        for (int t = 0; t < (kPairAcc ? 1 : NTOK); ++t) p[r][t] = 0ull;
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+        f2_t x01[NTOK], x23[NTOK];
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t) lds_f2x2(xr + 16u * uint32_t(t * S + i), x01[t], x23[t]);
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            f2_t wlo, whi;
+            F::dec(qv[r], i, wlo, whi, magic);
+#pragma unroll
+            for (int t = 0; t < NTOK; ++t) {
+                f2_t& pp = [&]() -> f2_t& {
+                    if constexpr (kPairAcc) return A.p[r][t]; else return p[r][t];
+                }();
+                pp = f2_fma(wlo, x01[t], pp);
+                pp = f2_fma(whi, x23[t], pp);
+            }
+        }
+    }
+    if constexpr (FMT == QG_Q8_0 || FMT == QG_Q4_0) {
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const float d = h2f(sv[r]);
+#pragma unroll
+            for (int t = 0; t < NTOK; ++t)
+                A.s[r][t] = __fmaf_rn(d, f2_sum(p[r][t]), A.s[r][t]);
+        }
+    } else if constexpr (FMT == QG_AFFINE4_G64) {
+        float csv[4];
+        {
+            const uint4 cv = lds128(xr + 16u * uint32_t(XT * S));
+            csv[0] = __uint_as_float(cv.x); csv[1] = __uint_as_float(cv.y);
+            csv[2] = __uint_as_float(cv.z); csv[3] = __uint_as_float(cv.w);
+        }
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const float s = h2f(sv[r] & 0xFFFFu), b = h2f(sv[r] >> 16);
+#pragma unroll
+            for (int t = 0; t < NTOK; ++t)
+                A.s[r][t] = __fmaf_rn(s, f2_sum(p[r][t]), __fmaf_rn(b, csv[t], A.s[r][t]));
+        }
+    }
+}
+
+// Transposed warp reduction of the V = RPW * NTOK lane sums (reduce-scatter by
+// halving, then xor steps): lane l returns the full sum of output l / (32 / VP).
+// The order depends only on V's power-of-two size, never on the data.
+template <int FMT, int NTOK, int RPW>
+__device__ __forceinline__ float warp_reduce(const Acc<FMT, NTOK, RPW>& A, int lane) {
+    constexpr int V = RPW * NTOK;
+    constexpr int VP = Pow2Up<V>::value;
+    constexpr int LG = Log2<VP>::value;
+    float v[VP];
+#pragma unroll
+    for (int j = 0; j < VP; ++j) v[j] = j < V ? A.value(j) : 0.f;
+#pragma unroll
+    for (int s = 0; s < LG; ++s) {
+        const int h = VP >> (s + 1);
+        const int mask = 16 >> s;
+        const bool upper = (lane & mask) != 0;
+#pragma unroll
+        for (int j = 0; j < h; ++j) {
+            const float send = upper ? v[j] : v[j + h];
+            const float keep = upper ? v[j + h] : v[j];
+            v[j] = keep + __shfl_xor_sync(kFull, send, mask);
+        }
+    }
+#pragma unroll
+    for (int mask = 16 >> LG; mask >= 1; mask >>= 1) v[0] += __shfl_xor_sync(kFull, v[0], mask);
+    return v[0];
+}
+
 // ------------------------------------------------------------------------------ kernel
 
 // Threads per CTA a kernel allows: 512 (16 warps), or 384 (12 warps) where a warp
@@ -350,7 +545,6 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
     constexpr int V = RPW * NTOK;                   // outputs per row group
     constexpr int VP = Pow2Up<V>::value;
     static_assert(VP >= V && VP <= 32, "butterfly width");
-    constexpr int LG = Log2<VP>::value;
     constexpr int SPAN = 32 / VP;                   // lanes sharing one reduced value
     constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
     constexpr int kStage = stage_bytes(FMT, RPW);   // ring stage: RPW rows of one step
@@ -360,7 +554,6 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
     extern __shared__ __align__(128) unsigned char smem[];
     const int n_in = a.n_in;
     const int n4 = n_in >> 2;
-    const int nchunks = n_in / F::kW;
     const int codes = FMT == QG_Q8_0 ? n_in : FMT == QG_BF16 ? 2 * n_in : n_in / 2;
     const int spr = (codes + 511) >> 9;             // steps per row
     const int last_codes = codes - 512 * (spr - 1);
@@ -388,7 +581,6 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
 
     constexpr int kCS = NTOK * S + 1;               // float4 slots per chunk in staged x
     const SmemPlan plan = smem_plan(FMT, NTOK, n_in, RPW, depth, nwarps, P);
-    float4* xs = reinterpret_cast<float4*>(smem);   // [nchunks][kCS]
     const uint32_t xs_base = smem_addr(smem);
     const uint32_t bars = smem_addr(smem + plan.bar_off) + warp * depth * 8;
     const uint32_t ring = ((smem_addr(smem + plan.ring_off) + 127u) & ~127u) + uint32_t(warp * depth * kStage);
@@ -442,62 +634,13 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
     // argmax workspace): wait for it to complete (a no-op without the early start).
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // ---- stage x (overlaps the first copies).  Each thread issues all its loads
-    // of a batch before its first store, so staging costs about one L2 round trip,
-    // not one per float4; token and chunk indices come from the loop structure and
-    // shifts (S is a power of two), not from divisions.
+    // ---- stage x (overlaps the first copies)
     {
         const float4* x4 = reinterpret_cast<const float4*>(a.x);
-        constexpr int kXG = NTOK >= 8 ? 1 : 8 / NTOK;   // float4 columns per thread and batch
-        const int nt = int(blockDim.x);
-        for (int g0 = threadIdx.x; g0 < n4; g0 += kXG * nt) {
-            float4 v[kXG][NTOK];
+        const float4* rows[NTOK];
 #pragma unroll
-            for (int j = 0; j < kXG; ++j) {
-                const int g = g0 + j * nt;
-#pragma unroll
-                for (int t = 0; t < NTOK; ++t)
-                    if (g < n4) v[j][t] = __ldg(x4 + t * n4 + g);
-            }
-#pragma unroll
-            for (int j = 0; j < kXG; ++j) {
-                const int g = g0 + j * nt;
-                if (g < n4) {
-                    float4* dst = xs + (g / S) * kCS + (g % S);
-#pragma unroll
-                    for (int t = 0; t < NTOK; ++t) {
-                        float4 w = v[j][t];
-                        if constexpr (FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64) {
-                            // column j is used as q*16^(j%4): store x * 16^-(j%4) (exact)
-                            w.y *= 0.0625f;
-                            w.z *= 0.00390625f;
-                            w.w *= 0.000244140625f;
-                        }
-                        dst[t * S] = w;
-                    }
-                }
-            }
-        }
-        if constexpr (FMT == QG_AFFINE4_G64) {
-            float* xf = reinterpret_cast<float*>(smem);
-            for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {   // (padding chunks stay 0)
-#pragma unroll 1
-                for (int t = 0; t < NTOK; ++t) {
-                    const float4* src = x4 + t * n4 + S * c;
-                    float sum = 0.f;
-#pragma unroll
-                    for (int q = 0; q < S; ++q) {
-                        const float4 v = __ldg(src + q);
-                        sum = __fadd_rn(sum, v.x); sum = __fadd_rn(sum, v.y);
-                        sum = __fadd_rn(sum, v.z); sum = __fadd_rn(sum, v.w);
-                    }
-                    xf[(c * kCS + NTOK * S) * 4 + t] = sum;
-                }
-            }
-        }
-        // Chunks past n_in (the lanes past a row's short last step) read as zero.
-        for (int i = nchunks * kCS + int(threadIdx.x); i < spr * 32 * kCS; i += int(blockDim.x))
-            xs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int t = 0; t < NTOK; ++t) rows[t] = x4 + t * n4;
+        stage_x<FMT, NTOK>(smem, rows, n_in, spr);
     }
     __syncthreads();
 
@@ -508,20 +651,8 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
     const uint32_t code_lane = ring + 16u * uint32_t(lane);
     const uint32_t scale_lane = ring + F::scale_off(lane);
 
-    // Per (row, token): within a chunk a pair of partial sums (even / odd columns),
-    // then added and scaled into one fp32 accumulator.  BF16 (no scales) keeps the
-    // pair over the whole row.
-    constexpr bool kPairAcc = (FMT == QG_BF16);
-    float acc[RPW][NTOK];
-    f2_t acc2[kPairAcc ? RPW : 1][kPairAcc ? NTOK : 1];
-#pragma unroll
-    for (int r = 0; r < RPW; ++r)
-#pragma unroll
-        for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.f;
-#pragma unroll
-    for (int r = 0; r < (kPairAcc ? RPW : 1); ++r)
-#pragma unroll
-        for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = 0ull;
+    Acc<FMT, NTOK, RPW> acc;
+    acc.clear();
 
     int gc = gw, sc = 0;
     uint32_t consumed = 0, phase = 0, jg = 0;       // jg: row groups this warp has finished
@@ -537,62 +668,9 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
         // scale bytes with a zero scale, against zero-padded x: they add exact zeros.
         const int codes_k = (kc == spr - 1) ? last_codes : 512;
         {
-            const uint32_t xr = x_lane + uint32_t(kc) * (32u * kCS * 16u);
             const uint32_t stage = uint32_t(sc) * uint32_t(kStage);
-            uint4 qv[RPW];
-            uint32_t sv[RPW];
-#pragma unroll
-            for (int r = 0; r < RPW; ++r) {
-                qv[r] = lds128(code_lane + stage + r * kFullStep);
-                sv[r] = F::scale(scale_lane + stage + uint32_t(codes_k) + r * kFullStep);
-            }
-            f2_t p[kPairAcc ? 1 : RPW][kPairAcc ? 1 : NTOK];
-#pragma unroll
-            for (int r = 0; r < (kPairAcc ? 1 : RPW); ++r)
-#pragma unroll
-                for (int t = 0; t < (kPairAcc ? 1 : NTOK); ++t) p[r][t] = 0ull;
-#pragma unroll
-            for (int i = 0; i < S; ++i) {
-                f2_t x01[NTOK], x23[NTOK];
-#pragma unroll
-                for (int t = 0; t < NTOK; ++t) lds_f2x2(xr + 16u * uint32_t(t * S + i), x01[t], x23[t]);
-#pragma unroll
-                for (int r = 0; r < RPW; ++r) {
-                    f2_t wlo, whi;
-                    F::dec(qv[r], i, wlo, whi, magic);
-#pragma unroll
-                    for (int t = 0; t < NTOK; ++t) {
-                        f2_t& pp = [&]() -> f2_t& {
-                            if constexpr (kPairAcc) return acc2[r][t]; else return p[r][t];
-                        }();
-                        pp = f2_fma(wlo, x01[t], pp);
-                        pp = f2_fma(whi, x23[t], pp);
-                    }
-                }
-            }
-            if constexpr (FMT == QG_Q8_0 || FMT == QG_Q4_0) {
-#pragma unroll
-                for (int r = 0; r < RPW; ++r) {
-                    const float d = h2f(sv[r]);
-#pragma unroll
-                    for (int t = 0; t < NTOK; ++t)
-                        acc[r][t] = __fmaf_rn(d, f2_sum(p[r][t]), acc[r][t]);
-                }
-            } else if constexpr (FMT == QG_AFFINE4_G64) {
-                float csv[4];
-                {
-                    const uint4 cv = lds128(xr + 16u * uint32_t(NTOK * S));
-                    csv[0] = __uint_as_float(cv.x); csv[1] = __uint_as_float(cv.y);
-                    csv[2] = __uint_as_float(cv.z); csv[3] = __uint_as_float(cv.w);
-                }
-#pragma unroll
-                for (int r = 0; r < RPW; ++r) {
-                    const float s = h2f(sv[r] & 0xFFFFu), b = h2f(sv[r] >> 16);
-#pragma unroll
-                    for (int t = 0; t < NTOK; ++t)
-                        acc[r][t] = __fmaf_rn(s, f2_sum(p[r][t]), __fmaf_rn(b, csv[t], acc[r][t]));
-                }
-            }
+            step_fma<FMT, NTOK, RPW>(acc, x_lane + uint32_t(kc) * (32u * kCS * 16u), code_lane + stage,
+                                     scale_lane + stage + uint32_t(codes_k), magic);
         }
         __syncwarp();          // every lane has read this stage before it is refilled
         issue();
@@ -601,28 +679,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
       if (failed) break;
         {
             // ---- finish the row group: transposed warp reduction
-            float v[VP];
-#pragma unroll
-            for (int j = 0; j < VP; ++j) {
-                if constexpr (kPairAcc)
-                    v[j] = j < V ? f2_sum(acc2[j / NTOK][j % NTOK]) : 0.f;
-                else
-                    v[j] = j < V ? acc[j / NTOK][j % NTOK] : 0.f;
-            }
-#pragma unroll
-            for (int s = 0; s < LG; ++s) {
-                const int h = VP >> (s + 1);
-                const int mask = 16 >> s;
-                const bool upper = (lane & mask) != 0;
-#pragma unroll
-                for (int j = 0; j < h; ++j) {
-                    const float send = upper ? v[j] : v[j + h];
-                    const float keep = upper ? v[j + h] : v[j];
-                    v[j] = keep + __shfl_xor_sync(kFull, send, mask);
-                }
-            }
-#pragma unroll
-            for (int mask = 16 >> LG; mask >= 1; mask >>= 1) v[0] += __shfl_xor_sync(kFull, v[0], mask);
+            float v0 = warp_reduce<FMT, NTOK, RPW>(acc, lane);
             const int vi = lane / SPAN;                       // value index this lane holds
             const bool holder = vi < V && (lane % SPAN) == 0;
             if (SPLIT && P > 1) {
@@ -636,7 +693,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
                         failed = true;
                         break;
                     }
-                    if (holder) slot[(seg - 1) * 32 + vi] = v[0];
+                    if (holder) slot[(seg - 1) * 32 + vi] = v0;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(tbar + 8 * par);
                 } else {
@@ -645,7 +702,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
                         break;
                     }
                     if (holder)
-                        for (int q = 0; q < P - 1; ++q) v[0] += slot[q * 32 + vi];
+                        for (int q = 0; q < P - 1; ++q) v0 += slot[q * 32 + vi];
                     __syncwarp();
                     if (lane == 0) mbar_arrive(tbar + 16 + 8 * par);
                 }
@@ -655,18 +712,11 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
                 const int r = vi / NTOK, t = vi - r * NTOK;
                 const long long row = (long long)gc * RPW + r;
                 if (row < a.n_out) {
-                    if (!ARGMAX || a.y) a.y[(long long)t * a.n_out + row] = v[0];
-                    if (ARGMAX && better(v[0], int(row), best_v, best_i)) { best_v = v[0]; best_i = int(row); }
+                    if (!ARGMAX || a.y) a.y[(long long)t * a.n_out + row] = v0;
+                    if (ARGMAX && better(v0, int(row), best_v, best_i)) { best_v = v0; best_i = int(row); }
                 }
             }
-#pragma unroll
-            for (int r = 0; r < RPW; ++r)
-#pragma unroll
-                for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.f;
-#pragma unroll
-            for (int r = 0; r < (kPairAcc ? RPW : 1); ++r)
-#pragma unroll
-                for (int t = 0; t < (kPairAcc ? NTOK : 1); ++t) acc2[r][t] = 0ull;
+            acc.clear();
         }
     }
 

@@ -108,6 +108,18 @@ Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
     return t;
 }
 
+Tile select_expert_tile(int fmt, int64_t n_out, int64_t n_in) {
+    (void)fmt;
+    (void)n_out;
+    (void)n_in;
+    Tile t;
+    t.rpw = 2;
+    t.depth = 3;
+    t.warps = 16;
+    t.ctas = 1;
+    return t;
+}
+
 int select_split(int fmt, int64_t n_out, int64_t n_in) {
     // Matrices with 8192 rows or more have row groups for every warp of the GPU
     // (at 4 rows per warp) and short rows gain nothing from a team (measured on

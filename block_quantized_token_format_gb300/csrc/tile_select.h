@@ -35,6 +35,10 @@ constexpr int kMaxSplit = 4;
 // The geometry for a call, before the override and the occupancy cap.
 Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok);
 
+// The geometry of the expert-grouped mat-vec (rpw 1, 2 or 4; no split) for one
+// expert's shape, before the override and the occupancy cap.
+Tile select_expert_tile(int fmt, int64_t n_out, int64_t n_in);
+
 // Apply an override on top of a selected tile.
 Tile apply_override(Tile t, const TileOverride& o);
 

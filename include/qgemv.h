@@ -173,6 +173,64 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
                            const int32_t* ids, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/* ------------------------------------------------------------ routed experts
+ * The routed-expert projections of a mixture-of-experts layer at ntok <= 4 (Track
+ * 2 Audit & Optimization Report, M5 Metal kernels, section 1 item 2, and table
+ * 2.2): a plan groups the step's (token, choice) pairs by expert, and each
+ * projection multiplies every group's expert once by the group's ne = 1..4 rows,
+ * so each active expert's weights are read once per projection.
+ *
+ * qg_expert_plan: ids = device int32 [ntok][topk] (4-byte aligned), the expert of
+ *   token t's choice j; pair i = t * topk + j; 1 <= ntok * topk <= 1024.  Writes
+ *   the plan, qg_expert_plan_ints(ntok * topk) device int32 (caller-allocated,
+ *   4-byte aligned), for G = ntok * topk slots:
+ *     plan[0]                      n_groups
+ *     plan[1 + g], g = 0..G        group_start: group g holds slots
+ *                                  [group_start[g], group_start[g + 1]); entries
+ *                                  n_groups..G hold G
+ *     plan[2 + G + g], g < G       group_expert (-1 from n_groups on)
+ *     plan[2 + 2G + s], s < G      slot_pair: the pair i in slot s
+ *     plan[2 + 3G + s], s < G      slot_token = slot_pair / topk
+ *     plan[2 + 4G + i], i < G      pair_slot: the slot of pair i
+ *   Groups come in increasing expert id; a group's slots hold its pairs in
+ *   increasing i; an expert with more than four pairs continues in the next
+ *   group, four pairs at a time (the pages' plan has one group per expert; with
+ *   ntok <= 4 and distinct experts per token the two agree).  An id outside
+ *   [0, n_experts) sets QG_DEVICE_BAD_PLAN and writes n_groups = 0 (the rest of the
+ *   plan is then unspecified).  One CTA, asynchronous on `stream`.  Errors:
+ *   QG_EINVAL (null pointer, ntok, topk or n_experts < 1, ntok * topk > 1024),
+ *   QG_EALIGN, QG_ECUDA.
+ *
+ * qgemv_experts: for every slot s of group g with e = group_expert[g],
+ *     y[s][o] = sum_i dequant(W_e)[o][i] * x_row(s)[i],   o < n_out,
+ *   where W_e = rows [e * n_out, (e + 1) * n_out) of W, the n_experts matrices
+ *   stacked and packed as one (n_experts * n_out)-row matrix in the device layout
+ *   (16-byte aligned), and x_row(s) = x[slot_token[s]] (x_by_slot = 0: the gate /
+ *   up projections read the step's token rows) or x[s] (x_by_slot = 1: the down
+ *   projection reads one activation row per slot).  x: device fp32 [n_x][n_in],
+ *   16-byte aligned.  y: device fp32 [n_slots][n_out], 4-byte aligned.  plan: as
+ *   written by qg_expert_plan for n_slots = ntok * topk (or by the caller to the
+ *   same layout).  The kernel reads n_groups and the groups from device memory;
+ *   a plan entry out of range (n_groups > n_slots, a group of 0 or more than 4
+ *   slots, an expert outside the stack, a row outside x) skips that group and
+ *   sets QG_DEVICE_BAD_PLAN.  Each output is bitwise the same for every ne, group
+ *   and geometry, and equals qgemv's on the expert's rows whenever that call does
+ *   not split (qg_describe_tile shows split=1).  Errors: QG_EINVAL (format, shape,
+ *   n_experts * n_out >= 2^31, n_slots outside 1..1024, n_x < 1, x_by_slot not 0
+ *   or 1, n_x < n_slots with x_by_slot = 1, null pointer), QG_EALIGN,
+ *   QG_EUNSUPPORTED, QG_ECUDA.  The geometry follows qg_set_tile_override's rpw,
+ *   depth, warps and ctas (rpw 1, 2 or 4; the split does not apply). */
+#define QG_DEVICE_BAD_PLAN 4u
+/* qg_describe_expert_tile: the geometry qgemv_experts would use for one expert's
+ * shape, written as qg_describe_tile does. */
+size_t    qg_expert_plan_ints(int64_t n_pairs);
+qg_status qg_expert_plan(const int32_t* ids, int ntok, int topk, int n_experts, int32_t* plan,
+                         void* stream);
+qg_status qgemv_experts(qg_fmt fmt, const void* W, int64_t n_experts, int64_t n_out, int64_t n_in,
+                        const float* x, int64_t n_x, int x_by_slot, const int32_t* plan,
+                        int64_t n_slots, float* y, void* stream);
+qg_status qg_describe_expert_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, char* buf, size_t len);
+
 /* ------------------------------------------------------- qgemv_argmax_noalloc
  * No counterpart on the source pages: an addition for callers that cannot call
  * cudaMalloc, such as a plugin inside a host framework that owns every device
@@ -253,7 +311,8 @@ qg_status qg_set_launch_options(unsigned int flags);
  * QG_DEVICE_WAIT_TIMEOUT in a per-device status word, stops issuing copies,
  * drains the copies it already issued (again bounded) and exits normally; its
  * outputs are then not valid.  qg_gather_rows sets QG_DEVICE_BAD_ROW_ID when a
- * listed id is outside the head.  qg_device_status copies the current device's
+ * listed id is outside the head; qg_expert_plan and qgemv_experts set
+ * QG_DEVICE_BAD_PLAN on a routed id or plan entry out of range.  qg_device_status copies the current device's
  * word into *status (synchronously: it waits for the device) and, if `clear`,
  * resets it to 0. */
 #define QG_DEVICE_WAIT_TIMEOUT 1u

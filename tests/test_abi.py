@@ -90,6 +90,37 @@ def test_draft_ids_calls_reject_before_launch():
     assert lib.qgemv_argmax_ids(0, A, 100, 256, A, A, A, 5, A, A, ws, None) == -1        # ntok 5
 
 
+def test_expert_calls_reject_before_launch():
+    lib = qg.load_library()
+    assert qg.qg_expert_plan_ints(40) == 2 + 5 * 40
+    assert qg.qg_expert_plan_ints(0) == 0 and qg.qg_expert_plan_ints(1025) == 0
+    # qg_expert_plan(ids, ntok, topk, n_experts, plan, stream)
+    assert lib.qg_expert_plan(None, 4, 10, 512, A, None) == -1
+    assert lib.qg_expert_plan(A, 4, 10, 512, None, None) == -1
+    assert lib.qg_expert_plan(A, 0, 10, 512, A, None) == -1
+    assert lib.qg_expert_plan(A, 4, 0, 512, A, None) == -1
+    assert lib.qg_expert_plan(A, 4, 10, 0, A, None) == -1
+    assert lib.qg_expert_plan(A, 64, 17, 512, A, None) == -1          # 1088 pairs > 1024
+    assert lib.qg_expert_plan(A + 2, 4, 10, 512, A, None) == -2
+    assert lib.qg_expert_plan(A, 4, 10, 512, A + 2, None) == -2
+    # qgemv_experts(fmt, W, n_experts, n_out, n_in, x, n_x, x_by_slot, plan, n_slots, y, stream)
+    ok = (0, A, 8, 64, 256, A, 4, 0, A, 40, A)
+    def call(**kw):
+        names = ["fmt", "W", "ne", "no", "ni", "x", "nx", "bs", "plan", "ns", "y"]
+        args = dict(zip(names, ok))
+        args.update(kw)
+        return lib.qgemv_experts(*[args[n] for n in names], None)
+    assert call(fmt=9) == -1
+    assert call(ne=0) == -1 and call(no=0) == -1
+    assert call(ne=1 << 20, no=1 << 12) == -1                            # stack of 2^32 rows
+    assert call(ni=48) == -1                                             # n_in not a multiple of 32
+    assert call(ns=0) == -1 and call(ns=1025) == -1
+    assert call(nx=0) == -1 and call(bs=2) == -1
+    assert call(bs=1, nx=39) == -1                                      # one x row per slot needed
+    assert call(W=None) == -1 and call(x=None) == -1 and call(plan=None) == -1 and call(y=None) == -1
+    assert call(W=A + 8) == -2 and call(x=A + 4) == -2 and call(plan=A + 2) == -2 and call(y=A + 2) == -2
+
+
 def test_tile_override_grammar():
     lib = qg.load_library()
     for good in (b"rpw=4", b"depth=2,rpw=1", b"rpw=2,depth=4,warps=8,ctas=2", b"", None, b"rpw=1,", b"rpw=8", b"split=3,rpw=2", b"rpw=3", b"rpw=5", b"rpw=6"):

@@ -64,6 +64,34 @@ DRAFT_IDS = {"q8_0_head_248320x2560": (106299, 131)}
 DENSE_SET = ["q8_0_6144x2560", "q8_0_10240x2560", "q8_0_12288x2560", "q8_0_2560x6144"]
 
 
+@dataclass(frozen=True)
+class ExpertLayer:
+    """Routed experts of one mixture-of-experts layer: n_experts experts, each a gate
+    and an up projection d_model -> d_ff (stacked as 2 * d_ff rows: gate, then up)
+    and a down projection d_ff -> d_model; top-k routing with inter-token share."""
+    name: str
+    fmt: str
+    n_experts: int
+    d_model: int
+    d_ff: int
+    topk: int
+    share: float
+    seed: int
+
+
+# Routed experts at the size the routed-expert table implies (~1.46 MB per expert at
+# about 2.5 bits per weight: 2 x 2560 x 640 gate/up + 640 x 2560 down), 512 experts,
+# top-10 routing, 65% inter-token share; stored here in Q8_0.
+EXPERT_LAYERS: dict[str, ExpertLayer] = {e.name: e for e in [
+    ExpertLayer("q8_0_experts_512x2560x640_top10", "q8_0", 512, 2560, 640, 10, 0.65, 150),
+]}
+
+
+def expert_matrix(seed: int, e: int, n_out: int, n_in: int) -> np.ndarray:
+    """Expert e's fp32 matrix of a stack drawn from ``seed`` (its own weight seed)."""
+    return weights(seed * 65536 + e, n_out, n_in)
+
+
 def _chunk_rng(seed: int, chunk: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(chunk,))))
 
@@ -127,7 +155,10 @@ def routing(seed: int, ntok: int, topk: int, n_experts: int, share: float) -> np
     probability ``share``, an expert that an earlier token chose (uniform among those
     this token has not taken yet), otherwise draws one that no token has chosen yet;
     so about ``topk + (ntok - 1) * topk * (1 - share)`` experts are active in a step.
+    (When one of the two pools is empty the choice comes from the other.)
     """
+    if not 1 <= topk <= n_experts:
+        raise ValueError("need 1 <= topk <= n_experts")
     g = np.random.Generator(np.random.PCG64(seed))
     ids = np.zeros((ntok, topk), dtype=np.int32)
     used: list[int] = []
@@ -135,10 +166,10 @@ def routing(seed: int, ntok: int, topk: int, n_experts: int, share: float) -> np
         mine: list[int] = []
         for _ in range(topk):
             old = [e for e in used if e not in mine]
-            if t > 0 and old and g.random() < share:
+            free = np.setdiff1d(np.arange(n_experts), np.array(used + mine, dtype=np.int64))
+            if old and (len(free) == 0 or (t > 0 and g.random() < share)):
                 e = old[int(g.integers(len(old)))]
             else:
-                free = np.setdiff1d(np.arange(n_experts), np.array(used + mine, dtype=np.int64))
                 e = int(free[int(g.integers(len(free)))])
             mine.append(e)
         for e in mine:
