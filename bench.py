@@ -499,12 +499,14 @@ def detail_table(args, qg, torch, dev, l2, peak):
 
 
 def experts_detail(qg, torch, dev, peak, layer, unique=32, routings=64):
-    """Routed experts, one layer: the plan, the gate/up projection (token rows) and the
-    down projection (one activation row per slot) per ntok, each step with its own
-    seeded routing (64 routings in turn), timed as 64-step graphs.  Bytes = the
-    active experts' weight bytes (each read once per projection).  The stack holds
-    n_experts experts at their own addresses; their contents repeat every `unique`
-    experts (the data does not change the timing; the addresses do)."""
+    """Routed experts, one layer: the plan, the gate/up projection (token rows; it also
+    prefetches the same experts' down rows into L2) and the down projection (one
+    activation row per slot) per ntok, each step with its own seeded routing (64
+    routings in turn), timed as 64-step graphs.  Bytes = the active experts' weight
+    bytes (each read from HBM once per layer).  The stack holds n_experts experts at
+    their own addresses; their contents repeat every `unique` experts (the data does
+    not change the timing; the addresses do).  "gate_up" and "down" are timed alone
+    ("down" alone reads HBM; in "layer" it reads what gate/up prefetched)."""
     E, dm, ff = layer.n_experts, layer.d_model, layer.d_ff
     shapes = {"gu": (2 * ff, dm, layer.seed), "dn": (dm, ff, layer.seed + 1)}
     stacks = {}
@@ -540,11 +542,13 @@ def experts_detail(qg, torch, dev, peak, layer, unique=32, routings=64):
         def plan(r):
             qg.qg_expert_plan(ids[r], E, plans[r])
 
-        def gu(r):
-            qg.qgemv_experts(layer.fmt, stacks["gu"], E, 2 * ff, dm, x, plans[r], G, y_gu)
+        def gu(r):   # also prefetches the same experts' down rows into L2
+            qg.qgemv_experts(layer.fmt, stacks["gu"], E, 2 * ff, dm, x, plans[r], G, y_gu,
+                             W_next=stacks["dn"], next_n_out=dm, next_n_in=ff)
 
-        def dn(r):
-            qg.qgemv_experts(layer.fmt, stacks["dn"], E, dm, ff, h, plans[r], G, y_dn, x_by_slot=True)
+        def dn(r):   # the plan was written two launches back: its copies start before the wait
+            qg.qgemv_experts(layer.fmt, stacks["dn"], E, dm, ff, h, plans[r], G, y_dn, x_by_slot=True,
+                             plan_ready=True)
 
         def layer_step(r):
             plan(r)

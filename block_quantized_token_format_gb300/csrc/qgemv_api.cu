@@ -565,6 +565,10 @@ __global__ void __launch_bounds__(kMaxPlanPairs) expert_plan_kernel(const int32_
     __shared__ int e_s[kMaxPlanPairs];
     __shared__ int start_s[kMaxPlanPairs];
     __shared__ int slot_e[kMaxPlanPairs];
+    // Let the projections that follow start their prologue; the ids may come from
+    // the previous kernel.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int i = int(threadIdx.x);
     const int G = n;
     int e = -1;
@@ -623,10 +627,13 @@ qg_status plan_experts(int fmt, int64_t n_out, int64_t n_in, Plan* plan) {
         return true;
     };
     if (!cap_warps()) return QG_EUNSUPPORTED;
+    // Sized for the largest plan (1024 slots); a launch allocates what its plan needs.
     auto total = [&](int depth, int warps) {
-        return size_t(smem_plan(fmt, kMaxNtok, int(n_in), t.rpw, depth, warps, 1).total);
+        return size_t(plan_smem_off(smem_plan(fmt, kMaxNtok, int(n_in), t.rpw, depth, warps, 1).total));
     };
-    auto fits = [&]() { return total(t.depth, t.warps) + kStaticSmemReserve <= size_t(optin); };
+    auto fits = [&]() {
+        return total(t.depth, t.warps) + plan_smem_bytes(kMaxPlanPairs) + kStaticSmemReserve <= size_t(optin);
+    };
     while (!fits() && t.depth > 2) --t.depth;
     while (!fits() && t.warps > 1) --t.warps;
     while (!fits() && t.rpw > 1) {
@@ -635,9 +642,9 @@ qg_status plan_experts(int fmt, int64_t n_out, int64_t n_in, Plan* plan) {
         if (!cap_warps()) return QG_EUNSUPPORTED;
     }
     const size_t smem = total(t.depth, t.warps);
-    if (smem + kStaticSmemReserve > size_t(optin)) return QG_EUNSUPPORTED;
+    if (!fits()) return QG_EUNSUPPORTED;
     const int threads = 32 * t.warps;
-    const int occ = blocks_per_sm(fn, dev, optin, threads, smem);
+    const int occ = blocks_per_sm(fn, dev, optin, threads, smem + plan_smem_bytes(kMaxPlanPairs));
     if (occ < 1) return QG_EUNSUPPORTED;
     int64_t grid = int64_t(sms) * std::min(t.ctas, occ);
     if (grid > kMaxGrid) grid = kMaxGrid;
@@ -676,7 +683,7 @@ qg_status launch_experts(const Plan& p, const ExpertArgs& args, void* stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
     cfg.blockDim = dim3(p.threads);
-    cfg.dynamicSmemBytes = p.smem;
+    cfg.dynamicSmemBytes = p.smem + plan_smem_bytes(a.n_slots);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     if (launch_flags() & QG_LAUNCH_EARLY_START) {
@@ -708,21 +715,39 @@ qg_status qg_expert_plan(const int32_t* ids, int ntok, int topk, int n_experts, 
     qg_status st = device_info(&dev, &sms, &optin, &status);
     if (st != QG_OK) return st;
     const int n = ntok * topk;
-    expert_plan_kernel<<<1, (n + 31) / 32 * 32, 0, static_cast<cudaStream_t>(stream)>>>(ids, n, topk, n_experts, plan,
-                                                                                         status);
-    if (cudaGetLastError() != cudaSuccess) return QG_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3((n + 31) / 32 * 32);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    if (launch_flags() & QG_LAUNCH_EARLY_START) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&cfg, expert_plan_kernel, ids, n, topk, n_experts, plan, status) != cudaSuccess) {
+        cudaGetLastError();
+        return QG_ECUDA;
+    }
     return QG_OK;
 }
 
 qg_status qgemv_experts(qg_fmt fmt, const void* W, int64_t n_experts, int64_t n_out, int64_t n_in, const float* x,
-                        int64_t n_x, int x_by_slot, const int32_t* plan, int64_t n_slots, float* y, void* stream) {
+                        int64_t n_x, unsigned int flags, const int32_t* plan, int64_t n_slots, float* y,
+                        const void* W_next, int64_t next_n_out, int64_t next_n_in, void* stream) {
     if (n_experts < 1 || n_out < 1 || n_experts > ((int64_t(1) << 31) - 1) / n_out) return QG_EINVAL;
     if (!shape_valid(fmt, n_experts * n_out, n_in)) return QG_EINVAL;
     if (n_slots < 1 || n_slots > kMaxPlanPairs || n_x < 1 || n_x > (int64_t(1) << 31) - 1) return QG_EINVAL;
-    if (x_by_slot != 0 && x_by_slot != 1) return QG_EINVAL;
-    if (x_by_slot == 1 && n_x < n_slots) return QG_EINVAL;
+    if (flags & ~(QG_EXPERTS_X_BY_SLOT | QG_EXPERTS_PLAN_READY)) return QG_EINVAL;
+    if ((flags & QG_EXPERTS_X_BY_SLOT) && n_x < n_slots) return QG_EINVAL;
     if (!W || !x || !plan || !y) return QG_EINVAL;
-    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(plan, 4) || !aligned(y, 4)) return QG_EALIGN;
+    if (W_next) {
+        if (next_n_out < 1 || n_experts > ((int64_t(1) << 31) - 1) / next_n_out) return QG_EINVAL;
+        if (!shape_valid(fmt, n_experts * next_n_out, next_n_in)) return QG_EINVAL;
+    }
+    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(plan, 4) || !aligned(y, 4) || !aligned(W_next, 16))
+        return QG_EALIGN;
     Plan p;
     qg_status st = plan_experts_cached(fmt, n_out, n_in, &p);
     if (st != QG_OK) return st;
@@ -738,13 +763,15 @@ qg_status qgemv_experts(qg_fmt fmt, const void* W, int64_t n_experts, int64_t n_
     a.n_in = int(n_in);
     a.n_slots = int(n_slots);
     a.n_x = int(n_x);
-    a.x_by_slot = x_by_slot;
+    a.flags = flags;
     a.depth = p.tile.depth;
     a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
     a.drain_limit = std::max<uint32_t>(a.wait_limit, 1u << 16);
     a.test_extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
     a.fmagic = 0x4B000000u;
     a.stage_tx = uint32_t(p.tile.rpw * full_step_bytes(fmt));
+    a.next_w = static_cast<const unsigned char*>(W_next);
+    a.next_bytes = W_next ? (long long)(next_n_out * row_stride(fmt, next_n_in)) : 0;
     return launch_experts(p, a, stream);
 }
 

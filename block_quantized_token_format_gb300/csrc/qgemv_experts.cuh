@@ -20,6 +20,13 @@
 // x is staged.  With more groups than CTAs, a CTA takes groups b, b + C, ...
 // one after the other, restaging x between them.
 //
+// Optionally a launch also prefetches into L2 the same experts' rows of the NEXT
+// projection's stack (the down projection while gate/up runs): the 129 MB L2
+// holds a step's active experts, so the next launch's first copies hit L2 instead
+// of waiting for HBM, and HBM keeps streaming across the launch boundary.  The
+// prefetch is spread over the group's CTAs: one SM's bulk-copy engine alone
+// would issue it far too slowly.
+//
 // The addition order of an output depends only on (fmt, n_in): it is the order of
 // the plain mat-vec without a split, whatever ne, the group, the tile or the grid.
 #pragma once
@@ -29,6 +36,8 @@
 namespace qg {
 
 constexpr unsigned kStatusBadPlan = 4u;   // a plan entry or a routed expert id out of range
+constexpr unsigned kExpertsXBySlot = QG_EXPERTS_X_BY_SLOT;
+constexpr unsigned kExpertsPlanReady = QG_EXPERTS_PLAN_READY;
 constexpr int kMaxPlanPairs = 1024;      // (token, choice) pairs one plan can hold
 
 // Offsets (in int32 entries) of the plan's arrays for n_slots = ntok * topk slots.
@@ -38,6 +47,11 @@ __host__ __device__ constexpr int plan_slot_pair(int G) { return 2 + 2 * G; }
 __host__ __device__ constexpr int plan_slot_token(int G) { return 2 + 3 * G; }
 __host__ __device__ constexpr int plan_pair_slot(int G) { return 2 + 4 * G; }
 __host__ __device__ constexpr int plan_ints(int G) { return 2 + 5 * G; }
+
+// The expert kernel's shared memory: the mat-vec layout for kMaxNtok tokens (x,
+// barriers, rings), then the plan's group arrays and slot tokens, 2 + 3G ints.
+__host__ __device__ constexpr int plan_smem_off(int plan_total) { return (plan_total + 15) / 16 * 16; }
+__host__ __device__ constexpr int plan_smem_bytes(int G) { return (2 + 3 * G) * 4; }
 
 struct ExpertArgs {
     CUtensorMap wmap;          // the stacked experts' packed rows as [n_experts * n_out][stride / 8]
@@ -51,11 +65,23 @@ struct ExpertArgs {
     int n_in;
     int n_slots;
     int n_x;                   // rows of x
-    int x_by_slot;             // 0: slot s reads x[slot_token[s]]; 1: slot s reads x[s]
+    unsigned flags;            // kExpertsXBySlot: slot s reads x[s] (else x[slot_token[s]]);
+                               // kExpertsPlanReady: the plan is complete when the launch begins
     int depth;
     uint32_t wait_limit, drain_limit, stage_tx, fmagic;
     uint32_t test_extra_tx;    // test hook: bytes added to every warp's first expected transaction
+    const unsigned char* next_w;   // optional: a second stack of the same experts whose active
+                                   // experts this launch prefetches into L2 (nullptr = none)
+    long long next_bytes;          // bytes per expert of that stack (a multiple of 16)
 };
+
+constexpr int kPrefetchPiece = 32768;   // bytes per L2 prefetch instruction
+
+// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
 
 // One warp's ring over the groups a CTA serves: the issue cursor (row block, step,
 // stage) runs `depth` steps ahead of the consume cursor (stage, phase).  All
@@ -140,6 +166,40 @@ __device__ __forceinline__ void expert_group(const ExpertArgs& a, Ring& R, unsig
     }
 }
 
+// Group g of the plan in shared memory: its first slot, token count, expert and x
+// rows; false if any entry is out of range.  Every thread reads the same words, so
+// the result is CTA-uniform.
+__device__ __forceinline__ bool decode_group(const ExpertArgs& a, const int* ps, int G, int g, int& s0, int& ne,
+                                             int& e, int (&xrow)[kMaxNtok]) {
+    s0 = ps[plan_group_start(G) + g];
+    const int s1 = ps[plan_group_start(G) + g + 1];
+    e = ps[plan_group_expert(G) + g];
+    ne = s1 - s0;
+    bool ok = s0 >= 0 && s1 <= G && ne >= 1 && ne <= kMaxNtok && e >= 0 && e < a.n_experts;
+#pragma unroll
+    for (int k = 0; k < kMaxNtok; ++k) {
+        xrow[k] = 0;
+        if (ok && k < ne) {
+            xrow[k] = (a.flags & kExpertsXBySlot) ? s0 + k : ps[2 + 2 * G + s0 + k];
+            ok = ok && xrow[k] >= 0 && xrow[k] < a.n_x;
+        }
+    }
+    return ok;
+}
+
+// The group's CTAs split expert e's bytes of the next stack; the warps of a CTA split
+// its share in pieces (lane 0 issues).  The copies land in L2 while this and the next
+// launch run, so the next projection starts on cached weights.
+__device__ __forceinline__ void prefetch_next(const ExpertArgs& a, int e, int ci, int cn, int warp, int nwarps) {
+    const long long B = a.next_bytes;
+    const long long per = ((B + cn - 1) / cn + 15) / 16 * 16;
+    const long long lo = (long long)ci * per;
+    const long long hi = lo + per < B ? lo + per : B;
+    const unsigned char* base = a.next_w + (long long)e * B;
+    for (long long off = lo + (long long)warp * kPrefetchPiece; off < hi; off += (long long)nwarps * kPrefetchPiece)
+        prefetch_l2(base + off, uint32_t(hi - off < kPrefetchPiece ? hi - off : kPrefetchPiece));
+}
+
 // Threads per CTA: 16 warps up to 2 rows per warp; 12 warps (168 registers a thread)
 // at 4 rows, whose four-token body does not fit in 128 registers beside the group
 // loop's state.
@@ -169,19 +229,45 @@ __global__ void __launch_bounds__(ExpertThreads<RPW>::value, 1) qgemv_experts_ke
     R.ring = ((smem_addr(smem + sp.ring_off) + 127u) & ~127u) + uint32_t(warp * R.depth * kStage);
     R.policy = l2_evict_first_policy();
 
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (lane == 0) {
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&a.wmap)) : "memory");
         for (int s = 0; s < R.depth; ++s) mbar_init(R.bars + s * 8, 1);
     }
     mbar_fence_init();
     __syncwarp();
-    // The plan and x may come from the previous kernel in the stream.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // x (and, unless the caller says it is complete, the plan) may come from the
+    // previous kernel in the stream.  Dependents may begin only once this launch's own
+    // dependencies are complete: a later launch that reads the plan before its wait
+    // (kExpertsPlanReady) then finds it complete.
+    const bool plan_ready = (a.flags & kExpertsPlanReady) != 0;
+    if (!plan_ready) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
 
+    // The plan's group arrays and slot tokens into shared memory with one round of
+    // independent loads (every group's entries then cost no further global latency):
+    // ps[0 .. 2 + 2G) = n_groups, group_start, group_expert; ps[2 + 2G ..) = slot_token.
     const int G = a.n_slots;
-    const int32_t* plan = a.plan;
-    int ng = __ldg(plan);
+    int* ps = reinterpret_cast<int*>(smem + plan_smem_off(sp.total));
+    {
+        const int n_head = 2 + 2 * G, n_all = 2 + 3 * G;
+        for (int i0 = threadIdx.x; i0 < n_all; i0 += 8 * blockDim.x) {
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * int(blockDim.x);
+                if (i < n_all) v[j] = __ldg(a.plan + (i < n_head ? i : i + G));   // skip slot_pair
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + j * int(blockDim.x);
+                if (i < n_all) ps[i] = v[j];
+            }
+        }
+    }
+    __syncthreads();
+    int ng = ps[0];
     if (ng < 0 || ng > G) {
         if (threadIdx.x == 0) atomicOr(a.status, kStatusBadPlan);
         ng = 0;
@@ -203,31 +289,36 @@ __global__ void __launch_bounds__(ExpertThreads<RPW>::value, 1) qgemv_experts_ke
         gstep = C;
     }
 
-    for (; g < ng; g += gstep) {
-        // Every thread reads the same plan words, so `ok` and ne are CTA-uniform.
-        const int s0 = __ldg(plan + plan_group_start(G) + g);
-        const int s1 = __ldg(plan + plan_group_start(G) + g + 1);
-        const int e = __ldg(plan + plan_group_expert(G) + g);
-        const int ne = s1 - s0;
-        bool ok = s0 >= 0 && s1 <= G && ne >= 1 && ne <= kMaxNtok && e >= 0 && e < a.n_experts;
-        int xrow[kMaxNtok];
-#pragma unroll
-        for (int k = 0; k < kMaxNtok; ++k) {
-            xrow[k] = 0;
-            if (ok && k < ne) {
-                xrow[k] = a.x_by_slot ? s0 + k : __ldg(plan + plan_slot_token(G) + s0 + k);
-                ok = ok && xrow[k] >= 0 && xrow[k] < a.n_x;
-            }
+    // The first group's weight copies need only the plan: they go out before the
+    // wait for the previous kernel when the plan is known to be complete.
+    // (e * n_out + n_out <= 2^31 - 1, checked at launch.)
+    const int first = ci + cn * warp;
+    int g_issued = -1;
+    if (g < ng) {
+        int s0, ne, e, xrow[kMaxNtok];
+        if (decode_group(a, ps, G, g, s0, ne, e, xrow)) {
+            R.start_group(first, cn * nwarps, e * a.n_out);
+            for (int s = 0; s < R.depth; ++s) R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
+            if (a.next_w != nullptr && lane == 0) prefetch_next(a, e, ci, cn, warp, nwarps);
+            g_issued = g;
         }
-        if (!ok) {
+    }
+    if (plan_ready) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    }
+
+    for (; g < ng; g += gstep) {
+        int s0, ne, e, xrow[kMaxNtok];
+        if (!decode_group(a, ps, G, g, s0, ne, e, xrow)) {
             if (threadIdx.x == 0) atomicOr(a.status, kStatusBadPlan);
             continue;
         }
-        // The group's first copies need only the expert's rows: they go out before
-        // x is staged.  (e * n_out + n_out <= 2^31 - 1, checked at launch.)
-        const int first = ci + cn * warp;
-        R.start_group(first, cn * nwarps, e * a.n_out);
-        for (int s = 0; s < R.depth; ++s) R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
+        if (g != g_issued) {
+            R.start_group(first, cn * nwarps, e * a.n_out);
+            for (int s = 0; s < R.depth; ++s) R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
+            if (a.next_w != nullptr && lane == 0) prefetch_next(a, e, ci, cn, warp, nwarps);
+        }
         __syncthreads();                         // no warp still reads the previous group's x
         {
             // One staging path for every ne (the layout for kMaxNtok tokens; slots of

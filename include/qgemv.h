@@ -205,9 +205,9 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
  *     y[s][o] = sum_i dequant(W_e)[o][i] * x_row(s)[i],   o < n_out,
  *   where W_e = rows [e * n_out, (e + 1) * n_out) of W, the n_experts matrices
  *   stacked and packed as one (n_experts * n_out)-row matrix in the device layout
- *   (16-byte aligned), and x_row(s) = x[slot_token[s]] (x_by_slot = 0: the gate /
- *   up projections read the step's token rows) or x[s] (x_by_slot = 1: the down
- *   projection reads one activation row per slot).  x: device fp32 [n_x][n_in],
+ *   (16-byte aligned), and x_row(s) = x[slot_token[s]] (the gate / up projections
+ *   read the step's token rows) or, with QG_EXPERTS_X_BY_SLOT in flags, x[s] (the
+ *   down projection reads one activation row per slot).  x: device fp32 [n_x][n_in],
  *   16-byte aligned.  y: device fp32 [n_slots][n_out], 4-byte aligned.  plan: as
  *   written by qg_expert_plan for n_slots = ntok * topk (or by the caller to the
  *   same layout).  The kernel reads n_groups and the groups from device memory;
@@ -215,20 +215,37 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
  *   slots, an expert outside the stack, a row outside x) skips that group and
  *   sets QG_DEVICE_BAD_PLAN.  Each output is bitwise the same for every ne, group
  *   and geometry, and equals qgemv's on the expert's rows whenever that call does
- *   not split (qg_describe_tile shows split=1).  Errors: QG_EINVAL (format, shape,
- *   n_experts * n_out >= 2^31, n_slots outside 1..1024, n_x < 1, x_by_slot not 0
- *   or 1, n_x < n_slots with x_by_slot = 1, null pointer), QG_EALIGN,
+ *   not split (qg_describe_tile shows split=1).
+ *   QG_EXPERTS_PLAN_READY in flags: the caller promises the plan is complete when
+ *   this launch begins; the launch then reads it and starts its weight copies
+ *   before waiting for the previous kernel (under early start, this overlaps the
+ *   previous kernel's tail).  It holds without early start whenever the plan's
+ *   writer precedes on the stream; under early start when the writer is at least
+ *   two launches back and every launch in between is a qgemv_experts call (each
+ *   lets its dependents begin only after its own wait) — e.g. plan, gate/up, down
+ *   with the flag on the down call.  Errors: QG_EINVAL (format, shape,
+ *   n_experts * n_out >= 2^31, n_slots outside 1..1024, n_x < 1, unknown flags,
+ *   n_x < n_slots with QG_EXPERTS_X_BY_SLOT, null pointer), QG_EALIGN,
  *   QG_EUNSUPPORTED, QG_ECUDA.  The geometry follows qg_set_tile_override's rpw,
- *   depth, warps and ctas (rpw 1, 2 or 4; the split does not apply). */
+ *   depth, warps and ctas (rpw 1, 2 or 4; the split does not apply).
+ *   W_next (optional, NULL = none): the stack of the projection that comes next
+ *   (same fmt and n_experts; next_n_out rows of next_n_in per expert, device
+ *   layout, 16-byte aligned), e.g. the down projection while gate/up runs.  The
+ *   launch prefetches each active expert's rows of it into L2 (a hint: no result
+ *   changes, nothing is written), so the next launch starts on cached weights.
+ *   Errors for it: QG_EINVAL (shape), QG_EALIGN. */
 #define QG_DEVICE_BAD_PLAN 4u
+#define QG_EXPERTS_X_BY_SLOT 1u
+#define QG_EXPERTS_PLAN_READY 2u
 /* qg_describe_expert_tile: the geometry qgemv_experts would use for one expert's
  * shape, written as qg_describe_tile does. */
 size_t    qg_expert_plan_ints(int64_t n_pairs);
 qg_status qg_expert_plan(const int32_t* ids, int ntok, int topk, int n_experts, int32_t* plan,
                          void* stream);
 qg_status qgemv_experts(qg_fmt fmt, const void* W, int64_t n_experts, int64_t n_out, int64_t n_in,
-                        const float* x, int64_t n_x, int x_by_slot, const int32_t* plan,
-                        int64_t n_slots, float* y, void* stream);
+                        const float* x, int64_t n_x, unsigned int flags, const int32_t* plan,
+                        int64_t n_slots, float* y, const void* W_next, int64_t next_n_out,
+                        int64_t next_n_in, void* stream);
 qg_status qg_describe_expert_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, char* buf, size_t len);
 
 /* ------------------------------------------------------- qgemv_argmax_noalloc

@@ -104,9 +104,9 @@ def test_expert_calls_reject_before_launch():
     assert lib.qg_expert_plan(A + 2, 4, 10, 512, A, None) == -2
     assert lib.qg_expert_plan(A, 4, 10, 512, A + 2, None) == -2
     # qgemv_experts(fmt, W, n_experts, n_out, n_in, x, n_x, x_by_slot, plan, n_slots, y, stream)
-    ok = (0, A, 8, 64, 256, A, 4, 0, A, 40, A)
+    ok = (0, A, 8, 64, 256, A, 4, 0, A, 40, A, None, 0, 0)
     def call(**kw):
-        names = ["fmt", "W", "ne", "no", "ni", "x", "nx", "bs", "plan", "ns", "y"]
+        names = ["fmt", "W", "ne", "no", "ni", "x", "nx", "bs", "plan", "ns", "y", "wn", "nno", "nni"]
         args = dict(zip(names, ok))
         args.update(kw)
         return lib.qgemv_experts(*[args[n] for n in names], None)
@@ -115,10 +115,12 @@ def test_expert_calls_reject_before_launch():
     assert call(ne=1 << 20, no=1 << 12) == -1                            # stack of 2^32 rows
     assert call(ni=48) == -1                                             # n_in not a multiple of 32
     assert call(ns=0) == -1 and call(ns=1025) == -1
-    assert call(nx=0) == -1 and call(bs=2) == -1
+    assert call(nx=0) == -1 and call(bs=4) == -1                        # unknown flag
     assert call(bs=1, nx=39) == -1                                      # one x row per slot needed
     assert call(W=None) == -1 and call(x=None) == -1 and call(plan=None) == -1 and call(y=None) == -1
     assert call(W=A + 8) == -2 and call(x=A + 4) == -2 and call(plan=A + 2) == -2 and call(y=A + 2) == -2
+    assert call(wn=A, nno=0, nni=256) == -1 and call(wn=A, nno=64, nni=48) == -1     # bad next stack
+    assert call(wn=A + 8, nno=64, nni=256) == -2
 
 
 def test_tile_override_grammar():

@@ -75,10 +75,12 @@ def oracle_plan_array(ids, n_experts):
     return a, p
 
 
-def run_experts(fmt, packed, n_experts, n_out, n_in, x, plan, n_slots, by_slot=False):
+def run_experts(fmt, packed, n_experts, n_out, n_in, x, plan, n_slots, by_slot=False, nxt=None):
     xd = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(dev())
     y = torch.full((n_slots, n_out), float("nan"), dtype=torch.float32, device=dev())
-    qg.qgemv_experts(fmt, packed, n_experts, n_out, n_in, xd, plan, n_slots, y, x_by_slot=by_slot)
+    W_next, nno, nni = nxt if nxt is not None else (None, 0, 0)
+    qg.qgemv_experts(fmt, packed, n_experts, n_out, n_in, xd, plan, n_slots, y, x_by_slot=by_slot,
+                     W_next=W_next, next_n_out=nno, next_n_in=nni)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
@@ -260,6 +262,54 @@ def test_wait_timeout_reports_and_recovers():
     check_close(y, ref, den, "after a timeout")
 
 
+def test_plan_ready_chain_under_early_start():
+    """plan -> gate/up -> down (QG_EXPERTS_PLAN_READY) for several routings back to back
+    under early start, no host sync in between: every down output equals the one from
+    the plain path (plan read after the wait), bit for bit."""
+    fmt, n_experts, d_model, d_ff, topk = "q8_0", 16, 512, 128, 4
+    _, canon_gu, gu = _small_case(fmt, n_experts, 2 * d_ff, d_model, 501)
+    _, canon_dn, dn = _small_case(fmt, n_experts, d_model, d_ff, 502)
+    runs = []
+    for r in range(6):
+        ntok = 1 + r % 4
+        ids = workloads.routing(600 + r, ntok, topk, n_experts, 0.65)
+        G = ntok * topk
+        runs.append((torch.from_numpy(ids).to(dev()), G,
+                     torch.from_numpy(workloads.gaussian(700 + r, (ntok, d_model))).to(dev()),
+                     torch.from_numpy(workloads.gaussian(800 + r, (G, d_ff))).to(dev())))
+
+    def chain(ready):
+        outs = []
+        for ids, G, x, h in runs:
+            plan = torch.full((qg.qg_expert_plan_ints(G),), -5, dtype=torch.int32, device=dev())
+            y_gu = torch.empty((G, 2 * d_ff), dtype=torch.float32, device=dev())
+            y_dn = torch.empty((G, d_model), dtype=torch.float32, device=dev())
+            qg.qg_expert_plan(ids, n_experts, plan)
+            qg.qgemv_experts(fmt, gu, n_experts, 2 * d_ff, d_model, x, plan, G, y_gu, W_next=dn,
+                             next_n_out=d_model, next_n_in=d_ff)
+            qg.qgemv_experts(fmt, dn, n_experts, d_model, d_ff, h, plan, G, y_dn, x_by_slot=True, plan_ready=ready)
+            outs.append((y_gu, y_dn, plan))      # every buffer stays alive until the sync
+        torch.cuda.synchronize()
+        return [(a.cpu().numpy(), b.cpu().numpy()) for a, b, _ in outs]
+
+    qg.qg_set_launch_options(qg.QG_LAUNCH_EARLY_START)
+    try:
+        plain = chain(False)
+        for _ in range(3):
+            ready = chain(True)
+            for (a0, b0), (a1, b1) in zip(plain, ready):
+                assert np.array_equal(a0.view(np.uint32), a1.view(np.uint32))
+                assert np.array_equal(b0.view(np.uint32), b1.view(np.uint32))
+    finally:
+        qg.qg_set_launch_options(0)
+    assert qg.qg_device_status() == 0
+    # and the plain path against the oracle
+    ids, G, x, h = runs[3]
+    _, p = oracle_plan_array(ids.cpu().numpy(), n_experts)
+    ref, den = slot_reference(fmt, canon_dn, n_experts, d_model, d_ff, h.cpu().numpy(), p, True)
+    check_close(plain[3][1], ref, den, "plan-ready chain, down")
+
+
 # ----------------------------------------------------------------------------- the full layer size, sampled
 
 def _packed_stack(layer, n_out, n_in, seed, experts, threads=16):
@@ -295,6 +345,9 @@ def test_full_size_layer_sampled():
         x = workloads.activations(layer.seed + ntok, dm, ntok)
         h = workloads.gaussian(layer.seed + 10 + ntok, (G, ff))
         y_gu = run_experts(layer.fmt, gu, n_experts, ff2, dm, x, plan_d, G)
+        # with the down stack prefetched into L2: the same bits
+        y_pf = run_experts(layer.fmt, gu, n_experts, ff2, dm, x, plan_d, G, nxt=(dn, dm, ff))
+        assert np.array_equal(y_pf.view(np.uint32), y_gu.view(np.uint32))
         y_dn = run_experts(layer.fmt, dn, n_experts, dm, ff, h, plan_d, G, by_slot=True)
         for g, e in enumerate(p["group_expert"]):
             e = int(e)
