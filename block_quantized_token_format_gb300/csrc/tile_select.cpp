@@ -108,14 +108,17 @@ Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
     return t;
 }
 
+// Measured on GB300 for the routed-expert layer (gate/up 1280x2560, down 2560x640,
+// Q8_0, 10-21 active experts): 4 rows per warp, 12 warps, a 2-stage ring beat 2 rows
+// x 16 warps by 8-12% and deeper rings (3-7 stages) by 1-10%.
 Tile select_expert_tile(int fmt, int64_t n_out, int64_t n_in) {
     (void)fmt;
     (void)n_out;
     (void)n_in;
     Tile t;
-    t.rpw = 2;
-    t.depth = 3;
-    t.warps = 16;
+    t.rpw = 4;
+    t.depth = 2;
+    t.warps = 12;
     t.ctas = 1;
     return t;
 }
