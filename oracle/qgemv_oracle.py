@@ -419,6 +419,21 @@ def experts_gemv_slots(fmt, packed, n_experts: int, n_out: int, n_in: int, x, pl
     return y
 
 
+def silu(v):
+    """v * sigmoid(v) = v / (1 + exp(-v)), fp64."""
+    v = np.asarray(v, dtype=np.float64)
+    return v / (1.0 + np.exp(-v))
+
+
+def swiglu_rows(y):
+    """The gated activation of an interleaved gate / up projection: for rows
+    ``y[..., 2j]`` (gate j) and ``y[..., 2j + 1]`` (up j), ``silu(gate) * up`` ([Track2]
+    section 1 item 2: ``moe_gu`` computes a group's gate and up projections together;
+    reading: the activation is SiLU-gated, the form of a gate / up pair)."""
+    y = np.asarray(y, dtype=np.float64)
+    return silu(y[..., 0::2]) * y[..., 1::2]
+
+
 def experts_gemv(fmt, packed, n_experts: int, n_out: int, n_in: int, x, group_expert, group_tokens):
     """Expert-grouped multi-token mat-vec.
 

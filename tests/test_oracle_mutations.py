@@ -49,6 +49,8 @@ MUTATIONS = {
                                    '"slot_token": np.array(slot_pair, dtype=np.int64) // max(topk - 1, 1),'),
     "slots read token rows in down mode": ("rows = slots if x_by_slot else",
                                            "rows = slots if not x_by_slot else"),
+    "swiglu gate and up swapped": ("return silu(y[..., 0::2]) * y[..., 1::2]", "return silu(y[..., 1::2]) * y[..., 0::2]"),
+    "silu without the sigmoid": ("return v / (1.0 + np.exp(-v))", "return v / (1.0 + np.exp(v))"),
     "draft gather ignores affine scales": ("s = packed[nw * 4: nw * 4 + ng * 2].reshape(n_out, n_in // 32)[ids]",
                                            "s = packed[nw * 4: nw * 4 + ng * 2].reshape(n_out, n_in // 32)[:ids.size]"),
 }

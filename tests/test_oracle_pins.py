@@ -464,11 +464,28 @@ def check_expert_plan(orc):
         assert np.allclose(y[s], full[s, e * n_out:(e + 1) * n_out], rtol=1e-13, atol=1e-15)
 
 
+def check_swiglu(orc):
+    """SiLU and the interleaved gate / up activation, by closed forms: silu(0) = 0,
+    silu(v) - silu(-v) = v (sigmoid(v) + sigmoid(-v) = 1), silu(ln 3) = 0.75 ln 3
+    (sigmoid(ln 3) = 3/4), silu(v) -> v for large v and -> 0 for very negative v; the
+    activation pairs row 2j (gate) with row 2j + 1 (up)."""
+    assert orc.silu(0.0) == 0.0
+    v = np.linspace(-9, 9, 37)
+    assert np.allclose(orc.silu(v) - orc.silu(-v), v, rtol=0, atol=1e-14)
+    assert abs(float(orc.silu(np.log(3.0))) - 0.75 * np.log(3.0)) < 1e-15
+    assert abs(float(orc.silu(40.0)) - 40.0) < 1e-12 and abs(float(orc.silu(-40.0))) < 1e-15
+    y = np.array([[np.log(3.0), 2.0, 0.0, 5.0, -np.log(3.0), 4.0]])
+    a = orc.swiglu_rows(y)
+    want = [0.75 * np.log(3.0) * 2.0, 0.0, -0.25 * np.log(3.0) * 4.0]
+    assert a.shape == (1, 3) and np.allclose(a[0], want, rtol=1e-15, atol=1e-15)
+
+
 ALL_CHECKS = [check_page_byte_counts, check_golden_q8_0, check_golden_q4_0, check_golden_affine4,
               check_golden_bf16, check_rounding, check_brute_force, check_idempotence,
               check_affine_constructed_roundtrip, check_linearity, check_token_independence,
               check_cross_format, check_argmax, check_quant_error_band, check_fp16_bf16_rounding,
-              check_draft_ids, check_experts, check_expert_plan]
+              check_draft_ids, check_experts, check_expert_plan,
+              check_swiglu]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
