@@ -499,10 +499,11 @@ def detail_table(args, qg, torch, dev, l2, peak):
 
 
 def experts_detail(qg, torch, dev, peak, layer, unique=32, routings=64):
-    """Routed experts, one layer: the plan, the gate/up projection (token rows; it also
-    prefetches the same experts' down rows into L2) and the down projection (one
-    activation row per slot) per ntok, each step with its own seeded routing (64
-    routings in turn), timed as 64-step graphs.  Bytes = the active experts' weight
+    """Routed experts, one layer: the plan, the gate/up projection (token rows, gate /
+    up row pairs written as silu(gate) * up; it also prefetches the same experts' down
+    rows into L2) and the down projection of that activation (one row per slot) per
+    ntok, each step with its own seeded routing (64 routings in turn), timed as
+    64-step graphs.  Bytes = the active experts' weight
     bytes (each read from HBM once per layer).  The stack holds n_experts experts at
     their own addresses; their contents repeat every `unique` experts (the data does
     not change the timing; the addresses do).  "gate_up" and "down" are timed alone
@@ -535,19 +536,18 @@ def experts_detail(qg, torch, dev, peak, layer, unique=32, routings=64):
         ids = [torch.from_numpy(i).to(dev) for i in ids_np]
         plans = [torch.empty(qg.qg_expert_plan_ints(G), dtype=torch.int32, device=dev) for _ in range(routings)]
         x = torch.from_numpy(workloads.activations(layer.seed, dm, ntok)).to(dev)
-        h = torch.from_numpy(workloads.gaussian(layer.seed + 3, (G, ff))).to(dev)
-        y_gu = torch.empty((G, 2 * ff), dtype=torch.float32, device=dev)
+        act = torch.zeros((G, ff), dtype=torch.float32, device=dev)
         y_dn = torch.empty((G, dm), dtype=torch.float32, device=dev)
 
         def plan(r):
             qg.qg_expert_plan(ids[r], E, plans[r])
 
-        def gu(r):   # also prefetches the same experts' down rows into L2
-            qg.qgemv_experts(layer.fmt, stacks["gu"], E, 2 * ff, dm, x, plans[r], G, y_gu,
+        def gu(r):   # gate/up pairs -> silu(gate) * up; also prefetches the down rows into L2
+            qg.qgemv_experts(layer.fmt, stacks["gu"], E, 2 * ff, dm, x, plans[r], G, act, swiglu=True,
                              W_next=stacks["dn"], next_n_out=dm, next_n_in=ff)
 
-        def dn(r):   # the plan was written two launches back: its copies start before the wait
-            qg.qgemv_experts(layer.fmt, stacks["dn"], E, dm, ff, h, plans[r], G, y_dn, x_by_slot=True,
+        def dn(r):   # reads the activation; the plan was written two launches back
+            qg.qgemv_experts(layer.fmt, stacks["dn"], E, dm, ff, act, plans[r], G, y_dn, x_by_slot=True,
                              plan_ready=True)
 
         def layer_step(r):

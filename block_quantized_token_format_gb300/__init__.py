@@ -24,6 +24,7 @@ __all__ = [
     "QG_LAUNCH_EARLY_START", "current_stream_handle", "qg_gather_rows", "qgemv_argmax_ids",
     "QG_DEVICE_BAD_ROW_ID", "qg_expert_plan_ints", "qg_expert_plan", "qgemv_experts", "qg_describe_expert_tile",
     "QG_DEVICE_BAD_PLAN", "QG_EXPERTS_X_BY_SLOT", "QG_EXPERTS_PLAN_READY",
+    "QG_EXPERTS_SWIGLU",
 ]
 
 QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
@@ -256,6 +257,7 @@ QG_DEVICE_BAD_ROW_ID = 2
 QG_DEVICE_BAD_PLAN = 4
 QG_EXPERTS_X_BY_SLOT = 1
 QG_EXPERTS_PLAN_READY = 2
+QG_EXPERTS_SWIGLU = 4
 
 
 def qg_expert_plan_ints(n_pairs: int) -> int:
@@ -273,12 +275,14 @@ def qg_expert_plan(ids, n_experts: int, plan, stream=None) -> None:
 
 def qgemv_experts(fmt, W, n_experts: int, n_out: int, n_in: int, x, plan, n_slots: int, y,
                   x_by_slot: bool = False, W_next=None, next_n_out: int = 0, next_n_in: int = 0,
-                  plan_ready: bool = False, stream=None) -> None:
+                  plan_ready: bool = False, swiglu: bool = False, stream=None) -> None:
     """Enqueue the expert-grouped mat-vec: ``y[s] = W_e . x_row(s)`` for every slot s of the
     plan (``x_row(s) = x[slot_token[s]]``, or ``x[s]`` with ``x_by_slot``); optionally prefetch
     the active experts of the next projection's stack ``W_next`` into L2.  ``plan_ready``:
-    the plan is complete when the launch begins (see QG_EXPERTS_PLAN_READY)."""
-    flags = (QG_EXPERTS_X_BY_SLOT if x_by_slot else 0) | (QG_EXPERTS_PLAN_READY if plan_ready else 0)
+    the plan is complete when the launch begins (see QG_EXPERTS_PLAN_READY).  ``swiglu``: the
+    rows pair up as (gate, up) and y receives silu(gate) * up, ``[n_slots, n_out / 2]``."""
+    flags = ((QG_EXPERTS_X_BY_SLOT if x_by_slot else 0) | (QG_EXPERTS_PLAN_READY if plan_ready else 0)
+             | (QG_EXPERTS_SWIGLU if swiglu else 0))
     _check(load_library().qgemv_experts(_fmt(fmt), _ptr(W), int(n_experts), int(n_out), int(n_in), _ptr(x),
                                         int(x.shape[0]), flags, _ptr(plan), int(n_slots), _ptr(y),
                                         _ptr(W_next), int(next_n_out), int(next_n_in), _stream(stream)),

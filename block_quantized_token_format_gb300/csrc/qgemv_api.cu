@@ -739,7 +739,8 @@ qg_status qgemv_experts(qg_fmt fmt, const void* W, int64_t n_experts, int64_t n_
     if (n_experts < 1 || n_out < 1 || n_experts > ((int64_t(1) << 31) - 1) / n_out) return QG_EINVAL;
     if (!shape_valid(fmt, n_experts * n_out, n_in)) return QG_EINVAL;
     if (n_slots < 1 || n_slots > kMaxPlanPairs || n_x < 1 || n_x > (int64_t(1) << 31) - 1) return QG_EINVAL;
-    if (flags & ~(QG_EXPERTS_X_BY_SLOT | QG_EXPERTS_PLAN_READY)) return QG_EINVAL;
+    if (flags & ~(QG_EXPERTS_X_BY_SLOT | QG_EXPERTS_PLAN_READY | QG_EXPERTS_SWIGLU)) return QG_EINVAL;
+    if ((flags & QG_EXPERTS_SWIGLU) && (n_out % 2) != 0) return QG_EINVAL;
     if ((flags & QG_EXPERTS_X_BY_SLOT) && n_x < n_slots) return QG_EINVAL;
     if (!W || !x || !plan || !y) return QG_EINVAL;
     if (W_next) {
@@ -751,6 +752,7 @@ qg_status qgemv_experts(qg_fmt fmt, const void* W, int64_t n_experts, int64_t n_
     Plan p;
     qg_status st = plan_experts_cached(fmt, n_out, n_in, &p);
     if (st != QG_OK) return st;
+    if ((flags & QG_EXPERTS_SWIGLU) && (p.tile.rpw % 2) != 0) return QG_EUNSUPPORTED;   // gate/up pairs per block
     ExpertArgs a{};
     st = encode_weight_map(&a.wmap, fmt, W, n_experts * n_out, n_in, p.tile.rpw);
     if (st != QG_OK) return st;

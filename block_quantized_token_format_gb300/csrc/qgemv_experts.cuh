@@ -38,6 +38,7 @@ namespace qg {
 constexpr unsigned kStatusBadPlan = 4u;   // a plan entry or a routed expert id out of range
 constexpr unsigned kExpertsXBySlot = QG_EXPERTS_X_BY_SLOT;
 constexpr unsigned kExpertsPlanReady = QG_EXPERTS_PLAN_READY;
+constexpr unsigned kExpertsSwiglu = QG_EXPERTS_SWIGLU;
 constexpr int kMaxPlanPairs = 1024;      // (token, choice) pairs one plan can hold
 
 // Offsets (in int32 entries) of the plan's arrays for n_slots = ntok * topk slots.
@@ -157,7 +158,22 @@ __device__ __forceinline__ void expert_group(const ExpertArgs& a, Ring& R, unsig
         if (R.failed) break;
         const float v0 = warp_reduce<FMT, NE, RPW>(acc, lane);
         const int vi = lane / SPAN;
-        if (vi < V && (lane % SPAN) == 0) {
+        bool stored = false;
+        if constexpr (RPW % 2 == 0) {
+            if (a.flags & kExpertsSwiglu) {
+                // Rows 2j (gate) and 2j + 1 (up) of a block sit NE values apart: the
+                // gate's lane takes the up value and writes silu(gate) * up.
+                const float up = __shfl_down_sync(kFull, v0, NE * SPAN);
+                if (vi < V && (lane % SPAN) == 0) {
+                    const int r = vi / NE, t = vi - r * NE;
+                    const int row = gc * RPW + r;
+                    if ((r & 1) == 0 && row < n_out)
+                        a.y[(long long)(s0 + t) * (n_out >> 1) + (row >> 1)] = v0 / (1.0f + expf(-v0)) * up;
+                }
+                stored = true;
+            }
+        }
+        if (!stored && vi < V && (lane % SPAN) == 0) {
             const int r = vi / NE, t = vi - r * NE;
             const int row = gc * RPW + r;
             if (row < n_out) a.y[(long long)(s0 + t) * n_out + row] = v0;

@@ -216,6 +216,11 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
  *   sets QG_DEVICE_BAD_PLAN.  Each output is bitwise the same for every ne, group
  *   and geometry, and equals qgemv's on the expert's rows whenever that call does
  *   not split (qg_describe_tile shows split=1).
+ *   QG_EXPERTS_SWIGLU in flags (a gate / up projection whose expert rows come in
+ *   pairs, row 2j = gate j, row 2j + 1 = up j; n_out even): instead of the n_out
+ *   projections, y[s][j] = silu(gate_j) * up_j with silu(v) = v / (1 + exp(-v)),
+ *   fp32, y [n_slots][n_out / 2] — the down projection's input, with no separate
+ *   activation launch.  QG_EUNSUPPORTED if a tile override forces an odd rpw.
  *   QG_EXPERTS_PLAN_READY in flags: the caller promises the plan is complete when
  *   this launch begins; the launch then reads it and starts its weight copies
  *   before waiting for the previous kernel (under early start, this overlaps the
@@ -225,6 +230,7 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
  *   lets its dependents begin only after its own wait) — e.g. plan, gate/up, down
  *   with the flag on the down call.  Errors: QG_EINVAL (format, shape,
  *   n_experts * n_out >= 2^31, n_slots outside 1..1024, n_x < 1, unknown flags,
+ *   odd n_out with QG_EXPERTS_SWIGLU,
  *   n_x < n_slots with QG_EXPERTS_X_BY_SLOT, null pointer), QG_EALIGN,
  *   QG_EUNSUPPORTED, QG_ECUDA.  The geometry follows qg_set_tile_override's rpw,
  *   depth, warps and ctas (rpw 1, 2 or 4; the split does not apply).
@@ -237,6 +243,7 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
 #define QG_DEVICE_BAD_PLAN 4u
 #define QG_EXPERTS_X_BY_SLOT 1u
 #define QG_EXPERTS_PLAN_READY 2u
+#define QG_EXPERTS_SWIGLU 4u
 /* qg_describe_expert_tile: the geometry qgemv_experts would use for one expert's
  * shape, written as qg_describe_tile does. */
 size_t    qg_expert_plan_ints(int64_t n_pairs);

@@ -115,7 +115,8 @@ def test_expert_calls_reject_before_launch():
     assert call(ne=1 << 20, no=1 << 12) == -1                            # stack of 2^32 rows
     assert call(ni=48) == -1                                             # n_in not a multiple of 32
     assert call(ns=0) == -1 and call(ns=1025) == -1
-    assert call(nx=0) == -1 and call(bs=4) == -1                        # unknown flag
+    assert call(nx=0) == -1 and call(bs=8) == -1                        # unknown flag
+    assert call(bs=4, no=63) == -1                                       # gate/up pairs need even n_out
     assert call(bs=1, nx=39) == -1                                      # one x row per slot needed
     assert call(W=None) == -1 and call(x=None) == -1 and call(plan=None) == -1 and call(y=None) == -1
     assert call(W=A + 8) == -2 and call(x=A + 4) == -2 and call(plan=A + 2) == -2 and call(y=A + 2) == -2

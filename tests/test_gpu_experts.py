@@ -203,6 +203,46 @@ def test_outputs_bitwise_independent_of_ne_group_and_tile(fmt):
             assert np.array_equal(y[slot[2 * t]].view(np.uint32), yq[t].view(np.uint32)), t
 
 
+def check_swiglu(act, ref_y, den_y, what):
+    """act = silu(gate) * up from the GPU against the oracle's gate / up rows (interleaved):
+    the error allowed is the mat-vec tolerance carried through the activation,
+    |d act| <= 1e-3 (|silu'(g) u| D_g + |silu(g)| D_u) + 1e-5 |act|."""
+    g, u = ref_y[..., 0::2], ref_y[..., 1::2]
+    Dg, Du = den_y[..., 0::2], den_y[..., 1::2]
+    ref = ORC.swiglu_rows(ref_y)
+    sig = 1.0 / (1.0 + np.exp(-g))
+    dsilu = sig * (1.0 + g * (1.0 - sig))
+    bound = TOL * (np.abs(dsilu * u) * Dg + np.abs(ORC.silu(g)) * Du) + 1e-5 * np.abs(ref) + 1e-30
+    act = act.astype(np.float64)
+    assert np.all(np.isfinite(act)), what
+    bad = np.abs(act - ref) > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} outputs outside the bound"
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n_experts,d_ff,n_in_base", [(6, 37, 640), (5, 320, 2560)])
+def test_swiglu_gate_up(fmt, n_experts, d_ff, n_in_base):
+    """Gate / up rows interleaved per expert; y = silu(gate) * up."""
+    n_out = 2 * d_ff
+    n_in, canon, packed = _small_case(fmt, n_experts, n_out, n_in_base, 900 + d_ff)
+    for ntok in (1, 2, 3, 4):
+        ids = workloads.routing(ntok * 5 + d_ff, ntok, 3, n_experts, 0.65)
+        G = ntok * 3
+        x = workloads.gaussian(ntok + n_in + 1, (ntok, n_in), 2.0)      # gate values around +-1
+        plan_d = gpu_plan(ids, n_experts)
+        _, p = oracle_plan_array(ids, n_experts)
+        xd = torch.from_numpy(x).to(dev())
+        act = torch.full((G, d_ff), float("nan"), dtype=torch.float32, device=dev())
+        qg.qgemv_experts(fmt, packed, n_experts, n_out, n_in, xd, plan_d, G, act, swiglu=True)
+        torch.cuda.synchronize()
+        ref, den = slot_reference(fmt, canon, n_experts, n_out, n_in, x, p, False)
+        check_swiglu(act.cpu().numpy(), ref, den, f"{fmt} swiglu ntok={ntok}")
+        # the same rows without the flag: the plain projection, whose pairs give the same act
+        y = run_experts(fmt, packed, n_experts, n_out, n_in, x, plan_d, G)
+        check_close(y, ref, den, f"{fmt} gate/up ntok={ntok}")
+    assert qg.qg_device_status() == 0
+
+
 def test_more_groups_than_ctas():
     """About 300 one- and two-slot groups on a one-CTA-per-SM grid: CTAs take whole
     groups one after the other, restaging x between them."""
@@ -348,16 +388,25 @@ def test_full_size_layer_sampled():
         # with the down stack prefetched into L2: the same bits
         y_pf = run_experts(layer.fmt, gu, n_experts, ff2, dm, x, plan_d, G, nxt=(dn, dm, ff))
         assert np.array_equal(y_pf.view(np.uint32), y_gu.view(np.uint32))
+        # the gated activation of the same launch (rows read as gate / up pairs)
+        act_d = torch.empty((G, ff), dtype=torch.float32, device=dev())
+        qg.qgemv_experts(layer.fmt, gu, n_experts, ff2, dm, torch.from_numpy(x).to(dev()), plan_d, G, act_d,
+                         swiglu=True)
+        torch.cuda.synchronize()
+        act = act_d.cpu().numpy()
         y_dn = run_experts(layer.fmt, dn, n_experts, dm, ff, h, plan_d, G, by_slot=True)
         for g, e in enumerate(p["group_expert"]):
             e = int(e)
             for (yy, n_out, n_in, seed, xin, by_slot) in ((y_gu, ff2, dm, layer.seed, x, False),
                                                          (y_dn, dm, ff, layer.seed + 1, h, True)):
-                rows = np.sort(rng.choice(n_out, size=8, replace=False))
+                pairs = np.sort(rng.choice(n_out // 2, size=4, replace=False))
+                rows = np.stack([2 * pairs, 2 * pairs + 1], axis=1).reshape(-1)     # (gate, up) pairs
                 canon = ORC.quantize(layer.fmt, workloads.expert_matrix(seed, e, n_out, n_in)[rows])
                 for s in range(int(p["group_start"][g]), int(p["group_start"][g + 1])):
                     r = s if by_slot else int(p["slot_token"][s])
                     ref = ORC.gemv(layer.fmt, canon, len(rows), n_in, xin[r:r + 1])[0]
                     den = ORC.gemv_abs(layer.fmt, canon, len(rows), n_in, xin[r:r + 1])[0]
                     check_close(yy[s, rows][None], ref[None], den[None], f"ntok={ntok} group {g} slot {s}")
+                    if not by_slot:
+                        check_swiglu(act[s, pairs][None], ref[None], den[None], f"ntok={ntok} group {g} act")
     assert qg.qg_device_status() == 0
