@@ -503,7 +503,7 @@ def experts_detail(qg, torch, dev, peak, layer, unique=32, routings=64):
     up row pairs written as silu(gate) * up; it also prefetches the same experts' down
     rows into L2) and the down projection of that activation (one row per slot) per
     ntok, each step with its own seeded routing (64 routings in turn), timed as
-    64-step graphs.  Bytes = the active experts' weight
+    64-step graphs; "layer_one_launch" is the same layer as one persistent launch.  Bytes = the active experts' weight
     bytes (each read from HBM once per layer).  The stack holds n_experts experts at
     their own addresses; their contents repeat every `unique` experts (the data does
     not change the timing; the addresses do).  "gate_up" and "down" are timed alone
@@ -555,12 +555,19 @@ def experts_detail(qg, torch, dev, peak, layer, unique=32, routings=64):
             gu(r)
             dn(r)
 
+        wsl = torch.zeros(qg.qgemv_expert_layer_workspace_bytes(), dtype=torch.uint8, device=dev)
+
+        def layer_one(r):   # the same layer as one persistent launch
+            qg.qgemv_expert_layer(layer.fmt, stacks["gu"], stacks["dn"], E, dm, ff, x, ids[r], plans[r], act, y_dn,
+                                  wsl)
+
         for r in range(routings):
             plan(r)
         torch.cuda.synchronize()
         row = {"pairs": G, "unique_experts": round(unique_e, 2),
                "grouping_saves": round(1.0 - unique_e / G, 3)}
-        for key, fn in (("plan", plan), ("gate_up", gu), ("down", dn), ("layer", layer_step)):
+        for key, fn in (("plan", plan), ("gate_up", gu), ("down", dn), ("layer", layer_step),
+                        ("layer_one_launch", layer_one)):
             for r in range(3):
                 fn(r)
             torch.cuda.synchronize()
@@ -579,7 +586,8 @@ def experts_detail(qg, torch, dev, peak, layer, unique=32, routings=64):
                 ts.append(a.elapsed_time(b) / routings * 1e3)
             us = statistics.median(ts)
             nbytes = unique_e * {"plan": 0, "gate_up": bytes_e["gu"], "down": bytes_e["dn"],
-                                 "layer": bytes_e["gu"] + bytes_e["dn"]}[key]
+                                 "layer": bytes_e["gu"] + bytes_e["dn"],
+                                 "layer_one_launch": bytes_e["gu"] + bytes_e["dn"]}[key]
             row[key] = {"us": round(us, 3)}
             if nbytes:
                 gbs = nbytes / (us * 1e-6) / 1e9

@@ -24,7 +24,7 @@ __all__ = [
     "QG_LAUNCH_EARLY_START", "current_stream_handle", "qg_gather_rows", "qgemv_argmax_ids",
     "QG_DEVICE_BAD_ROW_ID", "qg_expert_plan_ints", "qg_expert_plan", "qgemv_experts", "qg_describe_expert_tile",
     "QG_DEVICE_BAD_PLAN", "QG_EXPERTS_X_BY_SLOT", "QG_EXPERTS_PLAN_READY",
-    "QG_EXPERTS_SWIGLU",
+    "QG_EXPERTS_SWIGLU", "qgemv_expert_layer", "qgemv_expert_layer_workspace_bytes",
 ]
 
 QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
@@ -84,6 +84,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "qg_expert_plan": (i32, [vp, i32, i32, i32, vp, vp]),
         "qgemv_experts": (i32, [i32, vp, i64, i64, i64, vp, i64, ctypes.c_uint, vp, i64, vp, vp, i64, i64, vp]),
         "qg_describe_expert_tile": (i32, [i32, i64, i64, ctypes.c_char_p, sz]),
+        "qgemv_expert_layer_workspace_bytes": (sz, []),
+        "qgemv_expert_layer": (i32, [i32, vp, vp, i64, i64, i64, vp, i32, vp, i32, vp, vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -287,6 +289,22 @@ def qgemv_experts(fmt, W, n_experts: int, n_out: int, n_in: int, x, plan, n_slot
                                         int(x.shape[0]), flags, _ptr(plan), int(n_slots), _ptr(y),
                                         _ptr(W_next), int(next_n_out), int(next_n_in), _stream(stream)),
            "qgemv_experts")
+
+
+def qgemv_expert_layer_workspace_bytes() -> int:
+    return int(load_library().qgemv_expert_layer_workspace_bytes())
+
+
+def qgemv_expert_layer(fmt, W_gate_up, W_down, n_experts: int, d_model: int, d_ff: int, x, ids, plan, act, y,
+                       workspace, stream=None) -> None:
+    """Enqueue the whole routed-expert layer as one launch: plan (written to ``plan``),
+    ``act = silu(gate) * up`` for every slot, then ``y = W_down . act``.  ``ids``: device
+    int32 ``[ntok, topk]``; ``workspace``: zeroed once, ``qgemv_expert_layer_workspace_bytes()``."""
+    ntok, topk = int(ids.shape[0]), int(ids.shape[1])
+    _check(load_library().qgemv_expert_layer(_fmt(fmt), _ptr(W_gate_up), _ptr(W_down), int(n_experts), int(d_model),
+                                             int(d_ff), _ptr(x), ntok, _ptr(ids), topk, _ptr(plan), _ptr(act), _ptr(y),
+                                             _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                             _stream(stream)), "qgemv_expert_layer")
 
 
 def qg_describe_expert_tile(fmt, n_out: int, n_in: int) -> str:

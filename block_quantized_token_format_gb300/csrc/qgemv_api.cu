@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -775,6 +776,104 @@ qg_status qgemv_experts(qg_fmt fmt, const void* W, int64_t n_experts, int64_t n_
     a.next_w = static_cast<const unsigned char*>(W_next);
     a.next_bytes = W_next ? (long long)(next_n_out * row_stride(fmt, next_n_in)) : 0;
     return launch_experts(p, a, stream);
+}
+
+size_t qgemv_expert_layer_workspace_bytes(void) { return size_t(1 + kMaxPlanPairs) * 4 + 12; }   // 4112
+
+qg_status qgemv_expert_layer(qg_fmt fmt, const void* W_gate_up, const void* W_down, int64_t n_experts, int64_t d_model,
+                             int64_t d_ff, const float* x, int ntok, const int32_t* ids, int topk, int32_t* plan,
+                             float* act, float* y, void* workspace, size_t workspace_bytes, void* stream) {
+    const int64_t kMaxRows = (int64_t(1) << 31) - 1;
+    if (n_experts < 1 || d_model < 1 || d_ff < 1) return QG_EINVAL;
+    if (n_experts > kMaxRows / (2 * d_ff) || n_experts > kMaxRows / d_model) return QG_EINVAL;
+    if (!shape_valid(fmt, n_experts * 2 * d_ff, d_model) || !shape_valid(fmt, n_experts * d_model, d_ff))
+        return QG_EINVAL;
+    if (ntok < 1 || topk < 1 || int64_t(ntok) * topk > kMaxPlanPairs) return QG_EINVAL;
+    if (!W_gate_up || !W_down || !x || !ids || !plan || !act || !y) return QG_EINVAL;
+    if (!aligned(W_gate_up, 16) || !aligned(W_down, 16) || !aligned(x, 16) || !aligned(act, 16) || !aligned(y, 4) ||
+        !aligned(plan, 4) || !aligned(ids, 4))
+        return QG_EALIGN;
+    if (!workspace || workspace_bytes < qgemv_expert_layer_workspace_bytes()) return QG_EWORKSPACE;
+    if (!aligned(workspace, 16)) return QG_EALIGN;
+    int dev = 0, sms = 0, optin = 0;
+    unsigned int* status = nullptr;
+    qg_status st = device_info(&dev, &sms, &optin, &status);
+    if (st != QG_OK) return st;
+    const int G = ntok * topk;
+    const int max_in = int(std::max(d_model, d_ff));
+    Tile t = apply_override(select_expert_tile(fmt, 2 * d_ff, d_model), current_override());
+    if (!depth_ok(t.depth) || t.warps < 1 || t.warps > kMaxWarps || t.ctas < 1) return QG_EINVAL;
+    t.split = 1;
+    t.rpw = t.rpw >= 4 ? 4 : 2;                                 // gate/up pairs: an even row count
+    const void* fn = expert_layer_kernel_lookup(fmt, t.rpw);
+    if (!fn) return QG_EUNSUPPORTED;
+    t.warps = std::min(t.warps, max_threads(fn) / 32);
+    auto total = [&](int depth, int warps) {
+        return size_t(plan_smem_off(smem_plan(fmt, kMaxNtok, max_in, t.rpw, depth, warps, 1).total)) +
+               size_t(plan_build_bytes(G));
+    };
+    while (total(t.depth, t.warps) + kStaticSmemReserve > size_t(optin) && t.depth > 2) --t.depth;
+    while (total(t.depth, t.warps) + kStaticSmemReserve > size_t(optin) && t.warps > 1) --t.warps;
+    const size_t smem = total(t.depth, t.warps);
+    if (t.warps < 1 || smem + kStaticSmemReserve > size_t(optin)) return QG_EUNSUPPORTED;
+    const int threads = 32 * t.warps;
+    const int occ = blocks_per_sm(fn, dev, optin, threads, smem);
+    if (occ < 1) return QG_EUNSUPPORTED;
+    // Every CTA must be resident at once (they meet at the grid barrier).
+    const int grid = int(std::min<int64_t>(int64_t(sms) * std::min(t.ctas, occ), kMaxGrid));
+
+    LayerArgs L{};
+    st = encode_weight_map(&L.gu.wmap, fmt, W_gate_up, n_experts * 2 * d_ff, d_model, t.rpw);
+    if (st != QG_OK) return st;
+    st = encode_weight_map(&L.dn.wmap, fmt, W_down, n_experts * d_model, d_ff, t.rpw);
+    if (st != QG_OK) return st;
+    const uint32_t wl = g_wait_limit.load(std::memory_order_relaxed);
+    for (ExpertArgs* a : {&L.gu, &L.dn}) {
+        a->status = status;
+        a->n_experts = int(n_experts);
+        a->n_slots = G;
+        a->depth = t.depth;
+        a->wait_limit = wl;
+        a->drain_limit = std::max<uint32_t>(wl, 1u << 16);
+        a->test_extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
+        a->fmagic = 0x4B000000u;
+        a->stage_tx = uint32_t(t.rpw * full_step_bytes(fmt));
+    }
+    L.gu.x = x;
+    L.gu.y = act;
+    L.gu.n_out = int(2 * d_ff);
+    L.gu.n_in = int(d_model);
+    L.gu.n_x = ntok;
+    L.gu.flags = QG_EXPERTS_SWIGLU;
+    L.gu.next_w = static_cast<const unsigned char*>(W_down);
+    L.gu.next_bytes = (long long)(d_model * row_stride(fmt, d_ff));
+    L.dn.x = act;
+    L.dn.y = y;
+    L.dn.n_out = int(d_model);
+    L.dn.n_in = int(d_ff);
+    L.dn.n_x = G;
+    L.dn.flags = QG_EXPERTS_X_BY_SLOT;
+    L.ids = ids;
+    L.topk = topk;
+    L.plan_out = plan;
+    L.barrier = static_cast<unsigned int*>(workspace);
+    L.barrier_limit = std::max<uint32_t>(wl, 1u << 16) / 4u;   // ~1 s of polls by default
+
+    void* params[] = {&L};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    if (launch_flags() & QG_LAUNCH_EARLY_START) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (cudaLaunchKernelExC(&cfg, fn, params) != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
+    return QG_OK;
 }
 
 qg_status qg_describe_expert_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, char* buf, size_t len) {

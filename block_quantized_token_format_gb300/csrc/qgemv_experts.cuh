@@ -121,14 +121,14 @@ struct ExpertRing {
     }
 };
 
-// One group of NE tokens (x staged in the layout for kMaxNtok tokens): stream this
+// One group of NE tokens (x staged in the layout for XT >= NE tokens): stream this
 // warp's row blocks of the expert and write y[s0 + t][row].
-template <int FMT, int RPW, int NE, class Ring>
+template <int FMT, int RPW, int NE, int XT, class Ring>
 __device__ __forceinline__ void expert_group(const ExpertArgs& a, Ring& R, unsigned char* smem, int s0,
                                              int first_block, int lane) {
     using F = Fmt<FMT>;
     constexpr int S = F::kW / 4;
-    constexpr int kCS = kMaxNtok * S + 1;
+    constexpr int kCS = XT * S + 1;
     constexpr int V = RPW * NE;
     constexpr int SPAN = 32 / Pow2Up<V>::value;
     constexpr int kStage = stage_bytes(FMT, RPW);
@@ -149,7 +149,7 @@ __device__ __forceinline__ void expert_group(const ExpertArgs& a, Ring& R, unsig
             ++R.consumed;
             const int codes_k = (kc == R.spr - 1) ? last_codes : 512;
             const uint32_t stage = uint32_t(R.sc) * uint32_t(kStage);
-            step_fma<FMT, NE, RPW, kMaxNtok>(acc, x_lane + uint32_t(kc) * (32u * kCS * 16u), code_lane + stage,
+            step_fma<FMT, NE, RPW, XT>(acc, x_lane + uint32_t(kc) * (32u * kCS * 16u), code_lane + stage,
                                    scale_lane + stage + uint32_t(codes_k), a.fmagic);
             __syncwarp();                        // every lane has read this stage before it is refilled
             R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
@@ -221,6 +221,84 @@ __device__ __forceinline__ void prefetch_next(const ExpertArgs& a, int e, int ci
 // loop's state.
 template <int RPW> struct ExpertThreads { static constexpr int value = RPW >= 4 ? 384 : 512; };
 
+// CTAs over groups: with n_groups <= C, CTA b serves group floor(b * n_groups / C),
+// whose CTAs are [ceil(g C / n_groups), ceil((g + 1) C / n_groups)); with more groups
+// than CTAs, CTA b takes whole groups b, b + C, ...
+__device__ __forceinline__ void assign_groups(int ng, int C, int b, int& g, int& gstep, int& ci, int& cn) {
+    if (ng <= C) {
+        const int d = ng > 0 ? ng : 1;
+        g = int((long long)b * ng / C);
+        const int b0 = int(((long long)g * C + d - 1) / d);
+        const int b1 = int(((long long)(g + 1) * C + d - 1) / d);
+        ci = b - b0;
+        cn = b1 - b0;
+        gstep = d;
+    } else {
+        g = b;
+        ci = 0;
+        cn = 1;
+        gstep = C;
+    }
+}
+
+// A group's first copies (and its prefetch of the next stack): they need only the
+// expert id.  (e * n_out + n_out <= 2^31 - 1, checked at launch.)
+template <class Ring>
+__device__ __forceinline__ void issue_group(const ExpertArgs& a, Ring& R, int e, int ci, int cn, int warp, int nwarps,
+                                            int lane) {
+    R.start_group(ci + cn * warp, cn * nwarps, e * a.n_out);
+    for (int s = 0; s < R.depth; ++s) R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
+    if (a.next_w != nullptr && lane == 0) prefetch_next(a, e, ci, cn, warp, nwarps);
+}
+
+// Every group this CTA serves for one projection: stage the group's x rows once,
+// then its warps stream their row blocks (the bodies for ne = 1..4).  `g_issued`:
+// the group whose first copies are already out (-1: none).  COHERENT_X: x was
+// written earlier in this kernel.
+template <int FMT, int RPW, bool COHERENT_X, class Ring>
+__device__ __forceinline__ void serve_groups(const ExpertArgs& a, Ring& R, unsigned char* smem, const int* ps, int G,
+                                             int ng, int g, int gstep, int ci, int cn, int g_issued, int warp,
+                                             int nwarps, int lane) {
+    const int first = ci + cn * warp;
+    for (; g < ng; g += gstep) {
+        int s0, ne, e, xrow[kMaxNtok];
+        if (!decode_group(a, ps, G, g, s0, ne, e, xrow)) {
+            if (threadIdx.x == 0) atomicOr(a.status, kStatusBadPlan);
+            continue;
+        }
+        if (g != g_issued) issue_group(a, R, e, ci, cn, warp, nwarps, lane);
+        __syncthreads();                         // no warp still reads the previous group's x
+        {
+            // One staging path for every ne (the layout for kMaxNtok tokens; slots of
+            // tokens >= ne are never read).
+            const float4* x4 = reinterpret_cast<const float4*>(a.x);
+            const float4* rows[kMaxNtok];
+#pragma unroll
+            for (int k = 0; k < kMaxNtok; ++k) rows[k] = x4 + (long long)xrow[k] * (a.n_in >> 2);
+            stage_x<FMT, kMaxNtok, !COHERENT_X>(smem, rows, a.n_in, R.spr, ne);
+        }
+        __syncthreads();
+        if (R.failed) continue;
+        switch (ne) {
+            case 1: expert_group<FMT, RPW, 1, kMaxNtok>(a, R, smem, s0, first, lane); break;
+            case 2: expert_group<FMT, RPW, 2, kMaxNtok>(a, R, smem, s0, first, lane); break;
+            case 3: expert_group<FMT, RPW, 3, kMaxNtok>(a, R, smem, s0, first, lane); break;
+            default: expert_group<FMT, RPW, 4, kMaxNtok>(a, R, smem, s0, first, lane); break;
+        }
+    }
+}
+
+// After a failed wait: report, then drain (bounded) the copies issued but not consumed.
+template <class Ring>
+__device__ __forceinline__ void drain_ring(const ExpertArgs& a, Ring& R, int lane) {
+    if (!R.failed) return;
+    if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
+    for (uint32_t f = R.consumed; f < R.issued; ++f) {
+        mbar_wait(R.bars + R.sc * 8, R.phase, a.drain_limit);
+        if (++R.sc == R.depth) { R.sc = 0; R.phase ^= 1u; }
+    }
+}
+
 template <int FMT, int RPW>
 __global__ void __launch_bounds__(ExpertThreads<RPW>::value, 1) qgemv_experts_kernel(const __grid_constant__ ExpertArgs a) {
     using F = Fmt<FMT>;
@@ -288,34 +366,16 @@ __global__ void __launch_bounds__(ExpertThreads<RPW>::value, 1) qgemv_experts_ke
         if (threadIdx.x == 0) atomicOr(a.status, kStatusBadPlan);
         ng = 0;
     }
-    const int C = int(gridDim.x), b = int(blockIdx.x);
     int g, gstep, ci, cn;
-    if (ng <= C) {   // CTAs in proportion: group g owns CTAs [ceil(g C / ng), ceil((g + 1) C / ng))
-        const int d = ng > 0 ? ng : 1;
-        g = int((long long)b * ng / C);
-        const int b0 = int(((long long)g * C + d - 1) / d);
-        const int b1 = int(((long long)(g + 1) * C + d - 1) / d);
-        ci = b - b0;
-        cn = b1 - b0;
-        gstep = d;
-    } else {         // more groups than CTAs: whole groups b, b + C, ...
-        g = b;
-        ci = 0;
-        cn = 1;
-        gstep = C;
-    }
+    assign_groups(ng, int(gridDim.x), int(blockIdx.x), g, gstep, ci, cn);
 
     // The first group's weight copies need only the plan: they go out before the
     // wait for the previous kernel when the plan is known to be complete.
-    // (e * n_out + n_out <= 2^31 - 1, checked at launch.)
-    const int first = ci + cn * warp;
     int g_issued = -1;
     if (g < ng) {
         int s0, ne, e, xrow[kMaxNtok];
         if (decode_group(a, ps, G, g, s0, ne, e, xrow)) {
-            R.start_group(first, cn * nwarps, e * a.n_out);
-            for (int s = 0; s < R.depth; ++s) R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
-            if (a.next_w != nullptr && lane == 0) prefetch_next(a, e, ci, cn, warp, nwarps);
+            issue_group(a, R, e, ci, cn, warp, nwarps, lane);
             g_issued = g;
         }
     }
@@ -323,49 +383,222 @@ __global__ void __launch_bounds__(ExpertThreads<RPW>::value, 1) qgemv_experts_ke
         asm volatile("griddepcontrol.wait;" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
+    serve_groups<FMT, RPW, false>(a, R, smem, ps, G, ng, g, gstep, ci, cn, g_issued, warp, nwarps, lane);
+    drain_ring(a, R, lane);
+}
 
-    for (; g < ng; g += gstep) {
-        int s0, ne, e, xrow[kMaxNtok];
-        if (!decode_group(a, ps, G, g, s0, ne, e, xrow)) {
-            if (threadIdx.x == 0) atomicOr(a.status, kStatusBadPlan);
-            continue;
-        }
-        if (g != g_issued) {
-            R.start_group(first, cn * nwarps, e * a.n_out);
-            for (int s = 0; s < R.depth; ++s) R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
-            if (a.next_w != nullptr && lane == 0) prefetch_next(a, e, ci, cn, warp, nwarps);
-        }
-        __syncthreads();                         // no warp still reads the previous group's x
-        {
-            // One staging path for every ne (the layout for kMaxNtok tokens; slots of
-            // tokens >= ne are never read).
-            const float4* x4 = reinterpret_cast<const float4*>(a.x);
-            const float4* rows[kMaxNtok];
-#pragma unroll
-            for (int k = 0; k < kMaxNtok; ++k) rows[k] = x4 + (long long)xrow[k] * (n_in >> 2);
-            stage_x<FMT, kMaxNtok>(smem, rows, n_in, R.spr, ne);
+// ------------------------------------------------------------------------------ the plan
+
+// The plan of n routed pairs, built by one CTA: a pair's slot is the number of pairs
+// with a smaller expert id, or the same id and a smaller index (a stable sort by
+// expert); a slot starts a group when its pair is its expert's 0th, 4th, 8th, ...
+// Writes the compact shared-memory form ps (2 + 3n ints: n_groups, group_start[n + 1],
+// group_expert[n], slot_token[n]) and, if gplan is not null, the full plan in the
+// header's layout.  scratch: 3n + 1 ints.  Returns false (n_groups = 0) when an id is
+// outside [0, n_experts).  Every thread of the CTA must call it.
+__device__ __forceinline__ bool plan_build(const int32_t* ids, int n, int topk, int n_experts, int* scratch, int* ps,
+                                           int32_t* gplan) {
+    const int G = n, tid = int(threadIdx.x), bd = int(blockDim.x);
+    int* e_s = scratch;
+    int* start_s = scratch + n;
+    int* pair_s = scratch + 2 * n;
+    int* count_s = scratch + 3 * n;
+    bool bad = false;
+    for (int i = tid; i < n; i += bd) {
+        const int e = __ldg(ids + i);
+        bad = bad || e < 0 || e >= n_experts;
+        e_s[i] = e;
+    }
+    if (tid == 0) *count_s = 0;
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) {
+            ps[0] = 0;
+            if (gplan) gplan[0] = 0;
         }
         __syncthreads();
-        if (R.failed) continue;
-        switch (ne) {
-            case 1: expert_group<FMT, RPW, 1>(a, R, smem, s0, first, lane); break;
-            case 2: expert_group<FMT, RPW, 2>(a, R, smem, s0, first, lane); break;
-            case 3: expert_group<FMT, RPW, 3>(a, R, smem, s0, first, lane); break;
-            default: expert_group<FMT, RPW, 4>(a, R, smem, s0, first, lane); break;
+        return false;
+    }
+    for (int i = tid; i < n; i += bd) {
+        const int e = e_s[i];
+        int r = 0, w = 0;
+        for (int j = 0; j < n; ++j) {
+            const int f = e_s[j];
+            r += (f < e) || (f == e && j < i);
+            w += (f == e && j < i);
+        }
+        pair_s[r] = i;
+        start_s[r] = (w % kMaxNtok) == 0;
+        ps[2 + 2 * G + r] = i / topk;
+        if (gplan) {
+            gplan[plan_slot_pair(G) + r] = i;
+            gplan[plan_slot_token(G) + r] = i / topk;
+            gplan[plan_pair_slot(G) + i] = r;
+        }
+    }
+    __syncthreads();
+    int mine = 0;
+    for (int s = tid; s < n; s += bd) {
+        if (!start_s[s]) continue;
+        int g = 0;
+        for (int q = 0; q < s; ++q) g += start_s[q];
+        const int e = e_s[pair_s[s]];
+        ps[plan_group_start(G) + g] = s;
+        ps[plan_group_expert(G) + g] = e;
+        if (gplan) {
+            gplan[plan_group_start(G) + g] = s;
+            gplan[plan_group_expert(G) + g] = e;
+        }
+        ++mine;
+    }
+    if (mine) atomicAdd(count_s, mine);
+    __syncthreads();
+    const int ng = *count_s;
+    for (int g = ng + tid; g <= G; g += bd) {
+        ps[plan_group_start(G) + g] = G;
+        if (g < G) ps[plan_group_expert(G) + g] = -1;
+        if (gplan) {
+            gplan[plan_group_start(G) + g] = G;
+            if (g < G) gplan[plan_group_expert(G) + g] = -1;
+        }
+    }
+    if (tid == 0) {
+        ps[0] = ng;
+        if (gplan) gplan[0] = ng;
+    }
+    __syncthreads();
+    return true;
+}
+
+// Shared memory of the plan's compact form plus its scratch, for n pairs.
+__host__ __device__ constexpr int plan_build_bytes(int n) { return (2 + 3 * n) * 4 + (3 * n + 1) * 4; }
+
+// ------------------------------------------------------------------------------ one layer
+
+// The routed-expert layer in one persistent launch: every CTA builds the plan from
+// the routing ids in shared memory (CTA 0 also writes it out), serves its groups of
+// the gate/up projection (writing silu(gate) * up and prefetching the same experts'
+// down rows into L2), issues the first copies of its down rows, and serves the same
+// groups of the down projection.  A group's down rows read only that group's
+// activation rows, which only that group's CTAs write: so the CTAs of a group meet
+// at a barrier of their own (a counter per group), and a group that finishes its
+// gate/up early goes on without waiting for the slowest group.  (With more groups
+// than CTAs a group has one CTA and needs no barrier.)  The grid is sized to be
+// resident at once; every wait is bounded.
+struct LayerArgs {
+    ExpertArgs gu;               // gate/up: x = token rows, y = activation [n_slots][d_ff], SWIGLU
+    ExpertArgs dn;               // down: x = the activation (by slot), y = [n_slots][d_model]
+    const int32_t* ids;          // [ntok][topk] routed experts
+    int topk;
+    int32_t* plan_out;           // the plan in the header's layout (written by CTA 0)
+    unsigned int* barrier;       // [0] departures, [1 + g] arrivals of group g; zero between launches
+    uint32_t barrier_limit;      // polls of the arrival counter before the barrier gives up
+};
+
+template <int FMT, int RPW>
+__global__ void __launch_bounds__(ExpertThreads<RPW>::value, 1) qgemv_expert_layer_kernel(const __grid_constant__ LayerArgs L) {
+    using F = Fmt<FMT>;
+    constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
+    constexpr int kStage = stage_bytes(FMT, RPW);
+    constexpr int kBoxX = kFullStep / 8;
+    static_assert(kFullStep == full_step(FMT) && kFullStep % 16 == 0, "step size");
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int max_in = L.gu.n_in > L.dn.n_in ? L.gu.n_in : L.dn.n_in;
+    auto spr_of = [](int n_in) {
+        const int codes = FMT == QG_Q8_0 ? n_in : FMT == QG_BF16 ? 2 * n_in : n_in / 2;
+        return (codes + 511) >> 9;
+    };
+
+    const SmemPlan sp = smem_plan(FMT, kMaxNtok, max_in, RPW, L.gu.depth, nwarps, 1);
+    ExpertRing<RPW, kStage, kBoxX> R;
+    R.depth = L.gu.depth;
+    R.bars = smem_addr(smem + sp.bar_off) + warp * R.depth * 8;
+    R.ring = ((smem_addr(smem + sp.ring_off) + 127u) & ~127u) + uint32_t(warp * R.depth * kStage);
+    R.policy = l2_evict_first_policy();
+    if (lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&L.gu.wmap)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&L.dn.wmap)) : "memory");
+        for (int s = 0; s < R.depth; ++s) mbar_init(R.bars + s * 8, 1);
+    }
+    mbar_fence_init();
+    __syncwarp();
+    // The routing ids and x come from earlier kernels, and the outputs may still be
+    // read by them.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    const int G = L.gu.n_slots;
+    int* ps = reinterpret_cast<int*>(smem + plan_smem_off(sp.total));
+    int* scratch = ps + 2 + 3 * G;
+    if (!plan_build(L.ids, G, L.topk, L.gu.n_experts, scratch, ps, blockIdx.x == 0 ? L.plan_out : nullptr)) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(L.gu.status, kStatusBadPlan);
+    }
+    const int ng = ps[0];
+    int g, gstep, ci, cn;
+    assign_groups(ng, int(gridDim.x), int(blockIdx.x), g, gstep, ci, cn);
+    const int g0 = g;
+
+    // ---- gate/up (+ activation, + L2 prefetch of the down rows)
+    R.spr = spr_of(L.gu.n_in);
+    R.nblk = (L.gu.n_out + RPW - 1) / RPW;
+    serve_groups<FMT, RPW, false>(L.gu, R, smem, ps, G, ng, g, gstep, ci, cn, -1, warp, nwarps, lane);
+
+    // ---- the first down copies need only the plan: out before the barrier
+    R.spr = spr_of(L.dn.n_in);
+    R.nblk = (L.dn.n_out + RPW - 1) / RPW;
+    int g_issued = -1;
+    if (g0 < ng) {
+        int s0, ne, e, xrow[kMaxNtok];
+        if (decode_group(L.dn, ps, G, g0, s0, ne, e, xrow)) {
+            issue_group(L.dn, R, e, ci, cn, warp, nwarps, lane);
+            g_issued = g0;
         }
     }
 
-    if (R.failed) {
-        // Report, then drain (bounded) the copies issued but not consumed.
-        if (lane == 0) atomicOr(a.status, kStatusWaitTimeout);
-        for (uint32_t f = R.consumed; f < R.issued; ++f) {
-            mbar_wait(R.bars + R.sc * 8, R.phase, a.drain_limit);
-            if (++R.sc == R.depth) { R.sc = 0; R.phase ^= 1u; }
+    // ---- group barrier (bounded): the group's activation rows are all written
+    __shared__ int passed;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        bool ok = true;
+        if (g0 < ng && ng <= int(gridDim.x)) {
+            unsigned* cnt = L.barrier + 1 + g0;
+            atomicAdd(cnt, 1u);
+            ok = false;
+            for (uint32_t it = 0; it < L.barrier_limit; ++it) {
+                unsigned v;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+                if (v >= unsigned(cn)) { ok = true; break; }
+                __nanosleep(32);
+            }
+            __threadfence();
         }
+        if (!ok) atomicOr(L.gu.status, kStatusWaitTimeout);
+        passed = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (!passed) R.failed = true;
+
+    // ---- down
+    serve_groups<FMT, RPW, true>(L.dn, R, smem, ps, G, ng, g0, gstep, ci, cn, g_issued, warp, nwarps, lane);
+    drain_ring(L.dn, R, lane);
+
+    // ---- the last CTA out resets the counters for the next launch
+    __shared__ bool last;
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(L.barrier, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (last) {
+        for (int i = threadIdx.x; i <= G; i += blockDim.x) L.barrier[i] = 0u;   // [0] and the G groups
+        __threadfence();
     }
 }
 
 // Lookup of an instantiated expert kernel (qgemv_experts.cu).
 const void* expert_kernel_lookup(int fmt, int rpw);
+const void* expert_layer_kernel_lookup(int fmt, int rpw);
 
 }  // namespace qg

@@ -341,9 +341,12 @@ __host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int r
 // not one per float4; token and chunk indices come from the loop structure and shifts
 // (S is a power of two), not from divisions.  Ends without a barrier: the caller
 // synchronizes the CTA before the staged x is read.
-template <int FMT, int NTOK>
+template <int FMT, int NTOK, bool NC = true>
 __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const (&rows)[NTOK], int n_in, int spr,
                                         int live = NTOK) {
+    // NC: x is read-only for the kernel's lifetime (non-coherent loads); otherwise x
+    // was written earlier in this kernel by other CTAs (L2 loads).
+    auto ld = [](const float4* p) { if constexpr (NC) return __ldg(p); else return __ldcg(p); };
     constexpr int S = Fmt<FMT>::kW / 4;
     constexpr int kCS = NTOK * S + 1;
     float4* xs = reinterpret_cast<float4*>(smem);
@@ -358,7 +361,7 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
             const int g = g0 + j * nt;
 #pragma unroll
             for (int t = 0; t < NTOK; ++t)
-                if (g < n4 && t < live) v[j][t] = __ldg(rows[t] + g);
+                if (g < n4 && t < live) v[j][t] = ld(rows[t] + g);
         }
 #pragma unroll
         for (int j = 0; j < kXG; ++j) {
@@ -394,7 +397,7 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
                 float sum = 0.f;
 #pragma unroll
                 for (int q = 0; q < S; ++q) {
-                    const float4 v = __ldg(src + q);
+                    const float4 v = ld(src + q);
                     sum = __fadd_rn(sum, v.x); sum = __fadd_rn(sum, v.y);
                     sum = __fadd_rn(sum, v.z); sum = __fadd_rn(sum, v.w);
                 }

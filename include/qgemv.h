@@ -245,7 +245,36 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
 #define QG_EXPERTS_PLAN_READY 2u
 #define QG_EXPERTS_SWIGLU 4u
 /* qg_describe_expert_tile: the geometry qgemv_experts would use for one expert's
- * shape, written as qg_describe_tile does. */
+ * shape, written as qg_describe_tile does.
+ *
+ * qgemv_expert_layer: the whole routed-expert layer in ONE launch (no counterpart
+ * launch structure on the pages; the same arithmetic as qg_expert_plan +
+ * qgemv_experts(gate/up, QG_EXPERTS_SWIGLU) + qgemv_experts(down, X_BY_SLOT), and
+ * bitwise the same act and y).  Every CTA builds the plan from ids in shared memory
+ * (the plan is also written to `plan`, qg_expert_plan_ints(ntok * topk) int32),
+ * computes its groups' act = silu(gate) * up ([n_slots][d_ff], device fp32, 16-byte
+ * aligned) while prefetching the same experts' down rows into L2, starts its first
+ * down copies, waits at a barrier of its group's CTAs for the group's act, then
+ * computes its groups' y = W_down . act ([n_slots][d_model], fp32, 4-byte aligned).
+ *   W_gate_up: n_experts stacked [2 d_ff][d_model] matrices, rows interleaved gate /
+ *   up (row 2j = gate j); W_down: n_experts stacked [d_model][d_ff]; both device
+ *   layout, 16-byte aligned, same fmt.  x: [ntok][d_model] fp32, 16-byte aligned.
+ *   ids: [ntok][topk] int32 (1 <= ntok * topk <= 1024).
+ *   workspace: >= qgemv_expert_layer_workspace_bytes() bytes, 16-byte aligned,
+ *   ZEROED by the caller once; each launch leaves it zeroed.  Launches sharing a
+ *   workspace must be serialized (one stream).  After QG_DEVICE_WAIT_TIMEOUT,
+ *   zero it again.
+ *   The grid is one persistent wave (every CTA resident at once); the barriers'
+ *   waits are bounded: if other work holds SMs long enough, the launch gives up with
+ *   QG_DEVICE_WAIT_TIMEOUT instead of hanging.  Errors: QG_EINVAL (shapes,
+ *   ntok * topk, null pointers), QG_EALIGN, QG_EWORKSPACE, QG_EUNSUPPORTED,
+ *   QG_ECUDA; a routed id outside [0, n_experts) sets QG_DEVICE_BAD_PLAN and the
+ *   launch computes nothing. */
+size_t    qgemv_expert_layer_workspace_bytes(void);
+qg_status qgemv_expert_layer(qg_fmt fmt, const void* W_gate_up, const void* W_down, int64_t n_experts,
+                             int64_t d_model, int64_t d_ff, const float* x, int ntok, const int32_t* ids,
+                             int topk, int32_t* plan, float* act, float* y, void* workspace,
+                             size_t workspace_bytes, void* stream);
 size_t    qg_expert_plan_ints(int64_t n_pairs);
 qg_status qg_expert_plan(const int32_t* ids, int ntok, int topk, int n_experts, int32_t* plan,
                          void* stream);

@@ -124,6 +124,28 @@ def test_expert_calls_reject_before_launch():
     assert call(wn=A + 8, nno=64, nni=256) == -2
 
 
+def test_expert_layer_rejects_before_launch():
+    lib = qg.load_library()
+    ws = qg.qgemv_expert_layer_workspace_bytes()
+    assert ws >= 8
+    # (fmt, Wgu, Wdn, n_experts, d_model, d_ff, x, ntok, ids, topk, plan, act, y, ws, ws_bytes, stream)
+    ok = dict(fmt=0, wgu=A, wdn=A, ne=512, dm=2560, ff=640, x=A, ntok=4, ids=A, topk=10, plan=A, act=A, y=A,
+              ws=A, wsb=ws)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return lib.qgemv_expert_layer(*a.values(), None)
+    assert call(fmt=9) == -1 and call(ne=0) == -1 and call(dm=48) == -1 and call(ff=0) == -1
+    assert call(ne=1 << 20) == -1                                        # stacks of >= 2^31 rows
+    assert call(ntok=0) == -1 and call(topk=0) == -1 and call(ntok=64, topk=17) == -1
+    for k in ("wgu", "wdn", "x", "ids", "plan", "act", "y"):
+        assert call(**{k: None}) == -1, k
+    assert call(wgu=A + 8) == -2 and call(x=A + 4) == -2 and call(act=A + 4) == -2 and call(y=A + 2) == -2
+    assert call(ids=A + 2) == -2 and call(plan=A + 2) == -2
+    assert call(ws=None) == -4 and call(wsb=ws - 1) == -4 and call(ws=A + 8) == -2
+
+
 def test_tile_override_grammar():
     lib = qg.load_library()
     for good in (b"rpw=4", b"depth=2,rpw=1", b"rpw=2,depth=4,warps=8,ctas=2", b"", None, b"rpw=1,", b"rpw=8", b"split=3,rpw=2", b"rpw=3", b"rpw=5", b"rpw=6"):

@@ -410,3 +410,151 @@ def test_full_size_layer_sampled():
                     if not by_slot:
                         check_swiglu(act[s, pairs][None], ref[None], den[None], f"ntok={ntok} group {g} act")
     assert qg.qg_device_status() == 0
+
+
+# ----------------------------------------------------------------------------- the layer in one launch
+
+def _layer_case(fmt, n_experts, d_model, d_ff, seed):
+    W_gu = workloads.gaussian(seed, (n_experts * 2 * d_ff, d_model), 0.02)
+    W_dn = workloads.gaussian(seed + 1, (n_experts * d_model, d_ff), 0.05)
+    c_gu, c_dn = ORC.quantize(fmt, W_gu), ORC.quantize(fmt, W_dn)
+    gu = torch.from_numpy(qg.qg_to_device_layout(fmt, c_gu, n_experts * 2 * d_ff, d_model)).to(dev())
+    dn = torch.from_numpy(qg.qg_to_device_layout(fmt, c_dn, n_experts * d_model, d_ff)).to(dev())
+    return c_gu, c_dn, gu, dn
+
+
+def _three_launches(fmt, gu, dn, n_experts, d_model, d_ff, xd, idd):
+    G = idd.numel()
+    plan = torch.full((qg.qg_expert_plan_ints(G),), -5, dtype=torch.int32, device=dev())
+    act = torch.full((G, d_ff), float("nan"), dtype=torch.float32, device=dev())
+    y = torch.full((G, d_model), float("nan"), dtype=torch.float32, device=dev())
+    qg.qg_expert_plan(idd, n_experts, plan)
+    qg.qgemv_experts(fmt, gu, n_experts, 2 * d_ff, d_model, xd, plan, G, act, swiglu=True)
+    qg.qgemv_experts(fmt, dn, n_experts, d_model, d_ff, act, plan, G, y, x_by_slot=True)
+    torch.cuda.synchronize()
+    return plan.cpu().numpy(), act.cpu().numpy(), y.cpu().numpy()
+
+
+def _one_launch(fmt, gu, dn, n_experts, d_model, d_ff, xd, idd, ws):
+    G = idd.numel()
+    plan = torch.full((qg.qg_expert_plan_ints(G),), -5, dtype=torch.int32, device=dev())
+    act = torch.full((G, d_ff), float("nan"), dtype=torch.float32, device=dev())
+    y = torch.full((G, d_model), float("nan"), dtype=torch.float32, device=dev())
+    qg.qgemv_expert_layer(fmt, gu, dn, n_experts, d_model, d_ff, xd, idd, plan, act, y, ws)
+    return plan, act, y
+
+
+def check_layer_against_oracle(fmt, c_gu, c_dn, n_experts, d_model, d_ff, ids, x, act, y, what):
+    """act against the oracle's silu(gate) * up; y against the oracle's down projection of
+    the oracle's (fp64) activation, with the activation's tolerance carried through:
+    |dy| <= 1e-3 sum |w act| + sum |w| |d act|."""
+    _, p = oracle_plan_array(ids, n_experts)
+    g_ref, g_den = slot_reference(fmt, c_gu, n_experts, 2 * d_ff, d_model, x, p, False)
+    check_swiglu(act, g_ref, g_den, what + " act")
+    gt, ut = g_ref[..., 0::2], g_ref[..., 1::2]
+    sig = 1.0 / (1.0 + np.exp(-gt))
+    act_ref = ORC.swiglu_rows(g_ref)
+    act_tol = (TOL * (np.abs(sig * (1.0 + gt * (1.0 - sig)) * ut) * g_den[..., 0::2]
+                      + np.abs(ORC.silu(gt)) * g_den[..., 1::2]) + 1e-5 * np.abs(act_ref))
+    y_ref, y_den = slot_reference(fmt, c_dn, n_experts, d_model, d_ff, act_ref, p, True)
+    _, y_carry = slot_reference(fmt, c_dn, n_experts, d_model, d_ff, act_tol, p, True)
+    bound = TOL * y_den + y_carry + 1e-30
+    assert np.all(np.isfinite(y)), what
+    bad = np.abs(y.astype(np.float64) - y_ref) > bound
+    assert not bad.any(), f"{what} y: {int(bad.sum())} outputs outside the bound"
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_layer_one_launch_equals_three_launches_and_oracle(fmt):
+    n_experts, d_model, d_ff, topk = 16, 512, 128, 4
+    c_gu, c_dn, gu, dn = _layer_case(fmt, n_experts, d_model, d_ff, 1100)
+    ws = torch.zeros(qg.qgemv_expert_layer_workspace_bytes(), dtype=torch.uint8, device=dev())
+    for ntok in (1, 2, 3, 4):
+        ids = workloads.routing(1200 + ntok, ntok, topk, n_experts, 0.65)
+        x = workloads.gaussian(1300 + ntok, (ntok, d_model), 2.0)
+        xd, idd = torch.from_numpy(x).to(dev()), torch.from_numpy(ids).to(dev())
+        plan3, act3, y3 = _three_launches(fmt, gu, dn, n_experts, d_model, d_ff, xd, idd)
+        plan1, act1, y1 = _one_launch(fmt, gu, dn, n_experts, d_model, d_ff, xd, idd, ws)
+        torch.cuda.synchronize()
+        plan1, act1, y1 = plan1.cpu().numpy(), act1.cpu().numpy(), y1.cpu().numpy()
+        want, _ = oracle_plan_array(ids, n_experts)
+        assert np.array_equal(plan1, want) and np.array_equal(plan3, want)
+        assert np.array_equal(act1.view(np.uint32), act3.view(np.uint32)), ntok
+        assert np.array_equal(y1.view(np.uint32), y3.view(np.uint32)), ntok
+        check_layer_against_oracle(fmt, c_gu, c_dn, n_experts, d_model, d_ff, ids, x, act1, y1, f"{fmt} ntok={ntok}")
+    assert not ws.cpu().numpy().any()                     # the barrier words are zero again
+    assert qg.qg_device_status() == 0
+
+
+def test_layer_back_to_back_under_early_start():
+    """Eight layer launches in a row on one workspace, early start on, no host sync:
+    each equals the three-launch path bit for bit and the workspace ends zeroed."""
+    fmt, n_experts, d_model, d_ff, topk = "q8_0", 24, 640, 192, 6
+    _, _, gu, dn = _layer_case(fmt, n_experts, d_model, d_ff, 1400)
+    ws = torch.zeros(qg.qgemv_expert_layer_workspace_bytes(), dtype=torch.uint8, device=dev())
+    cases = []
+    for r in range(8):
+        ntok = 1 + r % 4
+        ids = torch.from_numpy(workloads.routing(1500 + r, ntok, topk, n_experts, 0.3)).to(dev())
+        x = torch.from_numpy(workloads.gaussian(1600 + r, (ntok, d_model))).to(dev())
+        cases.append((ids, x))
+    want = [_three_launches(fmt, gu, dn, n_experts, d_model, d_ff, x, ids) for ids, x in cases]
+    qg.qg_set_launch_options(qg.QG_LAUNCH_EARLY_START)
+    try:
+        got = [_one_launch(fmt, gu, dn, n_experts, d_model, d_ff, x, ids, ws) for ids, x in cases]
+        torch.cuda.synchronize()
+    finally:
+        qg.qg_set_launch_options(0)
+    for (p3, a3, y3), (p1, a1, y1) in zip(want, got):
+        assert np.array_equal(p1.cpu().numpy(), p3)
+        assert np.array_equal(a1.cpu().numpy().view(np.uint32), a3.view(np.uint32))
+        assert np.array_equal(y1.cpu().numpy().view(np.uint32), y3.view(np.uint32))
+    assert not ws.cpu().numpy().any()
+    assert qg.qg_device_status() == 0
+
+
+def test_layer_full_size():
+    """512 experts of the routed-expert table's size in one launch at ntok 4: equal to the
+    three-launch path bit for bit (those are checked against the oracle above)."""
+    layer = workloads.EXPERT_LAYERS["q8_0_experts_512x2560x640_top10"]
+    n_experts, dm, ff = 64, layer.d_model, layer.d_ff
+    experts = list(range(n_experts))
+    gu = torch.from_numpy(_packed_stack(layer, 2 * ff, dm, layer.seed, experts)).to(dev())
+    dn = torch.from_numpy(_packed_stack(layer, dm, ff, layer.seed + 1, experts)).to(dev())
+    ws = torch.zeros(qg.qgemv_expert_layer_workspace_bytes(), dtype=torch.uint8, device=dev())
+    for ntok in (1, 4):
+        ids = workloads.routing(layer.seed + 40 + ntok, ntok, layer.topk, n_experts, layer.share)
+        x = workloads.activations(layer.seed + ntok, dm, ntok)
+        xd, idd = torch.from_numpy(x).to(dev()), torch.from_numpy(ids).to(dev())
+        p3, a3, y3 = _three_launches(layer.fmt, gu, dn, n_experts, dm, ff, xd, idd)
+        p1, a1, y1 = _one_launch(layer.fmt, gu, dn, n_experts, dm, ff, xd, idd, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(p1.cpu().numpy(), p3)
+        assert np.array_equal(a1.cpu().numpy().view(np.uint32), a3.view(np.uint32))
+        assert np.array_equal(y1.cpu().numpy().view(np.uint32), y3.view(np.uint32))
+    assert qg.qg_device_status() == 0
+
+
+def test_layer_bad_id_and_timeout_recover():
+    fmt, n_experts, d_model, d_ff = "q8_0", 8, 256, 64
+    _, _, gu, dn = _layer_case(fmt, n_experts, d_model, d_ff, 1700)
+    ws = torch.zeros(qg.qgemv_expert_layer_workspace_bytes(), dtype=torch.uint8, device=dev())
+    x = torch.from_numpy(workloads.gaussian(1701, (2, d_model))).to(dev())
+    bad = torch.from_numpy(np.array([[0, 8], [3, 1]], dtype=np.int32)).to(dev())
+    plan, act, y = _one_launch(fmt, gu, dn, n_experts, d_model, d_ff, x, bad, ws)
+    torch.cuda.synchronize()
+    assert plan.cpu().numpy()[0] == 0 and np.all(np.isnan(y.cpu().numpy()))
+    assert qg.qg_device_status() == qg.QG_DEVICE_BAD_PLAN
+    assert not ws.cpu().numpy().any()
+    good = torch.from_numpy(np.array([[0, 7], [3, 1]], dtype=np.int32)).to(dev())
+    qg.qg_set_wait_limit(2000, 16)
+    _one_launch(fmt, gu, dn, n_experts, d_model, d_ff, x, good, ws)
+    torch.cuda.synchronize()
+    assert qg.qg_device_status() & qg.QG_DEVICE_WAIT_TIMEOUT
+    qg.qg_set_wait_limit(0, 0)
+    assert not ws.cpu().numpy().any()                     # every CTA still met and left the barrier
+    p3, a3, y3 = _three_launches(fmt, gu, dn, n_experts, d_model, d_ff, x, good)
+    p1, a1, y1 = _one_launch(fmt, gu, dn, n_experts, d_model, d_ff, x, good, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(y1.cpu().numpy().view(np.uint32), y3.view(np.uint32))
+    assert qg.qg_device_status() == 0
