@@ -54,6 +54,8 @@ def parse_args():
     p.add_argument("--no-detail", action="store_true", help="skip the per-workload table")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--detail-only", default="", help="comma list of workload names for the table")
+    p.add_argument("--one-experts", default="", help="ntok: five routed-expert layers on a 64-expert stack "
+                   "(the small case an ncu capture profiles)")
     p.add_argument("--one", default="", help="fmt,n_out,n_in,ntok[,tile spec]: run one shape 3 times "
                                              "(a small case for ncu) and exit")
     p.add_argument("--cpu-worker", default="", help=argparse.SUPPRESS)
@@ -699,8 +701,47 @@ def one_shape(spec: str):
     print("ok", qg.qg_describe_tile(fmt, n_out, n_in, ntok))
 
 
+def one_experts(spec: str):
+    """Five routed-expert layers (plan, gate/up with the activation and the down
+    prefetch, down) at `ntok` on a 64-expert Q8_0 stack of the expert table's shapes
+    (the small case an ncu capture profiles)."""
+    import torch
+    import block_quantized_token_format_gb300 as qg
+    import __graft_entry__
+    __graft_entry__.build()
+    ntok = int(spec)
+    layer = workloads.EXPERT_LAYERS["q8_0_experts_512x2560x640_top10"]
+    E, dm, ff, U = 64, layer.d_model, layer.d_ff, 32
+    stk = {}
+    for key, (n_out, n_in, seed) in {"gu": (2 * ff, dm, layer.seed), "dn": (dm, ff, layer.seed + 1)}.items():
+        stride = qg.qg_row_stride(layer.fmt, n_in)
+        host = np.empty(U * n_out * stride, dtype=np.uint8)
+        for k in range(U):
+            qg.qg_pack(layer.fmt, workloads.expert_matrix(seed, k, n_out, n_in),
+                       out=host[k * n_out * stride:(k + 1) * n_out * stride])
+        stk[key] = torch.from_numpy(host).cuda().repeat(E // U)
+    G = ntok * layer.topk
+    x = torch.from_numpy(workloads.activations(layer.seed, dm, ntok)).cuda()
+    act = torch.zeros((G, ff), device="cuda")
+    y = torch.empty((G, dm), device="cuda")
+    plan = torch.empty(qg.qg_expert_plan_ints(G), dtype=torch.int32, device="cuda")
+    qg.qg_set_launch_options(qg.QG_LAUNCH_EARLY_START)
+    for r in range(5):
+        ids = torch.from_numpy(workloads.routing(1000 + r, ntok, layer.topk, E, layer.share)).cuda()
+        qg.qg_expert_plan(ids, E, plan)
+        qg.qgemv_experts(layer.fmt, stk["gu"], E, 2 * ff, dm, x, plan, G, act, swiglu=True, W_next=stk["dn"],
+                         next_n_out=dm, next_n_in=ff)
+        qg.qgemv_experts(layer.fmt, stk["dn"], E, dm, ff, act, plan, G, y, x_by_slot=True, plan_ready=True)
+    torch.cuda.synchronize()
+    assert qg.qg_device_status() == 0
+    print("ok", qg.qg_describe_expert_tile(layer.fmt, 2 * ff, dm))
+
+
 def main():
     args = parse_args()
+    if args.one_experts:
+        one_experts(args.one_experts)
+        return
     if args.cpu_worker:
         cpu_worker(args.cpu_worker)
         return
