@@ -271,6 +271,7 @@ qg_status qgemv_experts(qg_fmt fmt, const void* W, int64_t n_experts, int64_t n_
     a.stage_tx = uint32_t(p.tile.rpw * full_step_bytes(fmt));
     a.next_w = static_cast<const unsigned char*>(W_next);
     a.next_bytes = W_next ? (long long)(next_n_out * row_stride(fmt, next_n_in)) : 0;
+    a.group_base = p.tile.gw;
     return launch_experts(p, a, stream);
 }
 
@@ -325,6 +326,7 @@ qg_status qgemv_expert_layer(qg_fmt fmt, const void* W_gate_up, const void* W_do
     if (st != QG_OK) return st;
     const uint32_t wl = wait_limit();
     for (ExpertArgs* a : {&L.gu, &L.dn}) {
+        a->group_base = t.gw;
         a->status = status;
         a->n_experts = int(n_experts);
         a->n_slots = G;
@@ -378,7 +380,7 @@ qg_status qg_describe_expert_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, char*
     Plan p;
     qg_status st = plan_experts(fmt, n_out, n_in, &p);
     if (st != QG_OK) return st;
-    std::snprintf(buf, len, "%s,grid=%d", tile_to_string(p.tile).c_str(), p.grid);
+    std::snprintf(buf, len, "%s,gw=%d,grid=%d", tile_to_string(p.tile).c_str(), p.tile.gw, p.grid);
     return QG_OK;
 }
 

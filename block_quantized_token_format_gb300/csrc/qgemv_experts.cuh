@@ -74,6 +74,7 @@ struct ExpertArgs {
     const unsigned char* next_w;   // optional: a second stack of the same experts whose active
                                    // experts this launch prefetches into L2 (nullptr = none)
     long long next_bytes;          // bytes per expert of that stack (a multiple of 16)
+    int group_base;                // CTA shares: weight base + ne per group (0 = equal)
 };
 
 constexpr int kPrefetchPiece = 32768;   // bytes per L2 prefetch instruction
@@ -221,24 +222,74 @@ __device__ __forceinline__ void prefetch_next(const ExpertArgs& a, int e, int ci
 // loop's state.
 template <int RPW> struct ExpertThreads { static constexpr int value = RPW >= 4 ? 384 : 512; };
 
-// CTAs over groups: with n_groups <= C, CTA b serves group floor(b * n_groups / C),
-// whose CTAs are [ceil(g C / n_groups), ceil((g + 1) C / n_groups)); with more groups
-// than CTAs, CTA b takes whole groups b, b + C, ...
-__device__ __forceinline__ void assign_groups(int ng, int C, int b, int& g, int& gstep, int& ci, int& cn) {
-    if (ng <= C) {
-        const int d = ng > 0 ? ng : 1;
+// CTAs over groups.  With n_groups <= C every group gets one CTA and the other
+// C - n_groups CTAs are dealt in proportion to the groups' weights base + ne (a group
+// costs its expert's bytes, the same for all, plus compute per token; base <= 0:
+// equal shares, CTA b serving group floor(b * n_groups / C)).  With more groups than
+// CTAs, CTA b takes whole groups b, b + C, ...  `ps` is the plan in shared memory.
+// Every thread of the CTA calls it (the weighted path has a barrier).
+__device__ __forceinline__ void assign_groups(const int* ps, int G, int ng, int C, int b, int base, int& g,
+                                              int& gstep, int& ci, int& cn) {
+    if (ng > C) {
+        g = b;
+        ci = 0;
+        cn = 1;
+        gstep = C;
+        return;
+    }
+    const int d = ng > 0 ? ng : 1;
+    gstep = d;
+    // Equal shares when the weights are equal: no weighting asked for, or every group
+    // one token (ng == G, e.g. ntok 1).
+    if (base <= 0 || ng == 0 || ng == G) {
         g = int((long long)b * ng / C);
         const int b0 = int(((long long)g * C + d - 1) / d);
         const int b1 = int(((long long)(g + 1) * C + d - 1) / d);
         ci = b - b0;
         cn = b1 - b0;
-        gstep = d;
-    } else {
-        g = b;
-        ci = 0;
-        cn = 1;
-        gstep = C;
+        return;
     }
+    // The first warp computes the shares with a scan over the groups' weights (one
+    // CTA's group is the one whose CTA range holds b); the others wait at the barrier.
+    auto weight = [&](int h) {
+        int ne = ps[plan_group_start(0) + h + 1] - ps[plan_group_start(0) + h];
+        ne = ne < 0 ? 0 : ne > kMaxNtok ? kMaxNtok : ne;
+        return (long long)(base + ne);
+    };
+    __shared__ int s_assign[3];
+    if (threadIdx.x < 32) {
+        const int lane = int(threadIdx.x);
+        long long W = 0;
+        for (int h = lane; h < ng; h += 32) W += weight(h);
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) W += __shfl_xor_sync(kFull, W, m);
+        const long long extra = C - ng;
+        long long carry = 0;
+        for (int h0 = 0; h0 < ng; h0 += 32) {
+            const int h = h0 + lane;
+            const long long w = h < ng ? weight(h) : 0;
+            long long inc = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long n = __shfl_up_sync(kFull, inc, o);
+                if (lane >= o) inc += n;
+            }
+            if (h < ng) {
+                const int st = h + int((extra * (carry + inc - w) + W - 1) / W);   // first CTA of group h
+                const int nx = h + 1 + int((extra * (carry + inc) + W - 1) / W);   // first CTA of group h + 1
+                if (b >= st && b < nx) {
+                    s_assign[0] = h;
+                    s_assign[1] = st;
+                    s_assign[2] = nx;
+                }
+            }
+            carry += __shfl_sync(kFull, inc, 31);
+        }
+    }
+    __syncthreads();
+    g = s_assign[0];
+    ci = b - s_assign[1];
+    cn = s_assign[2] - s_assign[1];
 }
 
 // A group's first copies (and its prefetch of the next stack): they need only the
@@ -367,7 +418,7 @@ __global__ void __launch_bounds__(ExpertThreads<RPW>::value, 1) qgemv_experts_ke
         ng = 0;
     }
     int g, gstep, ci, cn;
-    assign_groups(ng, int(gridDim.x), int(blockIdx.x), g, gstep, ci, cn);
+    assign_groups(ps, G, ng, int(gridDim.x), int(blockIdx.x), a.group_base, g, gstep, ci, cn);
 
     // The first group's weight copies need only the plan: they go out before the
     // wait for the previous kernel when the plan is known to be complete.
@@ -538,7 +589,7 @@ __global__ void __launch_bounds__(ExpertThreads<RPW>::value, 1) qgemv_expert_lay
     }
     const int ng = ps[0];
     int g, gstep, ci, cn;
-    assign_groups(ng, int(gridDim.x), int(blockIdx.x), g, gstep, ci, cn);
+    assign_groups(ps, G, ng, int(gridDim.x), int(blockIdx.x), L.gu.group_base, g, gstep, ci, cn);
     const int g0 = g;
 
     // ---- gate/up (+ activation, + L2 prefetch of the down rows)

@@ -110,7 +110,9 @@ Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
 
 // Measured on GB300 for the routed-expert layer (gate/up 1280x2560, down 2560x640,
 // Q8_0, 10-21 active experts): 4 rows per warp, 12 warps, a 2-stage ring beat 2 rows
-// x 16 warps by 8-12% and deeper rings (3-7 stages) by 1-10%.
+// x 16 warps by 8-12% and deeper rings (3-7 stages) by 1-10%.  CTA shares weighted
+// 4 + tokens per group (a 4-token group gets 1.6x the CTAs of a 1-token group) cut
+// the layer at ntok 3-4 by 7-10% against equal shares (2 + tokens: 5-8%).
 Tile select_expert_tile(int fmt, int64_t n_out, int64_t n_in) {
     (void)fmt;
     (void)n_out;
@@ -120,6 +122,7 @@ Tile select_expert_tile(int fmt, int64_t n_out, int64_t n_in) {
     t.depth = 2;
     t.warps = 12;
     t.ctas = 1;
+    t.gw = 4;
     return t;
 }
 
@@ -143,6 +146,7 @@ Tile apply_override(Tile t, const TileOverride& o) {
     if (o.warps > 0) t.warps = o.warps;
     if (o.ctas > 0) t.ctas = o.ctas;
     if (o.split > 0) t.split = o.split;
+    if (o.gw >= 0) t.gw = o.gw;
     return t;
 }
 
@@ -168,6 +172,7 @@ bool parse_tile_spec(const char* spec, TileOverride* out) {
         else if (key == "warps") { if (v < 1 || v > 16) return false; o.warps = v; }
         else if (key == "ctas") { if (v < 1 || v > 8) return false; o.ctas = v; }
         else if (key == "split") { if (v < 1 || v > kMaxSplit) return false; o.split = v; }
+        else if (key == "gw") { if (v > 64) return false; o.gw = v; }
         else return false;
     }
     *out = o;

@@ -233,7 +233,9 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
  *   odd n_out with QG_EXPERTS_SWIGLU,
  *   n_x < n_slots with QG_EXPERTS_X_BY_SLOT, null pointer), QG_EALIGN,
  *   QG_EUNSUPPORTED, QG_ECUDA.  The geometry follows qg_set_tile_override's rpw,
- *   depth, warps and ctas (rpw 1, 2 or 4; the split does not apply).
+ *   depth, warps and ctas (rpw 1, 2 or 4; the split does not apply) and gw: the CTAs
+ *   are dealt to groups in proportion to gw + the group's token count (default 4;
+ *   0 = equal shares; equal anyway when every group has one token).
  *   W_next (optional, NULL = none): the stack of the projection that comes next
  *   (same fmt and n_experts; next_n_out rows of next_n_in per expert, device
  *   layout, 16-byte aligned), e.g. the down projection while gate/up runs.  The
@@ -322,12 +324,13 @@ qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t
  * few row groups per warp use about one segment per three steps.)
  *
  * qg_set_tile_override: force a geometry for later calls, e.g.
- * "rpw=4,depth=4,warps=8,ctas=2,split=2" (any subset of the keys; rpw in
+ * "rpw=4,depth=4,warps=8,ctas=2,split=2,gw=4" (any subset of the keys; rpw in
  * {1,2,3,4,5,6,8}: 1, 2, 4 for every ntok, 8 for ntok <= 3, 6 for ntok 2-4,
  * 3 and 5 for ntok 4 (QG_EUNSUPPORTED otherwise); where rpw * ntok > 20 (or
  * >= 16 with 4-bit codes at ntok >= 2) a CTA has at most 12 warps; depth in
  * {2..16}, warps in {1..16}, ctas in
- * {1..8}, split in {1..4}).  The split is capped at one segment per step and
+ * {1..8}, split in {1..4}, gw in {0..64}: the expert calls' group weighting).  The
+ * split is capped at one segment per step and
  * lowered until one team fits in shared memory at ntok = 4 (so it stays the
  * same for every ntok); warps are rounded to whole teams; the ring depth, then
  * the warp count, then the rows per warp are lowered if the CTA would not fit

@@ -184,7 +184,7 @@ def test_outputs_bitwise_independent_of_ne_group_and_tile(fmt):
     slot = {int(i): int(s) for i, s in enumerate(p["pair_slot"])}
     results = []
     for spec in (None, "rpw=1", "rpw=2,depth=2,warps=4", "rpw=4,depth=3,warps=8", "rpw=4,warps=12,ctas=2",
-                 "rpw=2,warps=1,depth=2"):
+                 "rpw=2,warps=1,depth=2", "gw=0", "gw=9"):
         qg.qg_set_tile_override(spec)
         results.append(run_experts(fmt, packed, n_experts, n_out, n_in, x, plan_d, 8))
     qg.qg_set_tile_override(None)
