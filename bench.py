@@ -501,9 +501,9 @@ def detail_table(args, qg, torch, dev, l2, peak):
 
 
 def experts_detail(qg, torch, dev, peak, layer, unique=32, routings=64):
-    """Routed experts, one layer: the plan, the gate/up projection (token rows, gate /
-    up row pairs written as silu(gate) * up; it also prefetches the same experts' down
-    rows into L2) and the down projection of that activation (one row per slot) per
+    """Routed experts, one layer: the plan, the gate/up projection (token rows, gate / up
+    row pairs written as silu(gate) * up; it also prefetches the same experts' down rows
+    into L2) and the down projection of that activation (one row per slot) per
     ntok, each step with its own seeded routing (64 routings in turn), timed as
     64-step graphs; "layer_one_launch" is the same layer as one persistent launch.  Bytes = the active experts' weight
     bytes (each read from HBM once per layer).  The stack holds n_experts experts at

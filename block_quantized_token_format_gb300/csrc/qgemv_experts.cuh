@@ -77,10 +77,10 @@ struct ExpertArgs {
     int group_base;                // CTA shares: weight base + ne per group (0 = equal)
 };
 
-constexpr int kPrefetchPiece = 32768;   // bytes per L2 prefetch instruction
+constexpr int kL2PrefetchPiece = 32768;   // bytes per L2 prefetch instruction
 
 // Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
                  : "memory");
 }
@@ -213,8 +213,8 @@ __device__ __forceinline__ void prefetch_next(const ExpertArgs& a, int e, int ci
     const long long lo = (long long)ci * per;
     const long long hi = lo + per < B ? lo + per : B;
     const unsigned char* base = a.next_w + (long long)e * B;
-    for (long long off = lo + (long long)warp * kPrefetchPiece; off < hi; off += (long long)nwarps * kPrefetchPiece)
-        prefetch_l2(base + off, uint32_t(hi - off < kPrefetchPiece ? hi - off : kPrefetchPiece));
+    for (long long off = lo + (long long)warp * kL2PrefetchPiece; off < hi; off += (long long)nwarps * kL2PrefetchPiece)
+        l2_prefetch(base + off, uint32_t(hi - off < kL2PrefetchPiece ? hi - off : kL2PrefetchPiece));
 }
 
 // Threads per CTA: 16 warps up to 2 rows per warp; 12 warps (168 registers a thread)
