@@ -501,7 +501,10 @@ __device__ __forceinline__ bool plan_build(const int32_t* ids, int n, int topk, 
         }
         ++mine;
     }
-    if (mine) atomicAdd(count_s, mine);
+    // One shared atomic per warp (a per-thread atomic on one word serialises).
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) mine += __shfl_xor_sync(kFull, mine, m);
+    if ((tid & 31) == 0 && mine) atomicAdd(count_s, mine);
     __syncthreads();
     const int ng = *count_s;
     for (int g = ng + tid; g <= G; g += bd) {

@@ -7,7 +7,7 @@ tile specs (qg_set_tile_override grammar; default: a grid over rows per warp,
 ring depth, warps per CTA and CTAs per SM); NTOKS: comma list (default 1,2,3,4).
 Each point is the median of 3 CUDA-graph replays of 20 launches that rotate over
 weight copies totalling >= 4x L2.  One JSON line per point goes to FILE
-(default gpurun_out/sweep.jsonl) and the best spec per (workload, ntok) is
+(default tile_sweep.jsonl in the working directory) and the best spec per (workload, ntok) is
 printed.  Set QGEMV_EARLY_START=1 to sweep with early-start launches.  The
 table in csrc/tile_select.cpp was filled from such sweeps.
 """
@@ -50,7 +50,7 @@ def main(argv=None):
     ap.add_argument("names")
     ap.add_argument("specs", nargs="?", default="")
     ap.add_argument("ntoks", nargs="?", default="1,2,3,4")
-    ap.add_argument("--out", default=os.path.join("gpurun_out", "sweep.jsonl"))
+    ap.add_argument("--out", default="tile_sweep.jsonl")
     a = ap.parse_args(argv)
     specs = a.specs.split(";") if a.specs else [
         f"rpw={r},depth={d},warps={w},ctas={c}"
