@@ -10,15 +10,17 @@
 // separates routing from the projections.
 //
 // GB300 design, on the pieces of the plain mat-vec kernel (stage_x, step_fma,
-// warp_reduce): a persistent grid whose CTAs are dealt to groups in proportion
-// (CTA b of C serves group floor(b * n_groups / C), so every group gets C /
-// n_groups CTAs, rounded down or up); a CTA stages the x rows of its group's ne
-// tokens once and its warps stream the expert's row blocks round-robin through
-// their TMA rings.  ne is a run-time value: the kernel switches to a body
-// compiled for each ne, so a one-token group costs what a one-token mat-vec
-// costs.  The first copies of a group need only the expert id and go out before
-// x is staged.  With more groups than CTAs, a CTA takes groups b, b + C, ...
-// one after the other, restaging x between them.
+// warp_reduce): a persistent grid whose CTAs are dealt to groups (one each, the
+// rest in proportion to a weight base + the group's token count, since a group's
+// compute grows with its tokens; see assign_groups); a CTA stages the x rows of its
+// group's ne tokens once and its warps stream the expert's row blocks round-robin
+// through their TMA rings.  ne is a run-time value: the kernel switches to a body
+// compiled for each ne, so a one-token group costs what a one-token mat-vec costs.
+// The first copies of a group need only the expert id and go out before x is
+// staged.  With more groups than CTAs, a CTA takes groups b, b + C, ... one after
+// the other, restaging x between them.  The same pieces also make the whole layer
+// (plan, gate/up with its activation, down) one persistent launch
+// (qgemv_expert_layer_kernel, below).
 //
 // Optionally a launch also prefetches into L2 the same experts' rows of the NEXT
 // projection's stack (the down projection while gate/up runs): the 129 MB L2
