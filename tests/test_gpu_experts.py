@@ -558,3 +558,32 @@ def test_layer_bad_id_and_timeout_recover():
     torch.cuda.synchronize()
     assert np.array_equal(y1.cpu().numpy().view(np.uint32), y3.view(np.uint32))
     assert qg.qg_device_status() == 0
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "affine4_g64"])
+def test_one_x_row_and_repeated_experts(fmt):
+    """A single x row (gate/up at ntok 1) gives bitwise the results of the same call with
+    a second, unused row, also for a token that lists an expert more than once (one
+    group of several slots, all reading the same row)."""
+    n_experts, n_out, n_in = 12, 96, n_in_for(fmt, 2560)
+    n_in, canon, packed = _small_case(fmt, n_experts, n_out, n_in, 1800)
+    x1 = workloads.gaussian(1801, (1, n_in))
+    x2 = np.concatenate([x1, workloads.gaussian(1802, (1, n_in))])    # a second, unused row
+    for ids in (workloads.routing(1803, 1, 5, n_experts, 0.65), np.array([[3, 3, 5, 7, 3]], dtype=np.int32)):
+        plan_d = gpu_plan(ids, n_experts)
+        G = ids.size
+        for swiglu in (False, True):
+            outs = []
+            for x in (x1, x2):
+                xd = torch.from_numpy(x).to(dev())
+                y = torch.full((G, n_out // 2 if swiglu else n_out), float("nan"), dtype=torch.float32, device=dev())
+                qg.qgemv_experts(fmt, packed, n_experts, n_out, n_in, xd, plan_d, G, y, swiglu=swiglu)
+                torch.cuda.synchronize()
+                outs.append(y.cpu().numpy())
+            assert np.all(np.isfinite(outs[0]))
+            assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32)), (ids.tolist(), swiglu)
+        _, p = oracle_plan_array(ids, n_experts)
+        ref, den = slot_reference(fmt, canon, n_experts, n_out, n_in, x1, p, False)
+        y = run_experts(fmt, packed, n_experts, n_out, n_in, x1, plan_d, G)
+        check_close(y, ref, den, f"{fmt} one row {ids.tolist()}")
+    assert qg.qg_device_status() == 0
