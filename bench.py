@@ -56,6 +56,7 @@ def parse_args():
     p.add_argument("--detail-only", default="", help="comma list of workload names for the table")
     p.add_argument("--one-experts", default="", help="ntok: five routed-expert layers on a 64-expert stack "
                    "(the small case an ncu capture profiles)")
+    p.add_argument("--one-layer", default="", help="ntok: as --one-experts, with the layer as one launch")
     p.add_argument("--one", default="", help="fmt,n_out,n_in,ntok[,tile spec]: run one shape 3 times "
                                              "(a small case for ncu) and exit")
     p.add_argument("--cpu-worker", default="", help=argparse.SUPPRESS)
@@ -701,10 +702,10 @@ def one_shape(spec: str):
     print("ok", qg.qg_describe_tile(fmt, n_out, n_in, ntok))
 
 
-def one_experts(spec: str):
+def one_experts(spec: str, one_launch: bool = False):
     """Five routed-expert layers (plan, gate/up with the activation and the down
-    prefetch, down) at `ntok` on a 64-expert Q8_0 stack of the expert table's shapes
-    (the small case an ncu capture profiles)."""
+    prefetch, down; or, with one_launch, qgemv_expert_layer) at `ntok` on a 64-expert
+    Q8_0 stack of the expert table's shapes (the small case an ncu capture profiles)."""
     import torch
     import block_quantized_token_format_gb300 as qg
     import __graft_entry__
@@ -726,8 +727,12 @@ def one_experts(spec: str):
     y = torch.empty((G, dm), device="cuda")
     plan = torch.empty(qg.qg_expert_plan_ints(G), dtype=torch.int32, device="cuda")
     qg.qg_set_launch_options(qg.QG_LAUNCH_EARLY_START)
+    ws = torch.zeros(qg.qgemv_expert_layer_workspace_bytes(), dtype=torch.uint8, device="cuda")
     for r in range(5):
         ids = torch.from_numpy(workloads.routing(1000 + r, ntok, layer.topk, E, layer.share)).cuda()
+        if one_launch:
+            qg.qgemv_expert_layer(layer.fmt, stk["gu"], stk["dn"], E, dm, ff, x, ids, plan, act, y, ws)
+            continue
         qg.qg_expert_plan(ids, E, plan)
         qg.qgemv_experts(layer.fmt, stk["gu"], E, 2 * ff, dm, x, plan, G, act, swiglu=True, W_next=stk["dn"],
                          next_n_out=dm, next_n_in=ff)
@@ -741,6 +746,9 @@ def main():
     args = parse_args()
     if args.one_experts:
         one_experts(args.one_experts)
+        return
+    if args.one_layer:
+        one_experts(args.one_layer, one_launch=True)
         return
     if args.cpu_worker:
         cpu_worker(args.cpu_worker)
