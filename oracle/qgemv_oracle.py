@@ -55,6 +55,13 @@ silent):
   codes, element k at bits [4k, 4k+4); fp16 scales ``[n_out][n_in/64]``; fp16
   biases ``[n_out][n_in/64]``.  Dequant ``q * s + b``.
 * BF16: fp32 rounded to nearest even, row-major ``[n_out][n_in]``.
+* Q5_0, blocks of 32 (named on the opus-mtp-turbo Track 1 report, item 3, with its
+  quantization-error table; the pages give no layout): the 5-bit analogue of Q4_0.
+  ``m`` = the signed value of largest magnitude (first on ties), ``d = m / -16`` in
+  fp32, stored fp16; ``q = clamp(round(w / d) + 16, 0, 31)`` (unrounded d, half away
+  from zero); ``m == 0`` gives ``d = 0, q = 16``.  Block bytes: fp16 d, a uint32
+  whose bit j is bit 4 of element j's code, then 16 bytes where byte j holds the low
+  nibbles of elements j and j + 16 (the Q4_0 order) = 22 B.  Dequant ``(q - 16) * d``.
 
 "Parity unpinned": none.  Every function here is pinned by ``tests/`` against
 exact rational brute force, hand-built golden blocks under ``tests/golden/``,
@@ -64,14 +71,15 @@ from __future__ import annotations
 
 import numpy as np
 
-Q8_0, Q4_0, AFFINE4_G64, BF16 = 0, 1, 2, 3
-FMT_NAMES = {"q8_0": Q8_0, "q4_0": Q4_0, "affine4_g64": AFFINE4_G64, "bf16": BF16}
+Q8_0, Q4_0, AFFINE4_G64, BF16, Q5_0 = 0, 1, 2, 3, 4
+FMT_NAMES = {"q8_0": Q8_0, "q4_0": Q4_0, "affine4_g64": AFFINE4_G64, "bf16": BF16, "q5_0": Q5_0}
 
 # Weights per scale block / group.
-BLOCK = {Q8_0: 32, Q4_0: 32, AFFINE4_G64: 64, BF16: 1}
+BLOCK = {Q8_0: 32, Q4_0: 32, AFFINE4_G64: 64, BF16: 1, Q5_0: 32}
 
 _Q8_BLOCK = np.dtype([("d", "<f2"), ("q", "i1", (32,))])
 _Q4_BLOCK = np.dtype([("d", "<f2"), ("qs", "u1", (16,))])
+_Q5_BLOCK = np.dtype([("d", "<f2"), ("qh", "<u4"), ("qs", "u1", (16,))])
 
 ROW_CHUNK = 4096
 GEMV_CHUNK = 1024
@@ -100,6 +108,8 @@ def weight_bytes(fmt, n_out: int, n_in: int) -> int:
         return n // 2 + (n // 64) * 4
     if f == BF16:
         return n * 2
+    if f == Q5_0:
+        return n // 32 * 22
     raise ValueError(fmt)
 
 
@@ -138,6 +148,8 @@ def quantize(fmt, W: np.ndarray) -> np.ndarray:
         return _quantize_affine4(W)
     if f == BF16:
         return f32_to_bf16_bits(W).reshape(-1).view(np.uint8).copy()
+    if f == Q5_0:
+        return _quantize_q5_0(W)
     raise ValueError(fmt)
 
 
@@ -171,6 +183,26 @@ def _quantize_q4_0(W: np.ndarray) -> np.ndarray:
     out = np.empty((n_out, n_in // 32), dtype=_Q4_BLOCK)
     out["d"] = d32.astype(np.float16)
     out["qs"] = q[..., :16] | (q[..., 16:] << 4)
+    return out.reshape(-1).view(np.uint8).copy()
+
+
+def _quantize_q5_0(W: np.ndarray) -> np.ndarray:
+    n_out, n_in = W.shape
+    assert n_in % 32 == 0
+    B = W.reshape(n_out, n_in // 32, 32)
+    first = np.argmax(np.abs(B), axis=2)                    # first index on ties
+    m5 = np.take_along_axis(B, first[..., None], axis=2)[..., 0]
+    d32 = m5 / np.float32(-16)
+    safe = np.where(d32 != 0, d32, np.float32(1))
+    q = round_half_away(B / safe[..., None]) + np.float32(16)
+    q = np.where(d32[..., None] != 0, q, np.float32(16))
+    q = np.clip(q, 0, 31).astype(np.uint32)
+    out = np.empty((n_out, n_in // 32), dtype=_Q5_BLOCK)
+    out["d"] = d32.astype(np.float16)
+    out["qh"] = np.sum(((q >> np.uint32(4)) & np.uint32(1)) << np.arange(32, dtype=np.uint32), axis=2,
+                       dtype=np.uint32)
+    lo = (q & np.uint32(0xF)).astype(np.uint8)
+    out["qs"] = lo[..., :16] | (lo[..., 16:] << 4)
     return out.reshape(-1).view(np.uint8).copy()
 
 
@@ -229,6 +261,13 @@ def dequantize(fmt, packed: np.ndarray, n_out: int, n_in: int) -> np.ndarray:
         return (q * s[..., None] + b[..., None]).reshape(n_out, n_in)
     if f == BF16:
         return bf16_bits_to_f64(packed.view("<u2")).reshape(n_out, n_in)
+    if f == Q5_0:
+        blk = packed.view(_Q5_BLOCK).reshape(n_out, n_in // 32)
+        d = blk["d"].astype(np.float64)
+        lo = np.concatenate([blk["qs"] & 0x0F, blk["qs"] >> 4], axis=2).astype(np.uint32)   # elements 0..31
+        hb = (blk["qh"][..., None] >> np.arange(32, dtype=np.uint32)) & np.uint32(1)
+        q = (lo | (hb << np.uint32(4))).astype(np.float64)
+        return ((q - 16.0) * d[..., None]).reshape(n_out, n_in)
     raise ValueError(fmt)
 
 

@@ -51,6 +51,13 @@ MUTATIONS = {
                                            "rows = slots if not x_by_slot else"),
     "swiglu gate and up swapped": ("return silu(y[..., 0::2]) * y[..., 1::2]", "return silu(y[..., 1::2]) * y[..., 0::2]"),
     "silu without the sigmoid": ("return v / (1.0 + np.exp(-v))", "return v / (1.0 + np.exp(v))"),
+    "q5 offset 15": ("return ((q - 16.0) * d[..., None]).reshape(n_out, n_in)",
+                     "return ((q - 15.0) * d[..., None]).reshape(n_out, n_in)"),
+    "q5 high bit of the next element": ("hb = (blk[\"qh\"][..., None] >> np.arange(32, dtype=np.uint32)) & np.uint32(1)",
+                                         "hb = (blk[\"qh\"][..., None] >> ((np.arange(32, dtype=np.uint32) + 1) % 32)) & np.uint32(1)"),
+    "q5 divisor 15": ("d32 = m5 / np.float32(-16)", "d32 = m5 / np.float32(-15)"),
+    "q5 unsigned max": ("m5 = np.take_along_axis(B, first[..., None], axis=2)[..., 0]",
+                        "m5 = np.abs(np.take_along_axis(B, first[..., None], axis=2)[..., 0])"),
     "draft gather ignores affine scales": ("s = packed[nw * 4: nw * 4 + ng * 2].reshape(n_out, n_in // 32)[ids]",
                                            "s = packed[nw * 4: nw * 4 + ng * 2].reshape(n_out, n_in // 32)[:ids.size]"),
 }

@@ -87,6 +87,18 @@ def brute_decode(fmt: int, raw: bytes, n_out: int, n_in: int):
                 q = (w >> (4 * (i % 8))) & 15
                 g = r * (n_in // 64) + i // 64
                 W[r][i] = q * _f16(sc[g]) + _f16(bi[g])
+    elif fmt == ORC.Q5_0:
+        nb = n_in // 32
+        for r in range(n_out):
+            for b in range(nb):
+                off = (r * nb + b) * 22
+                d = _f16(struct.unpack_from("<H", raw, off)[0])
+                qh = struct.unpack_from("<I", raw, off + 2)[0]
+                qs = struct.unpack_from("<16B", raw, off + 6)
+                for j in range(16):
+                    lo0, lo1 = qs[j] & 15, qs[j] >> 4
+                    W[r][32 * b + j] = ((lo0 | (((qh >> j) & 1) << 4)) - 16) * d
+                    W[r][32 * b + j + 16] = ((lo1 | (((qh >> (j + 16)) & 1) << 4)) - 16) * d
     elif fmt == ORC.BF16:
         vals = struct.unpack_from(f"<{n_out * n_in}H", raw, 0)
         for r in range(n_out):
@@ -144,6 +156,25 @@ def check_golden_q4_0(orc):
     assert np.array_equal(back, raw)
 
 
+def check_golden_q5_0(orc):
+    g = _load("q5_0_block.json")
+    raw = np.array(g["bytes"], dtype=np.uint8)
+    assert raw.size == 22
+    deq = orc.dequantize("q5_0", raw, 1, 32)
+    assert np.array_equal(deq[0], np.array(g["values"], dtype=np.float64))
+    back = orc.quantize("q5_0", np.array([g["values"]], dtype=np.float32))
+    assert np.array_equal(back, raw)
+    # half away from zero: m = -4 gives d = 0.25; w = 0.625 is 2.5 d -> q = 3 + 16 = 19
+    w = np.zeros((1, 32), np.float32)
+    w[0, 0], w[0, 5] = -4.0, 0.625
+    deq = orc.dequantize("q5_0", orc.quantize("q5_0", w), 1, 32)
+    assert deq[0, 5] == 0.75 and deq[0, 0] == -4.0
+    # an all-zero block: d = 0 / -16 = -0 (fp16 0x8000), every code 16 (bit 4 set, low nibble 0)
+    z = orc.quantize("q5_0", np.zeros((1, 32), np.float32))
+    assert list(z[:6]) == [0x00, 0x80, 0xFF, 0xFF, 0xFF, 0xFF] and all(b == 0 for b in z[6:])
+    assert not orc.dequantize("q5_0", z, 1, 32).any()
+
+
 def check_golden_affine4(orc):
     g = _load("affine4_group.json")
     words = np.array([int(w, 16) for w in g["words"]], dtype="<u4")
@@ -199,7 +230,7 @@ def check_rounding(orc):
 
 def check_brute_force(orc):
     """The fp64 mat-vec equals exact rational arithmetic from the raw bytes."""
-    for fmt in ("q8_0", "q4_0", "affine4_g64", "bf16"):
+    for fmt in ("q8_0", "q4_0", "affine4_g64", "bf16", "q5_0"):
         f = orc.fmt_id(fmt)
         for n_out, n_in in ((1, 64), (3, 64), (7, 128)):
             W = workloads.gaussian(1000 + n_out + n_in + f, (n_out, n_in), 0.02)
@@ -219,8 +250,8 @@ def check_brute_force(orc):
 
 
 def check_idempotence(orc):
-    """quantize(dequantize(B)) == B on random blocks (Q8_0 and Q4_0)."""
-    for fmt in ("q8_0", "q4_0"):
+    """quantize(dequantize(B)) == B on random blocks (Q8_0, Q4_0, Q5_0)."""
+    for fmt in ("q8_0", "q4_0", "q5_0"):
         W = workloads.gaussian(77, (64, 256), 0.02)
         raw = orc.quantize(fmt, W)
         deq = orc.dequantize(fmt, raw, 64, 256).astype(np.float32)
@@ -315,17 +346,23 @@ def check_argmax(orc):
 
 def check_quant_error_band(orc):
     """GEMV rel-RMSE vs the fp32 weights on N(0, 0.02) W, N(0,1) x: same order as the
-    0.58-1.18% (Q8_0) and 5.8-10.7% (Q4_0) that the opus-mtp-turbo report's item 3
-    table measures on real tensors.  A sanity band, not a parity check."""
+    0.58-1.18% (Q8_0), 4.4-5.6% (Q5_0) and 5.8-10.7% (Q4_0) that the opus-mtp-turbo
+    report's item 3 table measures on real tensors, and Q5_0 between Q8_0 and Q4_0.
+    A sanity band, not a parity check."""
     n_out, n_in = 256, 2560
     W = workloads.gaussian(51, (n_out, n_in), 0.02)
     x = workloads.gaussian(52, (8, n_in))
     ref = x.astype(np.float64) @ W.astype(np.float64).T
-    bands = {"q8_0": (0.003, 0.012), "q4_0": (0.04, 0.12), "affine4_g64": (0.04, 0.12), "bf16": (0.0005, 0.004)}
+    bands = {"q8_0": (0.003, 0.012), "q4_0": (0.04, 0.12), "affine4_g64": (0.04, 0.12), "bf16": (0.0005, 0.004),
+             "q5_0": (0.02, 0.06)}
+    rels = {}
     for fmt, (lo, hi) in bands.items():
         y = orc.gemv(fmt, orc.quantize(fmt, W), n_out, n_in, x)
         rel = np.sqrt(np.mean((y - ref) ** 2) / np.mean(ref ** 2))
+        rels[fmt] = rel
         assert lo <= rel <= hi, (fmt, rel)
+    assert rels["q8_0"] < rels["q5_0"] < rels["q4_0"]
+    assert 1.6 < rels["q4_0"] / rels["q5_0"] < 2.4          # one more bit: about half the error
 
 
 def check_fp16_bf16_rounding(orc):
@@ -480,7 +517,7 @@ def check_swiglu(orc):
     assert a.shape == (1, 3) and np.allclose(a[0], want, rtol=1e-15, atol=1e-15)
 
 
-ALL_CHECKS = [check_page_byte_counts, check_golden_q8_0, check_golden_q4_0, check_golden_affine4,
+ALL_CHECKS = [check_page_byte_counts, check_golden_q8_0, check_golden_q4_0, check_golden_q5_0, check_golden_affine4,
               check_golden_bf16, check_rounding, check_brute_force, check_idempotence,
               check_affine_constructed_roundtrip, check_linearity, check_token_independence,
               check_cross_format, check_argmax, check_quant_error_band, check_fp16_bf16_rounding,
