@@ -111,7 +111,8 @@ def algo_bytes(fmt, n_out, n_in, ntok, argmax=False):
 
 def workloads_bytes(fmt, n_out, n_in):
     n = n_out * n_in
-    return {"q8_0": n // 32 * 34, "q4_0": n // 32 * 18, "affine4_g64": n // 2 + n // 64 * 4, "bf16": 2 * n}[fmt]
+    return {"q8_0": n // 32 * 34, "q4_0": n // 32 * 18, "affine4_g64": n // 2 + n // 64 * 4, "bf16": 2 * n,
+            "q5_0": n // 32 * 22}[fmt]
 
 
 class ClockSampler:

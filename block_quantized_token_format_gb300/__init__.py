@@ -16,7 +16,7 @@ import os
 import numpy as np
 
 __all__ = [
-    "QG_Q8_0", "QG_Q4_0", "QG_AFFINE4_G64", "QG_BF16", "FORMATS", "QGError", "load_library",
+    "QG_Q8_0", "QG_Q4_0", "QG_AFFINE4_G64", "QG_BF16", "QG_Q5_0", "FORMATS", "QGError", "load_library",
     "qg_strerror", "qg_abi_version", "qg_canonical_bytes", "qg_packed_bytes", "qg_row_stride",
     "qg_quantize", "qg_to_device_layout", "qg_pack", "qgemv", "qgemv_argmax_workspace_bytes",
     "qgemv_argmax", "qg_set_tile_override", "qg_describe_tile", "weight_bytes", "qg_device_status",
@@ -27,8 +27,8 @@ __all__ = [
     "QG_EXPERTS_SWIGLU", "qgemv_expert_layer", "qgemv_expert_layer_workspace_bytes",
 ]
 
-QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16 = 0, 1, 2, 3
-FORMATS = {"q8_0": QG_Q8_0, "q4_0": QG_Q4_0, "affine4_g64": QG_AFFINE4_G64, "bf16": QG_BF16}
+QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16, QG_Q5_0 = 0, 1, 2, 3, 4
+FORMATS = {"q8_0": QG_Q8_0, "q4_0": QG_Q4_0, "affine4_g64": QG_AFFINE4_G64, "bf16": QG_BF16, "q5_0": QG_Q5_0}
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqgemv.so")
 _lib = None

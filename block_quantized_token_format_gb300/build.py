@@ -1,7 +1,7 @@
 """Build the CUDA shared library ``_lib/libqgemv.so`` in-tree (sm_103a only).
 
-Compiles the four per-format kernel units, the C ABI and the host packer in
-parallel with nvcc / g++, then links one shared library.  Object files go to
+Compiles the per-format kernel units, the expert kernels, the C ABI and the host
+packer in parallel with nvcc / g++, then links one shared library.  Object files go to
 ``_build/`` at the repository root.  A stamp of the sources and flags skips
 the work when nothing changed.
 """
@@ -43,7 +43,7 @@ def _units():
     nvcc = os.path.join(cuda, "bin", "nvcc")
     cxx = os.environ.get("CXX", "g++")
     units = []
-    for f in range(4):
+    for f in range(5):
         units.append((os.path.join(BUILD, f"qgemv_inst_fmt{f}.o"),
                       [nvcc, *ARCH, *NVCC_FLAGS, f"-DQG_INST_FMT={f}", "-c",
                        os.path.join(CSRC, "qgemv_inst.cu")]))

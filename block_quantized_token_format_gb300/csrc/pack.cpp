@@ -1,6 +1,6 @@
 // Host weight packer: fp32 -> canonical block bytes -> device layout.
 //
-// The quantizer rules are the workload definitions of the four formats
+// The quantizer rules are the workload definitions of the formats
 // (Q8_0 / Q4_0 named in "Where the time goes on an M2 Max", format table, and
 // the opus-mtp-turbo Track 1 report, item 3; the MLX-style affine 4-bit head
 // in "perf(speculative): cut the MTP drafter's per-step cost", section "The
@@ -100,6 +100,28 @@ void quant_row_q4_0(const float* w, int64_t n_in, uint8_t* out) {
     }
 }
 
+// Q5_0: the Q4_0 rule with 5-bit codes (d = m / -16, q = clamp(roundf(w/d) + 16, 0, 31)).
+void quant_row_q5_0(const float* w, int64_t n_in, uint8_t* out) {
+    for (int64_t b = 0; b < n_in / 32; ++b) {
+        const float* v = w + 32 * b;
+        float m = 0.f, amax = -1.f;
+        for (int j = 0; j < 32; ++j)
+            if (std::fabs(v[j]) > amax) { amax = std::fabs(v[j]); m = v[j]; }   // first on ties
+        const float d = m / -16.0f;
+        uint8_t q[32];
+        uint32_t qh = 0;
+        for (int j = 0; j < 32; ++j) {
+            float c = d != 0.f ? std::roundf(v[j] / d) + 16.f : 16.f;
+            q[j] = uint8_t(std::min(31.f, std::max(0.f, c)));
+            qh |= uint32_t(q[j] >> 4) << j;
+        }
+        uint8_t* blk = out + 22 * b;
+        put16(blk, f32_to_f16(d));
+        put32(blk + 2, qh);
+        for (int j = 0; j < 16; ++j) blk[6 + j] = uint8_t((q[j] & 0xF) | ((q[j + 16] & 0xF) << 4));
+    }
+}
+
 // Affine rows write into three planes: words, scales, biases.
 void quant_row_affine4(const float* w, int64_t n_in, uint8_t* words, uint8_t* scales, uint8_t* biases) {
     for (int64_t g = 0; g < n_in / 64; ++g) {
@@ -166,6 +188,22 @@ void flat_device_row(int fmt, CanonRow c, int64_t n_in, uint8_t* dst) {
         case QG_BF16:
             std::memcpy(dst, c.a, size_t(cb));
             break;
+        case QG_Q5_0:
+            // codes: the low nibbles as Q4_0's words; scales: per block its fifth bits
+            // (uint32, bit j = element j) and then its fp16 d, 6 bytes.
+            for (int64_t b = 0; b < n_in / 32; ++b) {
+                const uint8_t* blk = c.a + 22 * b;
+                std::memcpy(dst + cb + 6 * b, blk + 2, 4);
+                std::memcpy(dst + cb + 6 * b + 4, blk, 2);
+                uint8_t q[32];
+                for (int j = 0; j < 16; ++j) { q[j] = blk[6 + j] & 0xF; q[j + 16] = blk[6 + j] >> 4; }
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t word = 0;
+                    for (int e = 0; e < 8; ++e) word |= uint32_t(q[8 * m + e]) << (4 * e);
+                    put32(dst + 16 * b + 4 * m, word);
+                }
+            }
+            break;
     }
 }
 
@@ -204,6 +242,7 @@ void quant_row(int fmt, const float* w, int64_t n_in, uint8_t* canon, int64_t n_
     uint8_t* out = canon + r * qg::canonical_row_bytes(fmt, n_in);
     if (fmt == QG_Q8_0) quant_row_q8_0(w, n_in, out);
     else if (fmt == QG_Q4_0) quant_row_q4_0(w, n_in, out);
+    else if (fmt == QG_Q5_0) quant_row_q5_0(w, n_in, out);
     else quant_row_bf16(w, n_in, out);
 }
 

@@ -17,12 +17,12 @@ namespace qg {
 constexpr int kMaxNtok = 4;
 constexpr int kChunkWeights = 16;   // weights per lane-chunk in every kernel
 
-inline bool fmt_valid(int fmt) { return fmt >= QG_Q8_0 && fmt <= QG_BF16; }
+inline bool fmt_valid(int fmt) { return fmt >= QG_Q8_0 && fmt <= QG_Q5_0; }
 
 // n_in must be a positive multiple of this.
 inline int64_t n_in_multiple(int fmt) {
     switch (fmt) {
-        case QG_Q8_0: case QG_Q4_0: return 32;
+        case QG_Q8_0: case QG_Q4_0: case QG_Q5_0: return 32;
         case QG_AFFINE4_G64: return 64;
         case QG_BF16: return 16;          // one lane-chunk of 16 weights
         default: return 0;
@@ -39,7 +39,7 @@ inline bool shape_valid(int fmt, int64_t n_out, int64_t n_in) {
 inline int64_t codes_bytes(int fmt, int64_t n_in) {
     switch (fmt) {
         case QG_Q8_0: return n_in;
-        case QG_Q4_0: case QG_AFFINE4_G64: return n_in / 2;
+        case QG_Q4_0: case QG_AFFINE4_G64: case QG_Q5_0: return n_in / 2;
         case QG_BF16: return 2 * n_in;
         default: return 0;
     }
@@ -51,6 +51,7 @@ inline int64_t scale_bytes_for(int fmt, int64_t codes) {
         case QG_Q8_0: return codes / 16;         // one fp16 d per 32 one-byte codes
         case QG_Q4_0: return codes / 8;          // one fp16 d per 16 bytes of nibbles
         case QG_AFFINE4_G64: return codes / 8;   // one (fp16 s, fp16 b) per 32 bytes of nibbles
+        case QG_Q5_0: return codes / 16 * 6;     // one (uint32 fifth bits, fp16 d) per 16 bytes of nibbles
         default: return 0;
     }
 }

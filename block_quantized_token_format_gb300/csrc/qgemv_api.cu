@@ -20,6 +20,7 @@ const void* kernel_lookup_fmt0(int, int, bool, bool);
 const void* kernel_lookup_fmt1(int, int, bool, bool);
 const void* kernel_lookup_fmt2(int, int, bool, bool);
 const void* kernel_lookup_fmt3(int, int, bool, bool);
+const void* kernel_lookup_fmt4(int, int, bool, bool);
 
 const void* kernel_lookup(int fmt, int ntok, int rpw, bool argmax, bool split) {
     switch (fmt) {
@@ -27,6 +28,7 @@ const void* kernel_lookup(int fmt, int ntok, int rpw, bool argmax, bool split) {
         case 1: return kernel_lookup_fmt1(ntok, rpw, argmax, split);
         case 2: return kernel_lookup_fmt2(ntok, rpw, argmax, split);
         case 3: return kernel_lookup_fmt3(ntok, rpw, argmax, split);
+        case 4: return kernel_lookup_fmt4(ntok, rpw, argmax, split);
         default: return nullptr;
     }
 }

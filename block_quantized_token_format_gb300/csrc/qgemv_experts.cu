@@ -19,7 +19,7 @@ const void* expert_kernel_lookup(int fmt, int rpw) {
         if (rpw == 4) return (const void*)&qgemv_experts_kernel<F, 4>;     \
         return nullptr;                                                    \
     }
-    QG_X(QG_Q8_0) QG_X(QG_Q4_0) QG_X(QG_AFFINE4_G64) QG_X(QG_BF16)
+    QG_X(QG_Q8_0) QG_X(QG_Q4_0) QG_X(QG_AFFINE4_G64) QG_X(QG_BF16) QG_X(QG_Q5_0)
 #undef QG_X
     return nullptr;
 }
@@ -32,7 +32,7 @@ const void* expert_layer_kernel_lookup(int fmt, int rpw) {
         if (rpw == 4) return (const void*)&qgemv_expert_layer_kernel<F, 4>;    \
         return nullptr;                                                        \
     }
-    QG_L(QG_Q8_0) QG_L(QG_Q4_0) QG_L(QG_AFFINE4_G64) QG_L(QG_BF16)
+    QG_L(QG_Q8_0) QG_L(QG_Q4_0) QG_L(QG_AFFINE4_G64) QG_L(QG_BF16) QG_L(QG_Q5_0)
 #undef QG_L
     return nullptr;
 }

@@ -1,10 +1,10 @@
 // Instantiations of the dequant-GEMV kernel for one weight format, selected at
 // compile time by QG_INST_FMT (the build compiles this file once per format so
-// the four formats build in parallel).
+// the formats build in parallel).
 #include "qgemv_kernels.cuh"
 
 #ifndef QG_INST_FMT
-#error "compile with -DQG_INST_FMT=<0..3>"
+#error "compile with -DQG_INST_FMT=<0..4>"
 #endif
 
 #define QG_CAT2(a, b) a##b

@@ -279,6 +279,30 @@ template <> struct Fmt<QG_BF16> {
     }
 };
 
+// Q5_0: the Q4_0 nibbles plus a fifth bit per element.  A chunk's scale record (6
+// bytes at 6j after the step's codes) holds its fifth bits (uint32, bit c = column c)
+// and then its fp16 d.  The fifth bit of column 4i + m goes to bit 4m + 4 of the
+// magic float, above its nibble: (2^23 + q*16^m) - (2^23 + 16*16^m) = (q - 16) * 16^m.
+template <> struct Fmt<QG_Q5_0> {
+    static constexpr int kW = 32;
+    static constexpr int kStepScale = 192;
+    static __device__ __forceinline__ uint32_t scale_off(int j) { return 6u * uint32_t(j); }
+    static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds16(a + 4); }
+    static __device__ __forceinline__ uint32_t high(uint32_t a) { return lds16(a) | (lds16(a + 2) << 16); }
+    static __device__ __forceinline__ void dec5(const uint4& q, uint32_t qh, int i, f2_t& lo, f2_t& hi,
+                                                uint32_t mg) {
+        const uint32_t w = (i >> 1) == 0 ? q.x : (i >> 1) == 1 ? q.y : (i >> 1) == 2 ? q.z : q.w;
+        const uint32_t h = (i & 1) ? (w >> 16) : w;
+        const uint32_t hq = qh >> (4 * i);
+        const uint32_t b0 = nib<0x000Fu>(h, mg) | ((hq << 4) & 0x10u);
+        const uint32_t b1 = nib<0x00F0u>(h, mg) | ((hq << 7) & 0x100u);
+        const uint32_t b2 = nib<0x0F00u>(h, mg) | ((hq << 10) & 0x1000u);
+        const uint32_t b3 = nib<0xF000u>(h, mg) | ((hq << 13) & 0x10000u);
+        lo = f2_add(f2_pack(b0, b1), f2_pack(__float_as_uint(-8388624.0f), __float_as_uint(-8388864.0f)));
+        hi = f2_add(f2_pack(b2, b3), f2_pack(__float_as_uint(-8392704.0f), __float_as_uint(-8454144.0f)));
+    }
+};
+
 // ------------------------------------------------------------------------------ helpers
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
@@ -305,7 +329,7 @@ struct SmemPlan {
 // One ring stage: RPW rows of one full step, rounded up to 128 bytes (tensor
 // copies land on 128-byte boundaries).
 __host__ __device__ constexpr int full_step(int fmt) {
-    return int(kStepCodeBytes) + (fmt == QG_Q8_0 ? 32 : fmt == QG_BF16 ? 0 : 64);
+    return int(kStepCodeBytes) + (fmt == QG_Q8_0 ? 32 : fmt == QG_BF16 ? 0 : fmt == QG_Q5_0 ? 192 : 64);
 }
 __host__ __device__ constexpr int stage_bytes(int fmt, int rpw) { return (rpw * full_step(fmt) + 127) / 128 * 128; }
 
@@ -372,7 +396,7 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
                 for (int t = 0; t < NTOK; ++t) {
                     if (t >= live) break;
                     float4 w = v[j][t];
-                    if constexpr (FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64) {
+                    if constexpr (FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64 || FMT == QG_Q5_0) {
                         // column j is used as q*16^(j%4): store x * 16^-(j%4) (exact)
                         w.y *= 0.0625f;
                         w.z *= 0.00390625f;
@@ -447,10 +471,12 @@ __device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
     constexpr bool kPairAcc = Acc<FMT, NTOK, RPW>::kPair;
     uint4 qv[RPW];
     uint32_t sv[RPW];
+    uint32_t hv[FMT == QG_Q5_0 ? RPW : 1];         // Q5_0: the chunk's fifth bits
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         qv[r] = lds128(codes + r * kFullStep);
         sv[r] = F::scale(scales + r * kFullStep);
+        if constexpr (FMT == QG_Q5_0) hv[r] = F::high(scales + r * kFullStep);
     }
     f2_t p[kPairAcc ? 1 : RPW][kPairAcc ? 1 : NTOK];
 #pragma unroll
@@ -465,7 +491,8 @@ __device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             f2_t wlo, whi;
-            F::dec(qv[r], i, wlo, whi, magic);
+            if constexpr (FMT == QG_Q5_0) F::dec5(qv[r], hv[r], i, wlo, whi, magic);
+            else F::dec(qv[r], i, wlo, whi, magic);
 #pragma unroll
             for (int t = 0; t < NTOK; ++t) {
                 f2_t& pp = [&]() -> f2_t& {
@@ -476,7 +503,7 @@ __device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
             }
         }
     }
-    if constexpr (FMT == QG_Q8_0 || FMT == QG_Q4_0) {
+    if constexpr (FMT == QG_Q8_0 || FMT == QG_Q4_0 || FMT == QG_Q5_0) {
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             const float d = h2f(sv[r]);
@@ -537,7 +564,7 @@ __device__ __forceinline__ float warp_reduce(const Acc<FMT, NTOK, RPW>& A, int l
 // thread may hold up to 168 registers instead of 128 and the extra rows'
 // accumulators do not spill.  Kernels that fit in 128 keep 16 warps.
 template <int FMT, int NTOK, int RPW> struct MaxThreads {
-    static constexpr bool kFourBit = FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64;
+    static constexpr bool kFourBit = FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64 || FMT == QG_Q5_0;
     static constexpr int value = (RPW * NTOK > 20 || (kFourBit && RPW * NTOK >= 16 && NTOK >= 2)) ? 384 : 512;
 };
 

@@ -82,8 +82,11 @@ const Entry kTable[] = {
 }  // namespace
 
 Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
+    // Q5_0 streams Q4_0's code layout plus 6 bytes per block and decodes the same way
+    // (one more bit per element): it takes Q4_0's entries (not measured separately).
+    const int key = fmt == QG_Q5_0 ? int(QG_Q4_0) : fmt;
     for (const Entry& e : kTable) {
-        if (e.fmt != fmt) continue;
+        if (e.fmt != key) continue;
         if (n_out < e.n_out_min || n_out > e.n_out_max) continue;
         if (e.n_in && e.n_in != n_in) continue;
         if (e.ntok && e.ntok != ntok) continue;

@@ -34,12 +34,14 @@
 extern "C" {
 #endif
 
-/* Weight formats.  Byte counts per 32 weights: Q8_0 34, Q4_0 18, AFFINE4_G64 18, BF16 64. */
+/* Weight formats.  Byte counts per 32 weights: Q8_0 34, Q4_0 18, AFFINE4_G64 18, BF16 64,
+ * Q5_0 22. */
 typedef enum {
     QG_Q8_0 = 0,        /* 32-weight blocks: fp16 d + 32 int8 q; w = q*d                         */
     QG_Q4_0 = 1,        /* 32-weight blocks: fp16 d + 16 B of nibbles; w = (q-8)*d                */
     QG_AFFINE4_G64 = 2, /* 64-weight groups: 4-bit q, fp16 scale s, fp16 bias b; w = q*s + b      */
-    QG_BF16 = 3         /* plain bf16                                                             */
+    QG_BF16 = 3,        /* plain bf16                                                             */
+    QG_Q5_0 = 4         /* 32-weight blocks: fp16 d + 32 fifth bits + 16 B of nibbles; w = (q-16)*d */
 } qg_fmt;
 
 typedef int qg_status;
@@ -66,6 +68,8 @@ int qg_abi_version(void);
  *          (element k of a word at bits [4k,4k+4)), fp16 scales [n_out][n_in/64],
  *          fp16 biases [n_out][n_in/64].
  *   BF16:  bf16 [n_out][n_in].
+ *   Q5_0:  per 32-block: fp16 d, a little-endian uint32 whose bit j is bit 4 of
+ *          element j's code, then the 16 bytes of low nibbles in the Q4_0 order.
  * Device layout: what qgemv reads.  Rows are stored one after the other, so
  * the first k rows of a packed matrix are themselves a packed k-row matrix (a
  * reduced draft vocabulary that is a prefix of the head needs no copy).  A row
@@ -74,10 +78,11 @@ int qg_abi_version(void);
  * of a row can be shorter).  No padding at all when the codes of a row are a
  * multiple of 512 bytes (n_in a multiple of 512 for Q8_0, 1024 for the 4-bit
  * formats, 256 for BF16), so then qg_packed_bytes == qg_canonical_bytes.
- *   codes:  Q8_0 q+128 (uint8); Q4_0 and AFFINE4_G64 uint32 words of 8
- *           consecutive elements (element k at bits [4k,4k+4)); BF16 raw.
+ *   codes:  Q8_0 q+128 (uint8); Q4_0, Q5_0 (low nibbles) and AFFINE4_G64 uint32
+ *           words of 8 consecutive elements (element k at bits [4k,4k+4)); BF16 raw.
  *   scales: Q8_0 / Q4_0 one fp16 d per 32 weights; AFFINE4_G64 one (fp16 s,
- *           fp16 b) pair per 64 weights.
+ *           fp16 b) pair per 64 weights; Q5_0 one (uint32 fifth bits, fp16 d)
+ *           record of 6 bytes per 32 weights.
  * Sizes return 0 for invalid arguments. */
 size_t  qg_canonical_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);
 size_t  qg_packed_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);
@@ -85,8 +90,8 @@ int64_t qg_row_stride(qg_fmt fmt, int64_t n_in);     /* device-layout bytes per 
 
 /* --------------------------------------------------------------------- host packer
  * All three work on host memory, use several CPU threads, and return QG_EINVAL on
- * a null pointer, n_out < 1, or n_in not a multiple of the block (32 for Q8_0
- * and Q4_0; 64 for AFFINE4_G64; 16 for BF16, the kernels' 16-weight chunk).
+ * a null pointer, n_out < 1, or n_in not a multiple of the block (32 for Q8_0,
+ * Q4_0 and Q5_0; 64 for AFFINE4_G64; 16 for BF16, the kernels' 16-weight chunk).
  *
  * qg_quantize: fp32 W [n_out][n_in] -> canonical bytes (qg_canonical_bytes).
  *   Q8_0: d = max|w|/127 (fp32), stored fp16 (nearest even); q = roundf(w/d) with
@@ -96,6 +101,8 @@ int64_t qg_row_stride(qg_fmt fmt, int64_t n_in);     /* device-layout bytes per 
  *   AFFINE4_G64: s = fp16((max-min)/15), b = fp16(min); q = clamp(roundf((w-b)/s),
  *         0, 15) in fp32 with the fp16 s and b; q = 0 when s == 0.
  *   BF16: round to nearest even.
+ *   Q5_0: as Q4_0 with 5-bit codes: d = m/-16 (fp32), stored fp16;
+ *         q = clamp(roundf(w/d)+16, 0, 31); d = 0, q = 16 when m == 0.
  * qg_to_device_layout: canonical bytes -> device layout (qg_packed_bytes).
  * qg_pack: fp32 W -> device layout directly (same bytes as the two steps). */
 qg_status qg_quantize(qg_fmt fmt, const float* W_host, int64_t n_out, int64_t n_in,

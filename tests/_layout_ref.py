@@ -4,9 +4,10 @@ bytes back to fp64 weights so tests can check the packer's device layout.
 
 Device layout: rows one after the other; a row is a run of steps, each step
 512 bytes of codes followed by the scales of those codes, padded to 16 bytes.
-Codes: Q8_0 q+128; Q4_0 / affine uint32 words of 8 consecutive elements
-(element k at bits 4k); BF16 raw.  Scales: Q8_0 / Q4_0 fp16 d per 32 weights;
-affine (fp16 s, fp16 b) per 64 weights.
+Codes: Q8_0 q+128; Q4_0 / Q5_0 (low nibbles) / affine uint32 words of 8
+consecutive elements (element k at bits 4k); BF16 raw.  Scales: Q8_0 / Q4_0 fp16 d
+per 32 weights; affine (fp16 s, fp16 b) per 64 weights; Q5_0 (uint32 fifth bits,
+fp16 d) per 32 weights.
 """
 from __future__ import annotations
 
@@ -16,11 +17,12 @@ STEP = 512
 
 
 def codes_bytes(fmt, n_in):
-    return {"q8_0": n_in, "q4_0": n_in // 2, "affine4_g64": n_in // 2, "bf16": 2 * n_in}[fmt]
+    return {"q8_0": n_in, "q4_0": n_in // 2, "affine4_g64": n_in // 2, "bf16": 2 * n_in, "q5_0": n_in // 2}[fmt]
 
 
 def scale_bytes_for(fmt, codes):
-    return {"q8_0": codes // 16, "q4_0": codes // 8, "affine4_g64": codes // 8, "bf16": 0}[fmt]
+    return {"q8_0": codes // 16, "q4_0": codes // 8, "affine4_g64": codes // 8, "bf16": 0,
+            "q5_0": codes // 16 * 6}[fmt]
 
 
 def r16(b):
@@ -59,9 +61,17 @@ def decode_device(fmt: str, packed: np.ndarray, n_out: int, n_in: int) -> np.nda
             q = codes.astype(np.int64) - 128
             d = scales.copy().view("<f2").astype(np.float64)
             out[r] = (q.reshape(-1, 32) * d[:, None]).reshape(-1)
-        elif fmt in ("q4_0", "affine4_g64"):
+        elif fmt in ("q4_0", "affine4_g64", "q5_0"):
             words = codes.copy().view("<u4")
             q = np.stack([(words >> np.uint32(4 * k)) & np.uint32(15) for k in range(8)], axis=1).reshape(-1)
+            if fmt == "q5_0":
+                rec = scales.reshape(-1, 6)
+                qh = rec[:, :4].copy().view("<u4").reshape(-1)
+                d = rec[:, 4:].copy().view("<f2").astype(np.float64).reshape(-1)
+                hb = (qh[:, None] >> np.arange(32, dtype=np.uint32)) & np.uint32(1)
+                q5 = (q.reshape(-1, 32) | (hb << np.uint32(4))).astype(np.float64)
+                out[r] = ((q5 - 16) * d[:, None]).reshape(-1)
+                continue
             q = q.astype(np.float64)
             if fmt == "q4_0":
                 d = scales.copy().view("<f2").astype(np.float64)

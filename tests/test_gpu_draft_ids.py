@@ -25,7 +25,7 @@ import block_quantized_token_format_gb300 as qg  # noqa: E402
 
 GAP = 1e-4
 TOL = 1e-3
-FMTS = ["q8_0", "q4_0", "affine4_g64", "bf16"]
+FMTS = ["q8_0", "q4_0", "affine4_g64", "bf16", "q5_0"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,7 +40,7 @@ def dev():
 
 
 def n_in_for(fmt, base):
-    m = {"q8_0": 32, "q4_0": 32, "affine4_g64": 64, "bf16": 16}[fmt]
+    m = {"q8_0": 32, "q4_0": 32, "affine4_g64": 64, "bf16": 16, "q5_0": 32}[fmt]
     return max(m, base // m * m)
 
 

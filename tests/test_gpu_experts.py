@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 import block_quantized_token_format_gb300 as qg  # noqa: E402
 
 TOL = 1e-3
-FMTS = ["q8_0", "q4_0", "affine4_g64", "bf16"]
+FMTS = ["q8_0", "q4_0", "affine4_g64", "bf16", "q5_0"]
 
 
 @pytest.fixture(autouse=True)
@@ -44,7 +44,7 @@ def dev():
 
 
 def n_in_for(fmt, base):
-    m = {"q8_0": 32, "q4_0": 32, "affine4_g64": 64, "bf16": 16}[fmt]
+    m = {"q8_0": 32, "q4_0": 32, "affine4_g64": 64, "bf16": 16, "q5_0": 32}[fmt]
     return max(m, base // m * m)
 
 

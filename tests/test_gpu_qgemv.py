@@ -18,7 +18,7 @@ pytestmark = pytest.mark.gpu
 import block_quantized_token_format_gb300 as qg  # noqa: E402
 
 TOL = 1e-3
-FMTS = ["q8_0", "q4_0", "affine4_g64", "bf16"]
+FMTS = ["q8_0", "q4_0", "affine4_g64", "bf16", "q5_0"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,7 +59,7 @@ def check_close(y, ref, den, what=""):
 
 
 def n_in_for(fmt, base):
-    m = {"q8_0": 32, "q4_0": 32, "affine4_g64": 64, "bf16": 16}[fmt]
+    m = {"q8_0": 32, "q4_0": 32, "affine4_g64": 64, "bf16": 16, "q5_0": 32}[fmt]
     return max(m, base // m * m)
 
 
@@ -85,7 +85,7 @@ def test_small_shapes(fmt, n_out, n_in_base):
 # ----------------------------------------------------------------------------- workload shapes, full oracle
 
 SMALL_WORKLOADS = ["q8_0_2560x2560", "q8_0_6144x2560", "q8_0_10240x2560", "q8_0_12288x2560",
-                   "q8_0_2560x6144", "q4_0_8192x2560", "bf16_8192x2560"]
+                   "q8_0_2560x6144", "q4_0_8192x2560", "bf16_8192x2560", "q5_0_8192x2560"]
 
 
 @pytest.mark.parametrize("name", SMALL_WORKLOADS)

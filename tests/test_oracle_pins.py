@@ -277,7 +277,7 @@ def check_linearity(orc):
     rng = np.random.Generator(np.random.PCG64(9))
     x1 = (rng.integers(-16384, 16384, (2, n_in)) / 4096.0).astype(np.float32)
     x2 = (rng.integers(-16384, 16384, (2, n_in)) / 4096.0).astype(np.float32)
-    for fmt in ("q8_0", "q4_0", "affine4_g64", "bf16"):
+    for fmt in ("q8_0", "q4_0", "affine4_g64", "bf16", "q5_0"):
         raw = orc.quantize(fmt, workloads.gaussian(11, (n_out, n_in), 0.02))
         y1 = orc.gemv(fmt, raw, n_out, n_in, x1)
         y2 = orc.gemv(fmt, raw, n_out, n_in, x2)
@@ -288,7 +288,7 @@ def check_linearity(orc):
 
 def check_token_independence(orc):
     n_out, n_in = 33, 512
-    for fmt in ("q8_0", "q4_0", "affine4_g64", "bf16"):
+    for fmt in ("q8_0", "q4_0", "affine4_g64", "bf16", "q5_0"):
         raw = orc.quantize(fmt, workloads.gaussian(21, (n_out, n_in), 0.02))
         x4 = workloads.activations(21, n_in, 4)
         y4 = orc.gemv(fmt, raw, n_out, n_in, x4)
@@ -321,6 +321,17 @@ def check_cross_format(orc):
     assert np.array_equal(orc.dequantize("q4_0", r4, n_out, n_in), W.astype(np.float64))
     assert np.array_equal(orc.dequantize("affine4_g64", ra, n_out, n_in), W.astype(np.float64))
     assert np.array_equal(orc.gemv("q4_0", r4, n_out, n_in, x), orc.gemv("affine4_g64", ra, n_out, n_in, x))
+    # Q4_0 code q with scale d equals Q5_0 code q + 8 with the same d: rebuild every Q4_0
+    # block as a Q5_0 block by hand (fifth bit = bit 4 of q + 8) and compare.
+    blocks = r4.reshape(-1, 18)
+    q5 = bytearray()
+    for blk in blocks:
+        lo = [int(b) & 15 for b in blk[2:]] + [int(b) >> 4 for b in blk[2:]]      # elements 0..31
+        c = [v + 8 for v in lo]
+        qh = sum(((v >> 4) & 1) << j for j, v in enumerate(c))
+        q5 += bytes(blk[:2]) + struct.pack("<I", qh) + bytes((c[j] & 15) | ((c[j + 16] & 15) << 4) for j in range(16))
+    r5 = np.frombuffer(bytes(q5), dtype=np.uint8)
+    assert np.array_equal(orc.dequantize("q5_0", r5, n_out, n_in), orc.dequantize("q4_0", r4, n_out, n_in))
 
 
 def check_argmax(orc):

@@ -11,7 +11,7 @@ import workloads
 import block_quantized_token_format_gb300 as qg
 from _layout_ref import decode_device
 
-FMTS = ["q8_0", "q4_0", "affine4_g64", "bf16"]
+FMTS = ["q8_0", "q4_0", "affine4_g64", "bf16", "q5_0"]
 
 
 def _special(n_out, n_in, seed):

@@ -48,6 +48,8 @@ WORKLOADS: dict[str, Workload] = {w.name: w for w in [
     # config 2: the 8192x2560 format comparison, Q4_0 and BF16 from the same fp32 W.
     Workload("q4_0_8192x2560", "q4_0", 8192, 2560, 120),
     Workload("bf16_8192x2560", "bf16", 8192, 2560, 120),
+    # Q5_0 (the Track 1 report's 5-bit draft format) on the same 8192x2560 matrix.
+    Workload("q5_0_8192x2560", "q5_0", 8192, 2560, 120),
     # config 3: Q8_0 LM head with fused argmax; the drafted-vocab variant is a row prefix.
     Workload("q8_0_head_248320x2560", "q8_0", 248320, 2560, 130, argmax=True),
     Workload("q8_0_head_106299x2560", "q8_0", 106299, 2560, 130, argmax=True,
