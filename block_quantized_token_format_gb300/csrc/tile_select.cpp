@@ -72,6 +72,9 @@ const Entry kTable[] = {
     {QG_BF16, 4096, 65535, 2560, 2, {4, 5, 8, 2}},
     {QG_BF16, 4096, 65535, 2560, 3, {4, 3, 16, 1}},
     {QG_BF16, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
+    // Q5_0, 8192 x 2560 (measured; ntok 2 and 4 fall through to Q4_0's entries)
+    {QG_Q5_0, 4096, 65535, 2560, 1, {2, 3, 16, 1}},
+    {QG_Q5_0, 4096, 65535, 2560, 3, {2, 3, 16, 1}},
     // affine 4-bit LM head
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {8, 2, 16, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {8, 2, 12, 1}},
@@ -82,16 +85,16 @@ const Entry kTable[] = {
 }  // namespace
 
 Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
-    // Q5_0 streams Q4_0's code layout plus 6 bytes per block and decodes the same way
-    // (one more bit per element): it takes Q4_0's entries (not measured separately).
-    const int key = fmt == QG_Q5_0 ? int(QG_Q4_0) : fmt;
     for (const Entry& e : kTable) {
-        if (e.fmt != key) continue;
+        if (e.fmt != fmt) continue;
         if (n_out < e.n_out_min || n_out > e.n_out_max) continue;
         if (e.n_in && e.n_in != n_in) continue;
         if (e.ntok && e.ntok != ntok) continue;
         return e.tile;
     }
+    // Q5_0 streams Q4_0's code layout plus 6 bytes per block and decodes the same way
+    // (one more bit per element): where it has no entry of its own it takes Q4_0's.
+    if (fmt == QG_Q5_0) return select_tile(QG_Q4_0, n_out, n_in, ntok);
     // Heuristic for unmeasured shapes: many rows stream 4 per warp (8 at ntok 1) in
     // one 12- or 16-warp CTA per SM with a shallow ring; few rows use 2 rows per warp
     // so that the row groups still spread over every SM.
