@@ -86,7 +86,7 @@ class ExpertLayer:
 # top-10 routing, 65% inter-token share; stored here in Q8_0.
 EXPERT_LAYERS: dict[str, ExpertLayer] = {e.name: e for e in [
     ExpertLayer("q8_0_experts_512x2560x640_top10", "q8_0", 512, 2560, 640, 10, 0.65, 150),
-    # The M2 Max page's routing dumps: consecutive tokens never shared an expert.
+    # The M2 Max page's routing dumps: no two consecutive tokens picked a common expert.
     ExpertLayer("q8_0_experts_512x2560x640_top10_share0", "q8_0", 512, 2560, 640, 10, 0.0, 150),
 ]}
 
