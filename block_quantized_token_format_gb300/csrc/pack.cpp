@@ -154,6 +154,16 @@ void quant_row_bf16(const float* w, int64_t n_in, uint8_t* out) {
 // Canonical row pointers (affine has three planes).
 struct CanonRow { const uint8_t* a; const uint8_t* s; const uint8_t* b; };
 
+// Q5_0 device record: the fifth bit of element e = 4i + m of a block (i = 0..7, m =
+// 0..3) sits at bit (4m + 4 + r_i) mod 32 of the record's word, r_i = i for i < 4 and
+// i + 12 for i >= 4.  Rotating the word right by r_i then puts the fifth bits of
+// elements 4i..4i+3 at bits 4, 8, 12, 16, one place above each element's nibble as
+// the decoder lays them out; the 32 positions are distinct.
+int q5_fifth_bit_pos(int e) {
+    const int i = e >> 2, m = e & 3;
+    return (4 * m + 4 + (i < 4 ? i : i + 12)) & 31;
+}
+
 // The row's codes (device byte / nibble order) followed by all its scales.
 void flat_device_row(int fmt, CanonRow c, int64_t n_in, uint8_t* dst) {
     const int64_t cb = qg::codes_bytes(fmt, n_in);
@@ -190,10 +200,14 @@ void flat_device_row(int fmt, CanonRow c, int64_t n_in, uint8_t* dst) {
             break;
         case QG_Q5_0:
             // codes: the low nibbles as Q4_0's words; scales: per block its fifth bits
-            // (uint32, bit j = element j) and then its fp16 d, 6 bytes.
+            // (a uint32 in the rotated order of q5_fifth_bit_pos) and then its fp16 d, 6 bytes.
             for (int64_t b = 0; b < n_in / 32; ++b) {
                 const uint8_t* blk = c.a + 22 * b;
-                std::memcpy(dst + cb + 6 * b, blk + 2, 4);
+                const uint32_t qh = uint32_t(blk[2]) | uint32_t(blk[3]) << 8 | uint32_t(blk[4]) << 16 |
+                                    uint32_t(blk[5]) << 24;
+                uint32_t rot = 0;
+                for (int e = 0; e < 32; ++e) rot |= ((qh >> e) & 1u) << q5_fifth_bit_pos(e);
+                put32(dst + cb + 6 * b, rot);
                 std::memcpy(dst + cb + 6 * b + 4, blk, 2);
                 uint8_t q[32];
                 for (int j = 0; j < 16; ++j) { q[j] = blk[6 + j] & 0xF; q[j + 16] = blk[6 + j] >> 4; }

@@ -280,24 +280,33 @@ template <> struct Fmt<QG_BF16> {
 };
 
 // Q5_0: the Q4_0 nibbles plus a fifth bit per element.  A chunk's scale record (6
-// bytes at 6j after the step's codes) holds its fifth bits (uint32, bit c = column c)
-// and then its fp16 d.  The fifth bit of column 4i + m goes to bit 4m + 4 of the
-// magic float, above its nibble: (2^23 + q*16^m) - (2^23 + 16*16^m) = (q - 16) * 16^m.
+// bytes at 6j after the step's codes) holds its fifth bits (uint32) and then its fp16
+// d.  The packer stores the fifth bit of column 4i + m at bit (4m + 4 + r_i) mod 32,
+// r_i = i (i < 4) or i + 12 (i >= 4), so one funnel rotation by r_i puts the fifth
+// bits of columns 4i..4i+3 at bits 4, 8, 12 and 16: bit 4m + 4 of the magic float,
+// just above nibble m, and one LOP3 per column merges it:
+// (2^23 + q*16^m) - (2^23 + 16*16^m) = (q - 16) * 16^m.
 template <> struct Fmt<QG_Q5_0> {
     static constexpr int kW = 32;
     static constexpr int kStepScale = 192;
     static __device__ __forceinline__ uint32_t scale_off(int j) { return 6u * uint32_t(j); }
     static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds16(a + 4); }
     static __device__ __forceinline__ uint32_t high(uint32_t a) { return lds16(a) | (lds16(a + 2) << 16); }
+    template <uint32_t BIT>
+    static __device__ __forceinline__ uint32_t merge(uint32_t rot, uint32_t nibble) {
+        uint32_t d;
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(rot), "n"(BIT), "r"(nibble));   // (rot & BIT) | nibble
+        return d;
+    }
     static __device__ __forceinline__ void dec5(const uint4& q, uint32_t qh, int i, f2_t& lo, f2_t& hi,
                                                 uint32_t mg) {
         const uint32_t w = (i >> 1) == 0 ? q.x : (i >> 1) == 1 ? q.y : (i >> 1) == 2 ? q.z : q.w;
         const uint32_t h = (i & 1) ? (w >> 16) : w;
-        const uint32_t hq = qh >> (4 * i);
-        const uint32_t b0 = nib<0x000Fu>(h, mg) | ((hq << 4) & 0x10u);
-        const uint32_t b1 = nib<0x00F0u>(h, mg) | ((hq << 7) & 0x100u);
-        const uint32_t b2 = nib<0x0F00u>(h, mg) | ((hq << 10) & 0x1000u);
-        const uint32_t b3 = nib<0xF000u>(h, mg) | ((hq << 13) & 0x10000u);
+        const uint32_t rot = i == 0 ? qh : __funnelshift_r(qh, qh, i < 4 ? i : i + 12);
+        const uint32_t b0 = merge<0x10u>(rot, nib<0x000Fu>(h, mg));
+        const uint32_t b1 = merge<0x100u>(rot, nib<0x00F0u>(h, mg));
+        const uint32_t b2 = merge<0x1000u>(rot, nib<0x0F00u>(h, mg));
+        const uint32_t b3 = merge<0x10000u>(rot, nib<0xF000u>(h, mg));
         lo = f2_add(f2_pack(b0, b1), f2_pack(__float_as_uint(-8388624.0f), __float_as_uint(-8388864.0f)));
         hi = f2_add(f2_pack(b2, b3), f2_pack(__float_as_uint(-8392704.0f), __float_as_uint(-8454144.0f)));
     }

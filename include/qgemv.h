@@ -82,7 +82,10 @@ int qg_abi_version(void);
  *           words of 8 consecutive elements (element k at bits [4k,4k+4)); BF16 raw.
  *   scales: Q8_0 / Q4_0 one fp16 d per 32 weights; AFFINE4_G64 one (fp16 s,
  *           fp16 b) pair per 64 weights; Q5_0 one (uint32 fifth bits, fp16 d)
- *           record of 6 bytes per 32 weights.
+ *           record of 6 bytes per 32 weights, the fifth bit of block element
+ *           e = 4i + m (m < 4) at bit (4m + 4 + r) mod 32 of the uint32, r = i for
+ *           i < 4 and i + 12 otherwise (rotating the word right by r lines up the
+ *           fifth bits of elements 4i..4i+3 one place above their nibbles).
  * Sizes return 0 for invalid arguments. */
 size_t  qg_canonical_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);
 size_t  qg_packed_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);

@@ -68,7 +68,10 @@ def decode_device(fmt: str, packed: np.ndarray, n_out: int, n_in: int) -> np.nda
                 rec = scales.reshape(-1, 6)
                 qh = rec[:, :4].copy().view("<u4").reshape(-1)
                 d = rec[:, 4:].copy().view("<f2").astype(np.float64).reshape(-1)
-                hb = (qh[:, None] >> np.arange(32, dtype=np.uint32)) & np.uint32(1)
+                # fifth bit of element e = 4i + m at bit (4m + 4 + r_i) mod 32, r_i = i or i + 12
+                e = np.arange(32)
+                pos = (4 * (e & 3) + 4 + np.where(e >> 2 < 4, e >> 2, (e >> 2) + 12)) % 32
+                hb = (qh[:, None] >> pos.astype(np.uint32)) & np.uint32(1)
                 q5 = (q.reshape(-1, 32) | (hb << np.uint32(4))).astype(np.float64)
                 out[r] = ((q5 - 16) * d[:, None]).reshape(-1)
                 continue
