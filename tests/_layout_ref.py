@@ -7,7 +7,8 @@ Device layout: rows one after the other; a row is a run of steps, each step
 Codes: Q8_0 q+128; Q4_0 / Q5_0 (low nibbles) / affine uint32 words of 8
 consecutive elements (element k at bits 4k); BF16 raw.  Scales: Q8_0 / Q4_0 fp16 d
 per 32 weights; affine (fp16 s, fp16 b) per 64 weights; Q5_0 (uint32 fifth bits,
-fp16 d) per 32 weights.
+fp16 d) per 32 weights, the fifth bit of element 4i + m at bit (4m + 4 + r_i) mod 32
+with r_i = i (i < 4) or i + 12 (i >= 4).
 """
 from __future__ import annotations
 
