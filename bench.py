@@ -1,19 +1,24 @@
 #!/usr/bin/env python
 """Benchmark: effective weight GB/s of the block-quantized mat-vec (qgemv) on GB300.
 
-One step = one pass of the Q8_0 dense projection set (n_in -> n_out: 2560->6144,
-2560->10240, 2560->12288, 6144->2560) at ntok = 1, 2, 3 and 4: 16 kernel launches
-over 379 MB of distinct weights.  value = weight bytes / time (scales included,
-1e9 B per GB).  The steps are replayed from CUDA graphs of 10 steps (160
-launches; the kernels are 3-12 us long, launching them one by one from Python
-would time the host).  Also reported, outside the timed region:
+One step = the two vocabulary-sized LM heads through the fused argmax call
+(qgemv_argmax) at ntok = 1, 2, 3 and 4: the Q8_0 head 248320x2560 (675.4 MB) and
+the affine 4-bit g64 drafter head 248320x5120 (715.2 MB), 8 launches and 5.56 GB
+of weight reads per step, logits and argmax written.  value = weight bytes / time
+(scales and biases included, 1e9 B per GB).  The step is one CUDA graph (early
+start between launches); the timed region is a block of exactly K steps, and
+blocks are repeated until at least 1 s has been timed, so the clock record
+covers a real interval.  Also reported, outside the timed region:
 
-* per_workload: every workload family x ntok (including the fused LM-head
-  argmax heads), median of 5 graph replays of 50 launches rotating over weight
-  copies totalling >= 4x L2;
+* config.per_config: every (head, ntok) launch alone and the 2560->12288
+  projection (the largest shapes), with GB/s, the fraction of the measured copy
+  peak and, for the 4-bit head, the fraction of the FP32 FMA pipe's peak;
+* per_workload: every other workload family x ntok, median of 5 graph replays of
+  50 launches rotating over weight copies totalling >= 4x L2;
 * e2e: the same step through the public API with host buffers, per call
-  (pinned x uploaded, y read back, host synchronized every step, no graph);
-* roofline of the dominant kernel, cpu_baseline (the fp64 oracle on the host).
+  (pinned x uploaded, logits and argmax read back, host synchronized every step);
+* roofline of the dominant kernel, cpu_baseline (the fp64 oracle on the host's
+  cores, one thread and all of them).
 
 --impl reference times the CPU oracle instead (the only reference there is).
 """
@@ -39,26 +44,39 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 METRIC = "effective weight GB/s and % of GB300 HBM peak, qgemv at ntok=1..4"
-WORKLOAD_NAME = ("Q8_0 dense projection set (n_in->n_out 2560->6144, 2560->10240, "
-                 "2560->12288, 6144->2560) at ntok=1,2,3,4")
+HEADS = ["q8_0_head_248320x2560", "affine4_head_248320x5120"]
+WORKLOAD_NAME = ("LM-head qgemv_argmax: Q8_0 248320x2560 and affine4-g64 248320x5120, "
+                 "each at ntok=1,2,3,4 (8 launches, 5.56 GB of weights per step)")
+LARGEST = HEADS + ["q8_0_12288x2560"]      # the shapes the >= 70% / >= 60% target is stated on
 NTOKS = (1, 2, 3, 4)
 PEAK_FALLBACK_GBS = 6800.0
+MIN_TIMED_S = 1.0                          # timed blocks of K steps are repeated up to this
+FMA_LANES_PER_CLK_SM = 128                 # FP32 FMA pipe, lane-ops per clock per SM (GB300)
 
 
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20000)
-    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-detail", action="store_true", help="skip the per-workload table")
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     p.add_argument("--detail-only", default="", help="comma list of workload names for the table")
     p.add_argument("--one-experts", default="", help="ntok: five routed-expert layers on a 64-expert stack "
                    "(the small case an ncu capture profiles)")
     p.add_argument("--one-layer", default="", help="ntok: as --one-experts, with the layer as one launch")
     p.add_argument("--one", default="", help="fmt,n_out,n_in,ntok[,tile spec]: run one shape 3 times "
                                              "(a small case for ncu) and exit")
+    p.add_argument("--one-argmax", default="", help="as --one, through qgemv_argmax (the LM-head call)")
+    p.add_argument("--sweep", default="", help="comma list of workload names: time every tile spec of "
+                   "--sweep-specs (';'-separated, qg_set_tile_override grammar; default a grid) at "
+                   "--sweep-ntoks, one JSON line per point to --sweep-out, the best per (workload, ntok) "
+                   "to stdout")
+    p.add_argument("--sweep-specs", default="")
+    p.add_argument("--sweep-ntoks", default="1,2,3,4")
+    p.add_argument("--sweep-out", default="tile_sweep.jsonl")
     p.add_argument("--cpu-worker", default="", help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -104,6 +122,13 @@ def job_gbs(step_bytes: int, steps: int, world: int, max_ms: float) -> float:
     return step_bytes * steps * world / (max_ms * 1e-3) / 1e9
 
 
+def timed_blocks(block_s_estimate: float, min_total_s: float = MIN_TIMED_S, min_blocks: int = 3) -> int:
+    """How many blocks of K steps to time so that at least min_total_s is timed."""
+    if block_s_estimate <= 0:
+        return min_blocks
+    return max(min_blocks, int(math.ceil(min_total_s / block_s_estimate)))
+
+
 def algo_bytes(fmt, n_out, n_in, ntok, argmax=False):
     b = workloads_bytes(fmt, n_out, n_in) + 4 * ntok * (n_in + n_out)
     return b + (4 * ntok if argmax else 0)
@@ -142,9 +167,6 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
-
-    def mark(self):
-        return time.time()
 
     def __exit__(self, *exc):
         if self.proc:
@@ -194,25 +216,53 @@ def gen_packed(qg, w: workloads.Workload, threads: int = 16) -> np.ndarray:
     return out
 
 
+def time_graph(torch, call, n, reps=5):
+    """Median per-call microseconds of a graph of n calls (call(i), i < n), over reps replays."""
+    for i in range(3):
+        call(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        for i in range(n):
+            call(i)
+    g.replay()
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / n * 1e3)
+    del g
+    return statistics.median(times)
+
+
 # ----------------------------------------------------------------------------- CPU oracle legs
 
 def cpu_worker(spec: str):
-    """Run inside a fresh process with BLAS pinned to one thread: time the oracle."""
+    """Run inside a fresh process with BLAS pinned to one thread: time the oracle on a
+    slice of each workload's rows (the slice starts at row0_frac of the rows)."""
     import oracle
     cfg = json.loads(spec)
     names, steps, warm, frac = cfg["names"], cfg["steps"], cfg["warmup"], cfg["row_frac"]
+    r0f = cfg.get("row0_frac", 0.0)
     data = []
     for name in names:
         w = workloads.WORKLOADS[name]
         rows = max(64, int(math.ceil(w.n_out * frac)))
-        W = workloads.weight_rows(w.seed, w.n_out, w.n_in, np.arange(rows))
+        r0 = min(int(w.n_out * r0f), w.n_out - rows)
+        W = workloads.weight_rows(w.seed, w.n_out, w.n_in, np.arange(r0, r0 + rows))
         data.append((w, rows, oracle.quantize(w.fmt, W), workloads.activations(w.seed, w.n_in, 4)))
     per_step_bytes = sum(workloads_bytes(w.fmt, rows, w.n_in) for w, rows, _, _ in data) * len(NTOKS)
 
     def step():
         for ntok in NTOKS:
             for w, rows, canon, x in data:
-                oracle.gemv(w.fmt, canon, rows, w.n_in, x[:ntok])
+                if w.argmax:
+                    oracle.qgemv_argmax(w.fmt, canon, rows, w.n_in, x[:ntok])
+                else:
+                    oracle.gemv(w.fmt, canon, rows, w.n_in, x[:ntok])
 
     for _ in range(warm):
         step()
@@ -224,16 +274,51 @@ def cpu_worker(spec: str):
                       "rows": {w.name: rows for w, rows, _, _ in data}}))
 
 
-def run_cpu_oracle(names, steps, warmup, row_frac):
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_cpu_oracle(names, steps, warmup, row_frac, procs=1):
+    """The oracle in `procs` concurrent worker processes (one BLAS thread each, disjoint
+    row slices of row_frac of the rows).  Returns the bytes all workers processed per
+    step, the slowest worker's seconds and the workers' row counts."""
     env = dict(os.environ)
     for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
         env[k] = "1"
-    spec = json.dumps({"names": names, "steps": steps, "warmup": warmup, "row_frac": row_frac})
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", spec],
-                       capture_output=True, text=True, env=env, timeout=1800)
-    if r.returncode != 0:
-        raise RuntimeError(r.stderr[-2000:])
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    ps = []
+    for p in range(procs):
+        spec = json.dumps({"names": names, "steps": steps, "warmup": warmup, "row_frac": row_frac,
+                           "row0_frac": p * row_frac})
+        ps.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), "--cpu-worker", spec],
+                                   stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env))
+    outs = []
+    for pr in ps:
+        so, se = pr.communicate(timeout=1800)
+        if pr.returncode != 0:
+            raise RuntimeError(se[-2000:])
+        outs.append(json.loads(so.strip().splitlines()[-1]))
+    return {"bytes_per_step": sum(o["bytes_per_step"] for o in outs), "seconds": max(o["seconds"] for o in outs),
+            "steps": steps, "rows": outs[0]["rows"], "procs": procs}
+
+
+def cpu_baseline_entry(names, row_frac, steps):
+    """cpu_baseline: the oracle on one thread and on every host core (one worker process
+    per core, each on its own slice of the rows)."""
+    cores = host_cores()
+    one = run_cpu_oracle(names, steps=steps, warmup=0, row_frac=row_frac, procs=1)
+    allc = run_cpu_oracle(names, steps=steps, warmup=0, row_frac=row_frac / cores, procs=cores)
+    v1 = one["bytes_per_step"] * one["steps"] / one["seconds"] / 1e9
+    va = allc["bytes_per_step"] * allc["steps"] / allc["seconds"] / 1e9
+    return {"value": round(va, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": (f"{steps} passes over a {row_frac:.2%} row slice of each head at ntok 1..4 "
+                       f"(qgemv_argmax in numpy fp64); all cores: {cores} worker processes on disjoint "
+                       f"slices of it, one BLAS thread each"),
+            "one_thread": {"value": round(v1, 4), "cores": 1, "seconds": round(one["seconds"], 3),
+                           "rows": one["rows"]},
+            "all_cores": {"value": round(va, 4), "cores": cores, "seconds": round(allc["seconds"], 3)}}
 
 
 # ----------------------------------------------------------------------------- GPU legs
@@ -247,100 +332,125 @@ def main_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+    sms = int(props.multi_processor_count)
     peak, peak_kind = peaks()
     stream = torch.cuda.current_stream()
 
-    # --- the dense set: two sets of 16 distinct weight buffers (one per shape x ntok)
-    dense = [workloads.WORKLOADS[n] for n in workloads.DENSE_SET]
-    host = {w.name: gen_packed(qg, w) for w in dense}
-    bufs = {}
-    for s in range(2):
-        for w in dense:
-            base = torch.from_numpy(host[w.name]).to(dev)
-            for ntok in NTOKS:
-                bufs[(s, w.name, ntok)] = base if ntok == 1 else base.clone()
-    xs = {w.name: torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).to(dev) for w in dense}
-    ys = {(w.name, ntok): torch.empty((ntok, w.n_out), dtype=torch.float32, device=dev)
-          for w in dense for ntok in NTOKS}
-    step_bytes = sum(workloads_bytes(w.fmt, w.n_out, w.n_in) for w in dense) * len(NTOKS)
-    distinct = sum(b.numel() for b in bufs.values())
+    heads = [workloads.WORKLOADS[n] for n in HEADS]
+    W = {w.name: torch.from_numpy(gen_packed(qg, w)).to(dev) for w in heads}
+    X = {w.name: torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).to(dev) for w in heads}
+    Y = {w.name: torch.empty((4, w.n_out), dtype=torch.float32, device=dev) for w in heads}
+    AM = torch.full((len(NTOKS), len(heads), 4), -7, dtype=torch.int32, device=dev)
+    WS = {w.name: torch.zeros(qg.qgemv_argmax_workspace_bytes(w.n_out, 4), dtype=torch.uint8, device=dev)
+          for w in heads}
+    launches_per_step = len(NTOKS) * len(heads)
+    step_bytes = sum(workloads_bytes(w.fmt, w.n_out, w.n_in) for w in heads) * len(NTOKS)
+    step_algo = sum(algo_bytes(w.fmt, w.n_out, w.n_in, t, True) for w in heads for t in NTOKS)
 
-    def launches(s, ntoks):
-        for ntok in ntoks:
-            for w in dense:
-                qg.qgemv(w.fmt, bufs[(s, w.name, ntok)], w.n_out, w.n_in, xs[w.name], ys[(w.name, ntok)], ntok)
+    def call(w, ntok, stream_handle=None):
+        qg.qgemv_argmax(w.fmt, W[w.name], w.n_out, w.n_in, X[w.name], Y[w.name][:ntok],
+                        AM[ntok - 1, HEADS.index(w.name)], WS[w.name], ntok, stream=stream_handle)
+
+    def launches():
+        for ntok in NTOKS:
+            for w in heads:
+                call(w, ntok)
 
     def barrier():
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
 
-    G = 10   # steps per chunk graph (even: the two buffer sets alternate inside it)
-
     def capture(early: bool):
-        """One graph per step (per buffer set) and one graph of G consecutive steps."""
         qg.qg_set_launch_options(qg.QG_LAUNCH_EARLY_START if early else 0)
-        for s in range(2):                              # warm every kernel / cache occupancy before capture
-            launches(s, NTOKS)
+        launches()                                 # every kernel and plan warmed before capture
         torch.cuda.synchronize()
-        single = []
-        for s in range(2):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, capture_error_mode="thread_local"):
-                launches(s, NTOKS)
-            single.append(g)
-        chunk = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(chunk, capture_error_mode="thread_local"):
-            for i in range(G):
-                launches(i % 2, NTOKS)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            launches()
         torch.cuda.synchronize()
-        return single, chunk
+        return g
 
-    def run(graphs, K, Wm):
-        single, chunk = graphs
-        for i in range(Wm):
-            single[i % 2].replay()
+    def run_block(g, K):
+        """Exactly K steps between a barrier + synchronize on both sides; CUDA-event ms."""
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
-        t0 = time.time()
         start.record()
-        i = 0
-        while i + G <= K:
-            chunk.replay()
-            i += G
-        while i < K:
-            single[i % 2].replay()
-            i += 1
+        for _ in range(K):
+            g.replay()
         end.record()
         torch.cuda.synchronize()
         barrier()
-        t1 = time.time()
-        return start.elapsed_time(end), t0, t1
+        return start.elapsed_time(end)
 
-    K, Wm = args.steps, max(3, args.warmup)
+    K, Wm = max(1, args.steps), max(3, args.warmup)
     # Secondary: ordinary launches (each kernel waits for the previous one to finish).
-    plain_graphs = capture(False)
-    plain_ms, _, _ = run(plain_graphs, max(10, K // 4), Wm)
-    plain_value = step_bytes * max(10, K // 4) / (plain_ms * 1e-3) / 1e9
-    del plain_graphs
+    g_plain = capture(False)
+    for _ in range(Wm):
+        g_plain.replay()
+    plain_ms = run_block(g_plain, K)
+    plain_value = step_bytes * K / (plain_ms * 1e-3) / 1e9
+    del g_plain
     # Headline: early start (programmatic dependent launch): the weights are written
     # once before the run, so a call may stream them while the previous call finishes.
-    graphs = capture(True)
+    g = capture(True)
+    t_w = time.perf_counter()
+    for _ in range(Wm):
+        g.replay()
+    torch.cuda.synchronize()
+    est_step_s = (time.perf_counter() - t_w) / Wm
+    blocks = timed_blocks(K * est_step_s)
+    if world > 1:
+        blocks = int(max_over_ranks(float(blocks), world, dev))
     uuid = getattr(props, "uuid", None)
     gpu_id = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else (str(uuid) if uuid else str(local_rank))
+    block_ms = []
     with ClockSampler(gpu_id) as clk:
-        total_ms, t_wall0, t_wall1 = run(graphs, K, Wm)
+        t_wall0 = time.time()
+        for _ in range(blocks):
+            block_ms.append(run_block(g, K))
+        t_wall1 = time.time()
     clocks = clk.summary(t_wall0, t_wall1)
-    total_ms = max_over_ranks(total_ms, world, dev)
-    ms_per_step = total_ms / K
-    value = job_gbs(step_bytes, K, world, total_ms)
+    total_ms = max_over_ranks(sum(block_ms), world, dev)
+    steps_timed = K * blocks
+    ms_per_step = total_ms / steps_timed
+    value = job_gbs(step_bytes, steps_timed, world, total_ms)
+    sm_mhz = clocks.get("sm_mhz") or 2070.0
 
-    # --- roofline of the dominant kernel.  Every launch of the step is qgemv_kernel
-    # (100% of the step's GPU time), so its average launch duration is the step time
-    # over the 16 launches (consecutive launches overlap slightly under early start).
-    step_algo = sum(algo_bytes(w.fmt, w.n_out, w.n_in, t) for w in dense for t in NTOKS)
-    achieved = step_algo * K / (total_ms * 1e-3) / 1e9
+    # --- per-config table: each (head, ntok) launch alone, and the 2560->12288 projection
+    per_config = {}
+    for w in heads:
+        row = {}
+        for ntok in NTOKS:
+            us = time_graph(torch, lambda i, w=w, ntok=ntok: call(w, ntok), n=20)
+            gbs = workloads_bytes(w.fmt, w.n_out, w.n_in) / (us * 1e-6) / 1e9
+            fma_rate = ntok * w.n_out * w.n_in / (us * 1e-6)
+            fma_peak = FMA_LANES_PER_CLK_SM * sms * sm_mhz * 1e6
+            row[str(ntok)] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                              "frac_nominal_7900": round(gbs / 7900.0, 4),
+                              "fma_frac": round(fma_rate / fma_peak, 4)}
+        per_config[w.name] = row
+    proj = workloads.WORKLOADS["q8_0_12288x2560"]
+    pbase = torch.from_numpy(gen_packed(qg, proj)).to(dev)
+    copies = max(1, math.ceil(4 * l2 / pbase.numel()))
+    pool = [pbase] + [pbase.clone() for _ in range(copies - 1)]
+    px = torch.from_numpy(workloads.activations(proj.seed, proj.n_in, 4)).to(dev)
+    py = torch.empty((4, proj.n_out), dtype=torch.float32, device=dev)
+    row = {}
+    for ntok in NTOKS:
+        us = time_graph(torch, lambda i, ntok=ntok: qg.qgemv(proj.fmt, pool[i % copies], proj.n_out, proj.n_in,
+                                                             px, py[:ntok], ntok), n=50)
+        gbs = workloads_bytes(proj.fmt, proj.n_out, proj.n_in) / (us * 1e-6) / 1e9
+        row[str(ntok)] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                          "frac_nominal_7900": round(gbs / 7900.0, 4)}
+    per_config[proj.name] = row
+    del pool, pbase
+
+    # --- roofline of the dominant kernel: every launch of the step is qgemv_kernel
+    # (100% of the step's GPU time); its average launch duration is the step time
+    # over the 8 launches (consecutive launches overlap slightly under early start).
+    achieved = step_algo * steps_timed / (total_ms * 1e-3) / 1e9 / world
     traffic = None
     tfile = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     if os.path.exists(tfile):
@@ -348,109 +458,120 @@ def main_gpu(args, rank, world, local_rank):
             td = json.load(f)
         if td.get("csrc_hash") == csrc_hash():
             traffic = td.get("traffic_bytes_per_launch")
+    aff = per_config["affine4_head_248320x5120"]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": "qgemv_kernel (all 16 launches of the step: 4 shapes x ntok 1..4)",
-                "algorithmic_bytes_per_launch": round(step_algo / 16),
-                "avg_launch_us": round(ms_per_step / 16 * 1e3, 3), "peak_kind": peak_kind}
+                "kernel": "qgemv_kernel (all 8 launches of the step: 2 heads x ntok 1..4)",
+                "algorithmic_bytes_per_launch": round(step_algo / launches_per_step),
+                "avg_launch_us": round(ms_per_step / launches_per_step * 1e3, 3), "peak_kind": peak_kind,
+                "secondary": {"bound": "fp32 fma pipe (4-bit head at ntok 3-4)",
+                              "peak_fma_per_s": FMA_LANES_PER_CLK_SM * sms * sm_mhz * 1e6,
+                              "fma_frac": {t: aff[t]["fma_frac"] for t in ("3", "4")}}}
 
     result = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
               "warmup": Wm, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
               "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
-              "config": {"workload": WORKLOAD_NAME, "formats": "Q8_0 weights, fp32 x and y, fp32 accumulation",
-                         "weight_bytes_per_step": step_bytes, "launches_per_step": 16,
-                         "l2": f"inputs larger than L2: each step reads {step_bytes / 1e6:.0f} MB of distinct "
-                               f"weights; two alternating sets ({distinct / 1e6:.0f} MB) vs L2 {l2 / 1e6:.0f} MB",
-                         "timing": f"CUDA graph replay ({G} steps = {16 * G} launches per graph), "
-                                   "CUDA events on the launch stream",
+              "config": {"workload": WORKLOAD_NAME,
+                         "formats": "Q8_0 and affine 4-bit g64 weights, fp32 x, logits and accumulation, "
+                                    "int32 argmax",
+                         "weight_bytes_per_step": step_bytes, "launches_per_step": launches_per_step,
+                         "l2": f"inputs larger than L2: every launch reads a {675.4:.0f}-{715.2:.0f} MB head "
+                               f"(L2 {l2 / 1e6:.0f} MB)",
+                         "timing": f"{blocks} timed blocks of exactly {K} steps (CUDA graph of one step replayed), "
+                                   f"each between a barrier and a synchronize, CUDA events on the launch stream; "
+                                   f"{steps_timed} steps, {total_ms / 1e3:.2f} s timed",
+                         "timed_blocks": blocks, "block_ms": [round(b, 3) for b in block_ms],
                          "launch": "early start (programmatic dependent launch, QG_LAUNCH_EARLY_START)",
                          "value_plain_launches": round(plain_value, 2),
+                         "per_config": per_config,
                          "parallelism": "replicas" if world > 1 else "single GPU"},
               "frac_of_peak": round(value / world / peak, 4), "peak_gbs": peak, "peak_kind": peak_kind,
               "frac_of_nominal_7900": round(value / world / 7900.0, 4),
-              "clocks": clocks, "gpu_launches": 16 * K, "roofline": roofline}
+              "clocks": clocks, "gpu_launches": launches_per_step * steps_timed, "roofline": roofline}
 
     # --- e2e through the public API with host buffers (no graph), rank-local.  A
-    # step uploads every shape's x in one copy from pinned memory, makes the 16 calls
-    # and reads every y back in one copy (x and y are views of one buffer each, as a
-    # caller would lay them out), then waits for the host copy.
-    x_elems = {w.name: 4 * w.n_in for w in dense}
-    y_elems = {(w.name, ntok): ntok * w.n_out for w in dense for ntok in NTOKS}
-    pin_x_all = torch.empty(sum(x_elems.values()), dtype=torch.float32).pin_memory()
-    dx_all = torch.empty(pin_x_all.numel(), dtype=torch.float32, device=dev)
-    pin_y_all = torch.empty(sum(y_elems.values()), dtype=torch.float32).pin_memory()
-    dy_all = torch.empty(pin_y_all.numel(), dtype=torch.float32, device=dev)
-    dx, dy, off = {}, {}, 0
-    for w in dense:
-        n = x_elems[w.name]
-        pin_x_all[off:off + n].copy_(torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).reshape(-1))
-        dx[w.name] = dx_all[off:off + n].view(4, w.n_in)
-        off += n
-    off = 0
-    for k, n in y_elems.items():
-        dy[k] = dy_all[off:off + n]
-        off += n
-    h2d = pin_x_all.numel() * 4
-    d2h = pin_y_all.numel() * 4
-    sh = qg.current_stream_handle()
-
-    def e2e_step(s):
-        dx_all.copy_(pin_x_all, non_blocking=True)
+    # step uploads both heads' x in one copy from pinned memory, makes the 8 calls,
+    # reads the logits and the argmax ids back (one copy each) and waits for them.
+    if not args.no_e2e:
+        xs_elems = [4 * w.n_in for w in heads]
+        pin_x = torch.empty(sum(xs_elems), dtype=torch.float32).pin_memory()
+        dx = torch.empty(pin_x.numel(), dtype=torch.float32, device=dev)
+        off, xv = 0, {}
+        for w, n in zip(heads, xs_elems):
+            pin_x[off:off + n].copy_(torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).reshape(-1))
+            xv[w.name] = dx[off:off + n].view(4, w.n_in)
+            off += n
+        y_all = torch.empty(sum(t * w.n_out for w in heads for t in NTOKS), dtype=torch.float32, device=dev)
+        pin_y = torch.empty(y_all.numel(), dtype=torch.float32).pin_memory()
+        pin_am = torch.empty(AM.numel(), dtype=torch.int32).pin_memory()
+        yv, off = {}, 0
         for ntok in NTOKS:
-            for w in dense:
-                qg.qgemv(w.fmt, bufs[(s, w.name, ntok)], w.n_out, w.n_in, dx[w.name], dy[(w.name, ntok)], ntok,
-                         stream=sh)
-        pin_y_all.copy_(dy_all, non_blocking=True)
-        stream.synchronize()
+            for w in heads:
+                yv[(w.name, ntok)] = y_all[off:off + ntok * w.n_out].view(ntok, w.n_out)
+                off += ntok * w.n_out
+        sh = qg.current_stream_handle()
 
-    for i in range(5):
-        e2e_step(i % 2)
-    n_e2e = max(50, min(2000, K // 10))
-    t0 = time.perf_counter()
-    for i in range(n_e2e):
-        e2e_step(i % 2)
-    e2e_s = time.perf_counter() - t0
-    result["e2e"] = {"value": round(step_bytes * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
-                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-                     "how": "python qgemv calls per launch (ctypes), all x uploaded in one copy from pinned "
-                            "memory and all y read back in one copy, host synchronized every step; no CUDA "
-                            "graph; early start on"}
+        def e2e_step():
+            dx.copy_(pin_x, non_blocking=True)
+            for ntok in NTOKS:
+                for w in heads:
+                    qg.qgemv_argmax(w.fmt, W[w.name], w.n_out, w.n_in, xv[w.name], yv[(w.name, ntok)],
+                                    AM[ntok - 1, HEADS.index(w.name)], WS[w.name], ntok, stream=sh)
+            pin_y.copy_(y_all, non_blocking=True)
+            pin_am.copy_(AM.view(-1), non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        n_e2e = max(20, min(400, int(1.0 / max(est_step_s, 1e-4))))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_s = time.perf_counter() - t0
+        result["e2e"] = {"value": round(step_bytes * n_e2e / e2e_s / 1e9, 2), "unit": "GB/s",
+                         "h2d_bytes_per_step": pin_x.numel() * 4,
+                         "d2h_bytes_per_step": pin_y.numel() * 4 + pin_am.numel() * 4, "steps": n_e2e,
+                         "how": "python qgemv_argmax calls (ctypes), x of both heads uploaded in one copy from "
+                                "pinned memory, all logits and argmax ids read back, host synchronized every "
+                                "step; no CUDA graph; early start on"}
 
     if rank == 0 and not args.no_detail:
-        result["per_workload"] = detail_table(args, qg, torch, dev, l2, peak)
+        result["per_workload"] = detail_table(args, qg, torch, dev, l2, peak, have=W)
 
     if rank == 0 and not args.no_cpu:
         try:
-            cores = 1
-            r = run_cpu_oracle(workloads.DENSE_SET, steps=1, warmup=0, row_frac=1.0)
-            result["cpu_baseline"] = {"value": round(r["bytes_per_step"] * r["steps"] / r["seconds"] / 1e9, 4),
-                                      "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                      "sample": "one full step of the workload (16 oracle calls: 4 shapes x ntok "
-                                                "1..4, all rows), numpy fp64, BLAS pinned to 1 thread",
-                                      "seconds": round(r["seconds"], 3),
-                                      "host_cores_available": len(os.sched_getaffinity(0))}
+            result["cpu_baseline"] = cpu_baseline_entry(HEADS, row_frac=1.0 / 16, steps=6)
         except Exception as e:  # noqa: BLE001
-            result["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            result["cpu_baseline"] = {"value": None, "unit": "GB/s", "cores": host_cores(), "kind": "oracle",
                                       "sample": f"failed: {e}"}
     return result
 
 
-def detail_table(args, qg, torch, dev, l2, peak):
-    """Every workload x ntok: median of 5 replays of a 50-launch graph over rotating copies."""
-    names = [n for n in workloads.WORKLOADS] if not args.detail_only else args.detail_only.split(",")
+def detail_table(args, qg, torch, dev, l2, peak, have=None):
+    """Every workload x ntok except the headline heads (timed in config.per_config): median of
+    5 replays of a 50-launch graph over rotating copies.  `have`: packed matrices already on
+    the device, by workload name (the drafted-vocabulary variants reuse the full Q8_0 head)."""
+    if args.detail_only:
+        names = args.detail_only.split(",")
+    else:
+        names = [n for n in workloads.WORKLOADS if n not in HEADS]
     table = {}
     cache = {}
+    have = have or {}
     for name in names:
         w = workloads.WORKLOADS[name]
         src = name
         if name == "q8_0_head_106299x2560":
             src = "q8_0_head_248320x2560"
-        if src not in cache:
-            ws = workloads.WORKLOADS[src]
-            cache.clear()
-            torch.cuda.empty_cache()
-            cache[src] = torch.from_numpy(gen_packed(qg, ws)).to(dev)
-        base = cache[src]
+        if src in have:
+            base = have[src]
+        else:
+            if src not in cache:
+                ws = workloads.WORKLOADS[src]
+                cache.clear()
+                torch.cuda.empty_cache()
+                cache[src] = torch.from_numpy(gen_packed(qg, ws)).to(dev)
+            base = cache[src]
         wbytes = workloads_bytes(w.fmt, w.n_out, w.n_in)
         copies = max(1, math.ceil(4 * l2 / base.numel()))
         pool = [base] + [base.clone() for _ in range(copies - 1)]
@@ -490,9 +611,13 @@ def detail_table(args, qg, torch, dev, l2, peak):
         table[name] = {"fmt": w.fmt, "n_out": w.n_out, "n_in": w.n_in, "weight_bytes": wbytes,
                        "call": "qgemv_argmax" if w.argmax else "qgemv", "copies": copies, "ntok": row}
         del pool
-        if name in workloads.DRAFT_IDS:
-            table[f"{w.fmt}_draft_ids_{workloads.DRAFT_IDS[name][0]}_of_{w.n_out}x{w.n_in}"] = \
-                draft_ids_detail(qg, torch, dev, l2, peak, w, base)
+
+    for name in [n for n in workloads.DRAFT_IDS if (n in names or (n in HEADS and not args.detail_only))]:
+        w = workloads.WORKLOADS[name]
+        base = have[name] if name in have else torch.from_numpy(gen_packed(qg, w)).to(dev)
+        table[f"{w.fmt}_draft_ids_{workloads.DRAFT_IDS[name][0]}_of_{w.n_out}x{w.n_in}"] = \
+            draft_ids_detail(qg, torch, dev, l2, peak, w, base)
+        del base
     cache.clear()
     torch.cuda.empty_cache()
     if not args.detail_only or any(n in workloads.EXPERT_LAYERS for n in names):
@@ -661,30 +786,89 @@ def draft_ids_detail(qg, torch, dev, l2, peak, w, head):
 # ----------------------------------------------------------------------------- reference arm
 
 def reference_arm(args, rank, world):
+    """The oracle as it stands on the host's cores (one worker process per core, one BLAS
+    thread each, disjoint row slices), on the headline workload; each step is a bounded
+    row sample of it, sized so the run ends within a few minutes."""
     if rank != 0:
         return None
-    K, Wm = args.steps, max(3, args.warmup)
-    full_rows = sum(workloads.WORKLOADS[n].n_out for n in workloads.DENSE_SET)
-    # a full step of the oracle takes seconds; sample rows so the run ends within ~2 minutes
-    est_full_step_s = 6.0
-    frac = min(1.0, 120.0 / ((K + Wm) * est_full_step_s))
-    r = run_cpu_oracle(workloads.DENSE_SET, steps=K, warmup=Wm, row_frac=frac)
+    K, Wm = max(1, args.steps), max(3, args.warmup)
+    cores = host_cores()
+    # One step over every row of both heads takes ~60-80 s of oracle work on one core;
+    # sample rows so that K + Wm steps take about two minutes on all cores.
+    est_full_step_core_s = 60.0
+    frac = min(1.0, 120.0 * cores / ((K + Wm) * est_full_step_core_s))
+    r = run_cpu_oracle(HEADS, steps=K, warmup=Wm, row_frac=frac / cores, procs=cores)
     value = r["bytes_per_step"] * r["steps"] / r["seconds"] / 1e9
-    sample = (f"each step: the oracle on the first {frac:.4%} of each shape's rows (>= 64 rows), "
-              f"4 shapes x ntok 1..4, numpy fp64, BLAS pinned to 1 thread")
+    sample = (f"each step: the oracle (qgemv_argmax, numpy fp64) on {frac:.3%} of each head's rows at ntok "
+              f"1..4, split over {cores} worker processes (one per host core, one BLAS thread each)")
     return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": Wm, "ms_per_step": round(r["seconds"] / K * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD_NAME, "rows_sampled": r["rows"]},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "config": {"workload": WORKLOAD_NAME, "rows_sampled_per_worker": r["rows"], "workers": cores},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def tile_sweep(args):
+    """GB/s per (workload, ntok, tile spec): each point is the median of 3 replays of a
+    20-launch graph rotating over weight copies totalling >= 4x L2 (set
+    QGEMV_EARLY_START=1 to sweep with early-start launches).  The table in
+    csrc/tile_select.cpp was filled from such sweeps."""
+    import itertools
+    import torch
+    import block_quantized_token_format_gb300 as qg
+    import __graft_entry__
+    __graft_entry__.build()
+    specs = args.sweep_specs.split(";") if args.sweep_specs else [
+        f"rpw={r},depth={d},warps={w},ctas={c}"
+        for r, d, w, c in itertools.product((1, 2, 4), (2, 3, 5, 8), (4, 8, 12, 16), (1, 2, 3))]
+    ntoks = [int(v) for v in args.sweep_ntoks.split(",")]
+    dev = torch.device("cuda:0")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    out = open(args.sweep_out, "a")
+    for name in args.sweep.split(","):
+        w = workloads.WORKLOADS[name]
+        base = torch.from_numpy(gen_packed(qg, w)).to(dev)
+        copies = max(1, math.ceil(4 * l2 / base.numel()))
+        pool = [base] + [base.clone() for _ in range(copies - 1)]
+        x = torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).to(dev)
+        y = torch.empty((4, w.n_out), dtype=torch.float32, device=dev)
+        am = torch.empty(4, dtype=torch.int32, device=dev)
+        ws = torch.zeros(qg.qgemv_argmax_workspace_bytes(w.n_out, 4), dtype=torch.uint8, device=dev)
+        wb = workloads_bytes(w.fmt, w.n_out, w.n_in)
+        for ntok in ntoks:
+            best = None
+            for spec in specs:
+                try:
+                    qg.qg_set_tile_override(spec)
+                    desc = qg.qg_describe_tile(w.fmt, w.n_out, w.n_in, ntok)
+                except qg.QGError:
+                    continue
+
+                def call(i, ntok=ntok):
+                    if w.argmax:
+                        qg.qgemv_argmax(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y[:ntok], am, ws, ntok)
+                    else:
+                        qg.qgemv(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y[:ntok], ntok)
+                us = time_graph(torch, call, n=20, reps=3)
+                rec = {"name": name, "ntok": ntok, "spec": spec, "desc": desc, "us": round(us, 3),
+                       "gbs": round(wb / us / 1e3, 1)}
+                out.write(json.dumps(rec) + "\n")
+                out.flush()
+                if best is None or rec["gbs"] > best["gbs"]:
+                    best = rec
+            print(json.dumps({"best": best}), flush=True)
+        del pool, base
+        torch.cuda.empty_cache()
+    qg.qg_set_tile_override(None)
+
+
 # ----------------------------------------------------------------------------- entry
 
-def one_shape(spec: str):
-    """Run one synthetic shape three times (the small case an ncu capture profiles)."""
+def one_shape(spec: str, argmax: bool = False):
+    """Run one synthetic shape three times (the small case an ncu capture profiles), through
+    qgemv or, with argmax, qgemv_argmax."""
     import torch
     import block_quantized_token_format_gb300 as qg
     import __graft_entry__
@@ -697,9 +881,15 @@ def one_shape(spec: str):
     packed = torch.from_numpy(gen_packed(qg, w)).cuda()
     x = torch.from_numpy(workloads.activations(w.seed, n_in, 4)).cuda()
     y = torch.empty((4, n_out), device="cuda")
+    am = torch.empty(4, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(qg.qgemv_argmax_workspace_bytes(n_out, 4), dtype=torch.uint8, device="cuda")
     for _ in range(3):
-        qg.qgemv(fmt, packed, n_out, n_in, x, y, ntok)
+        if argmax:
+            qg.qgemv_argmax(fmt, packed, n_out, n_in, x, y[:ntok], am, ws, ntok)
+        else:
+            qg.qgemv(fmt, packed, n_out, n_in, x, y[:ntok], ntok)
     torch.cuda.synchronize()
+    assert qg.qg_device_status() == 0
     print("ok", qg.qg_describe_tile(fmt, n_out, n_in, ntok))
 
 
@@ -754,8 +944,14 @@ def main():
     if args.cpu_worker:
         cpu_worker(args.cpu_worker)
         return
+    if args.sweep:
+        tile_sweep(args)
+        return
     if args.one:
         one_shape(args.one.replace(";", ","))
+        return
+    if args.one_argmax:
+        one_shape(args.one_argmax.replace(";", ","), argmax=True)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
