@@ -121,20 +121,26 @@ def test_workspace_reuse_across_calls_and_ntok():
 
 
 def _oracle_full(w, x, threads=16):
-    """Oracle logits of a whole head, quantized chunk by chunk by the oracle itself."""
+    """Oracle logits of a whole head, quantized chunk by chunk by the oracle itself, and the
+    head's device bytes as the library's packer (qg_pack, the call the benchmark packs with)
+    writes them.  Every chunk's packer bytes must equal the oracle's bytes carried into the
+    device layout, so the bytes the kernel reads here are the tested bytes and the benched ones."""
     n_chunks = (w.n_out + workloads.ROW_CHUNK - 1) // workloads.ROW_CHUNK
 
     def one(c):
         Wc = workloads.weight_chunk(w.seed, w.n_out, w.n_in, c)
         canon = ORC.quantize(w.fmt, Wc)
         rows = Wc.shape[0]
-        return (c, canon, ORC.gemv(w.fmt, canon, rows, w.n_in, x), ORC.gemv_abs(w.fmt, canon, rows, w.n_in, x))
+        from_oracle = qg.qg_to_device_layout(w.fmt, canon, rows, w.n_in)
+        packed = qg.qg_pack(w.fmt, Wc)
+        same = np.array_equal(packed, from_oracle)
+        return (c, same, packed, ORC.gemv(w.fmt, canon, rows, w.n_in, x), ORC.gemv_abs(w.fmt, canon, rows, w.n_in, x))
 
     ys, dens, packed = [None] * n_chunks, [None] * n_chunks, [None] * n_chunks
     with ThreadPoolExecutor(threads) as ex:
-        for c, canon, y, den in ex.map(one, range(n_chunks)):
-            ys[c], dens[c] = y, den
-            packed[c] = qg.qg_to_device_layout(w.fmt, canon, canon.size // ORC.weight_bytes(w.fmt, 1, w.n_in), w.n_in)
+        for c, same, pk, y, den in ex.map(one, range(n_chunks)):
+            assert same, f"{w.name}: qg_pack bytes differ from the oracle's in row chunk {c}"
+            ys[c], dens[c], packed[c] = y, den, pk
     return np.concatenate(ys, axis=1), np.concatenate(dens, axis=1), np.concatenate(packed)
 
 
@@ -160,3 +166,68 @@ def test_full_lm_head(name):
             y, am = run_argmax(w.fmt, packed, n_draft, w.n_in, x[:ntok], ws)
             check_argmax(am, ref[:ntok, :n_draft], f"draft ntok={ntok}")
     print(f"{name}: max normalised error {worst:.3g}, argmax {am}")
+
+
+def _nan_scales(fmt, canon, n_out, n_in, rows):
+    """Canonical bytes with every block scale of `rows` set to an fp16 NaN (0x7E00)."""
+    c = canon.copy()
+    if fmt == "q8_0":
+        rb = n_in // 32 * 34
+        for r in rows:
+            for b in range(n_in // 32):
+                c[r * rb + 34 * b:r * rb + 34 * b + 2] = (0x00, 0x7E)
+    elif fmt == "affine4_g64":
+        scales = c[n_out * n_in // 2:n_out * n_in // 2 + n_out * n_in // 32].view(np.uint16).reshape(n_out, -1)
+        for r in rows:
+            scales[r, :] = 0x7E00
+    else:
+        raise ValueError(fmt)
+    return c
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "affine4_g64"])
+def test_nan_rows_never_win(fmt):
+    """A row whose block scales are NaN has NaN logits and never wins the argmax, even when
+    its finite counterpart would be the largest logit of every token."""
+    n_out, n_in = 5003, 2560
+    x = workloads.activations(21, n_in, 4)
+    W = workloads.gaussian(21, (n_out, n_in), 0.02)
+    W[1234] = 0.2 * np.sign(x[0])            # the winner of token 0 while its scales are finite
+    W[77] = 0.2 * np.sign(x[3])              # the winner of token 3
+    canon = ORC.quantize(fmt, W)
+    nan_rows = [0, 1234, n_out - 1]
+    bad = _nan_scales(fmt, canon, n_out, n_in, nan_rows)
+    packed = torch.from_numpy(qg.qg_to_device_layout(fmt, bad, n_out, n_in)).to(dev())
+    ref = ORC.gemv(fmt, bad, n_out, n_in, x)
+    den = ORC.gemv_abs(fmt, bad, n_out, n_in, x)
+    assert np.isnan(ref[:, nan_rows]).all()
+    ws = new_workspace(n_out)
+    for ntok in (1, 4):
+        y, am = run_argmax(fmt, packed, n_out, n_in, x[:ntok], ws)
+        assert np.isnan(y[:, nan_rows]).all()
+        fin = np.setdiff1d(np.arange(n_out), nan_rows)
+        rel = np.abs(y[:, fin].astype(np.float64) - ref[:ntok, fin]) / den[:ntok, fin]
+        assert rel.max() <= TOL
+        assert not np.isin(am, nan_rows).any(), am
+        assert np.array_equal(am, ORC.argmax_first(y))
+        check_argmax(am, np.where(np.isnan(ref[:ntok]), -np.inf, ref[:ntok]), f"{fmt} NaN rows ntok={ntok}")
+        if ntok == 4:
+            assert am[3] == 77
+        _, am2 = run_argmax(fmt, packed, n_out, n_in, x[:ntok], ws, write_logits=False)
+        assert np.array_equal(am2, am)
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "affine4_g64"])
+def test_all_nan_logits_give_minus_one(fmt):
+    n_out, n_in = 3001, 2560
+    x = workloads.activations(22, n_in, 4)
+    canon = ORC.quantize(fmt, workloads.gaussian(22, (n_out, n_in), 0.02))
+    bad = _nan_scales(fmt, canon, n_out, n_in, range(n_out))
+    packed = torch.from_numpy(qg.qg_to_device_layout(fmt, bad, n_out, n_in)).to(dev())
+    ws = new_workspace(n_out)
+    for ntok in (1, 3, 4):
+        y, am = run_argmax(fmt, packed, n_out, n_in, x[:ntok], ws)
+        assert np.isnan(y).all()
+        assert (am == -1).all(), am
+        _, am2 = run_argmax(fmt, packed, n_out, n_in, x[:ntok], ws, write_logits=False)
+        assert (am2 == -1).all(), am2
