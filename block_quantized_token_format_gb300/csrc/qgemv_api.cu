@@ -575,8 +575,33 @@ constexpr size_t kNoAllocScratchBytes = 16 + size_t(kNoAllocMaxGrid) * kMaxNtok 
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch per device, looked up once per device.
-std::atomic<void*> g_noalloc_addr[kMaxDevices];
+// Device address of g_noalloc_scratch per device, looked up once per device and
+// context: a device reset gives the device a new context, in which the library's
+// module (and the array) may sit at another address, so a change of the current
+// context repeats the lookup.
+struct NoAllocSlot {
+    std::mutex mu;
+    void* ctx = nullptr;
+    void* addr = nullptr;
+};
+NoAllocSlot g_noalloc[kMaxDevices];
+
+// cuCtxGetCurrent, fetched from the driver through the runtime once (the library
+// links only the runtime).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+    static const CtxGetCurrentFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return CtxGetCurrentFn(nullptr);
+        }
+        return reinterpret_cast<CtxGetCurrentFn>(f);
+    }();
+    return fn;
+}
 
 }  // namespace
 }  // namespace qg
@@ -589,18 +614,31 @@ extern "C" qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_o
     if (!argmax) return QG_EINVAL;
     if ((y && !aligned(y, 4)) || !aligned(argmax, 4)) return QG_EALIGN;
 
-    // Set-up, once per device, with that device current: the host-side name of the
-    // array is only a stand-in, so ask the runtime for its device address.
+    // Set-up, once per device (and again after a device reset), with that device
+    // current: the host-side name of the array is only a stand-in, so ask the runtime
+    // for its device address.
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
     if (dev < 0 || dev >= kMaxDevices) return QG_EUNSUPPORTED;
-    void* scratch = g_noalloc_addr[dev].load(std::memory_order_acquire);
-    if (scratch == nullptr) {
-        if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || scratch == nullptr) {
-            cudaGetLastError();
-            return QG_ECUDA;
+    void* scratch = nullptr;
+    {
+        CUcontext ctx = nullptr;
+        const CtxGetCurrentFn get = ctx_get_current();
+        if (get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+        NoAllocSlot& slot = g_noalloc[dev];
+        std::lock_guard<std::mutex> lk(slot.mu);
+        if (slot.addr == nullptr || ctx == nullptr || slot.ctx != static_cast<void*>(ctx)) {
+            // (The lookup makes the device's primary context current if none was.)
+            void* a = nullptr;
+            if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || a == nullptr) {
+                cudaGetLastError();
+                return QG_ECUDA;
+            }
+            if (ctx == nullptr && get && get(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+            slot.addr = a;
+            slot.ctx = ctx;
         }
-        g_noalloc_addr[dev].store(scratch, std::memory_order_release);
+        scratch = slot.addr;
     }
 
     Plan p;

@@ -366,14 +366,28 @@ qg_status qgemv_expert_layer(qg_fmt fmt, const void* W_gate_up, const void* W_do
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = static_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    // A cooperative launch: the driver starts the grid only when every CTA can be
+    // resident at once, so the CTAs that meet at the barriers never wait on a CTA that
+    // other work keeps off the GPU (the bounded waits stay as a guard).  Early start is
+    // added when enabled; if the driver refuses the two together, the layer launches
+    // cooperatively without it.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (launch_flags() & QG_LAUNCH_EARLY_START) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
     }
-    if (cudaLaunchKernelExC(&cfg, fn, params) != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, params);
+    if (e != cudaSuccess && cfg.numAttrs == 2) {
+        cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelExC(&cfg, fn, params);
+    }
+    if (e != cudaSuccess) { cudaGetLastError(); return QG_ECUDA; }
     return QG_OK;
 }
 

@@ -52,7 +52,9 @@ typedef int qg_status;
 #define QG_EWORKSPACE   (-4)  /* argmax workspace missing or too small                  */
 #define QG_ECUDA        (-5)  /* the CUDA runtime reported an error at launch             */
 
-/* A static, human-readable string for a status code. */
+/* A static, human-readable string for a status code.  The status codes are this
+ * library's own error contract (validation before launch, no trap or exit); the
+ * pages have no counterpart. */
 const char* qg_strerror(qg_status status);
 
 /* ABI version of this header (incremented on incompatible change). */
@@ -60,7 +62,15 @@ int qg_abi_version(void);
 
 /* ------------------------------------------------------------------ sizes and layouts
  * Canonical layout: the format's stored bytes, row-major, exactly the weight bytes
- * of the bandwidth metric.
+ * of the bandwidth metric (Where the time goes on an M2 Max, "Dense K-quants are
+ * integer-ALU bound at small batches": effective bandwidth = weight bytes / time,
+ * scales included).  The byte counts match the pages where they print them: Q8_0's
+ * 34 bytes per 32 weights reproduces the (time, GB/s) rows of the Track 2 Audit &
+ * Optimization Report's table 2.1 (e.g. 2560 x 40525 = 110.2 MB); the affine 4-bit
+ * g64 head's 715.2 MB is the split of perf(speculative): cut the MTP drafter's
+ * per-step cost, "The cost model" (weights 635.7 + scales 39.7 + biases 39.7 MB).
+ * The pages name the formats but print no block layout: the layouts below are the
+ * formats' usual ones (Q8_0 / Q4_0 / Q5_0 blocks of 32, MLX-style affine planes).
  *   Q8_0:  per 32-block: little-endian fp16 d, then 32 int8 q.
  *   Q4_0:  per 32-block: fp16 d, then 16 bytes; byte j holds element j in its low
  *          nibble and element j+16 in its high nibble.
@@ -92,6 +102,13 @@ size_t  qg_packed_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);
 int64_t qg_row_stride(qg_fmt fmt, int64_t n_in);     /* device-layout bytes per row */
 
 /* --------------------------------------------------------------------- host packer
+ * The pages give no encoder for any format (they time and name Q8_0, Q4_0 and
+ * Q5_0 draft weights: opus-mtp-turbo Track 1 report, item 3, and the M2 Max page's
+ * format table; the drafter issue's 4-bit head).  The quantizers below are the
+ * rules of the workloads this library is measured on (d = max|w|/127 for Q8_0;
+ * d = m/-8 with m the value of largest magnitude for Q4_0; min/max fit of s and
+ * b per 64 for the affine format); what those rules leave open (rounding, nibble
+ * order, which d the codes use) is stated per format.
  * All three work on host memory, use several CPU threads, and return QG_EINVAL on
  * a null pointer, n_out < 1, or n_in not a multiple of the block (32 for Q8_0,
  * Q4_0 and Q5_0; 64 for AFFINE4_G64; 16 for BF16, the kernels' 16-weight chunk).
@@ -259,8 +276,12 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
 /* qg_describe_expert_tile: the geometry qgemv_experts would use for one expert's
  * shape, written as qg_describe_tile does.
  *
- * qgemv_expert_layer: the whole routed-expert layer in ONE launch (no counterpart
- * launch structure on the pages; the same arithmetic as qg_expert_plan +
+ * qgemv_expert_layer: the whole routed-expert layer in ONE launch, for callers that
+ * want one call instead of three.  It is the SLOWER path: on GB300 it measured 4-6%
+ * slower than qg_expert_plan + qgemv_experts x 2 with early start (a barrier waits
+ * for the slowest CTA just as the next launch would, and the single kernel holds
+ * both projections' registers); prefer the three calls where speed matters.  (No
+ * counterpart launch structure on the pages; the same arithmetic as qg_expert_plan +
  * qgemv_experts(gate/up, QG_EXPERTS_SWIGLU) + qgemv_experts(down, X_BY_SLOT), and
  * bitwise the same act and y).  Every CTA builds the plan from ids in shared memory
  * (the plan is also written to `plan`, qg_expert_plan_ints(ntok * topk) int32),
@@ -276,9 +297,12 @@ qg_status qgemv_argmax_ids(qg_fmt fmt, const void* W_sub, int64_t n_sub, int64_t
  *   ZEROED by the caller once; each launch leaves it zeroed.  Launches sharing a
  *   workspace must be serialized (one stream).  After QG_DEVICE_WAIT_TIMEOUT,
  *   zero it again.
- *   The grid is one persistent wave (every CTA resident at once); the barriers'
- *   waits are bounded: if other work holds SMs long enough, the launch gives up with
- *   QG_DEVICE_WAIT_TIMEOUT instead of hanging.  Errors: QG_EINVAL (shapes,
+ *   The grid is one persistent wave, launched cooperatively: the driver starts it
+ *   only when every CTA can be resident at once (early start is added when enabled
+ *   and the driver accepts the pair; otherwise the launch is cooperative only).  The
+ *   barriers' waits stay bounded as a guard: should a wait run out, the launch sets
+ *   QG_DEVICE_WAIT_TIMEOUT and its y is not valid, so a caller that cannot rule that
+ *   out checks qg_device_status after the call.  Errors: QG_EINVAL (shapes,
  *   ntok * topk, null pointers), QG_EALIGN, QG_EWORKSPACE, QG_EUNSUPPORTED,
  *   QG_ECUDA; a routed id outside [0, n_experts) sets QG_DEVICE_BAD_PLAN and the
  *   launch computes nothing. */
@@ -306,7 +330,8 @@ qg_status qg_describe_expert_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, char*
  * 32 KiB + 16 bytes, present on every GPU that loads the library until the
  * process exits.  It allocates nothing and calls no allocating routine.
  *   - The first call on a device looks up that array's device address for the
- *     current device (a one-time set-up); make that first call before any
+ *     current device (a one-time set-up, repeated only if the device's context
+ *     changes, e.g. after cudaDeviceReset); make that first call before any
  *     stream capture.
  *   - Each call clears the ticket (cudaMemsetAsync on `stream`) before its
  *     kernel; the array otherwise keeps the last call's contents.
