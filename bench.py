@@ -555,6 +555,8 @@ def detail_table(args, qg, torch, dev, l2, peak, have=None):
         names = args.detail_only.split(",")
     else:
         names = [n for n in workloads.WORKLOADS if n not in HEADS]
+    expert_names = [n for n in names if n in workloads.EXPERT_LAYERS]
+    names = [n for n in names if n not in workloads.EXPERT_LAYERS]
     table = {}
     cache = {}
     have = have or {}
@@ -620,8 +622,8 @@ def detail_table(args, qg, torch, dev, l2, peak, have=None):
         del base
     cache.clear()
     torch.cuda.empty_cache()
-    if not args.detail_only or any(n in workloads.EXPERT_LAYERS for n in names):
-        for name in workloads.EXPERT_LAYERS:
+    if not args.detail_only or expert_names:
+        for name in (expert_names or workloads.EXPERT_LAYERS):
             table[name] = experts_detail(qg, torch, dev, peak, workloads.EXPERT_LAYERS[name])
             torch.cuda.empty_cache()
     return table

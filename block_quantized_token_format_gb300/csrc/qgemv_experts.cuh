@@ -131,7 +131,7 @@ __device__ __forceinline__ void expert_group(const ExpertArgs& a, Ring& R, unsig
                                              int first_block, int lane) {
     using F = Fmt<FMT>;
     constexpr int S = F::kW / 4;
-    constexpr int kCS = XT * S + 1;
+    constexpr int kCS = XT * x_slots(FMT) + x_pad_slots(FMT);
     constexpr int V = RPW * NE;
     constexpr int SPAN = 32 / Pow2Up<V>::value;
     constexpr int kStage = stage_bytes(FMT, RPW);

@@ -21,14 +21,21 @@
 //    read.  The bytes in flight per SM are set by shared memory, not by
 //    registers, and every weight byte is read exactly once.  One flat pipeline
 //    runs across row-group boundaries, so the copies never drain between groups.
-//  * Dequantization in registers without I2F: a code is placed in the
-//    mantissa of 2^23 (byte permute or mask) and the offset is removed with an
-//    exact packed FADD (add.rn.f32x2).  4-bit codes at nibble position 4m of a
-//    half-word come out as q*16^m; x is stored pre-multiplied by 16^-m (exact),
-//    so the products are q*x exactly.  Block scales are applied once per chunk.
-//    (A magic of 2^(23-4m) per nibble position would give q directly without
-//    the x pre-scale, but measured ~4% slower on the affine head: two more
-//    constant pairs and three more magic registers in the inner loop.)
+//  * Q8_0, BF16, Q5_0: dequantization in registers without I2F.  A code is
+//    placed in the mantissa of 2^23 (byte permute or mask) and the offset is
+//    removed with an exact packed FADD (add.rn.f32x2); Q5_0's codes at nibble
+//    position 4m come out as q*16^m and x is stored pre-multiplied by 16^-m
+//    (exact).  Block scales are applied once per chunk.
+//  * Q4_0 and affine 4-bit: integer chunk dots.  x is staged per 32-column chunk
+//    and token as 16-bit integers X = rn(x * 2^(14-k)) with 2^(k-1) <= max|x| <
+//    2^k (|X| <= 2^14, error <= 2^-14 of the chunk's largest |x|); a word of 8
+//    codes becomes two words of 4 bytes (one mask, one shift and mask), and
+//    dp2a (16-bit x 8-bit pairs into int32, exact) takes two products per
+//    instruction.  Per chunk one I2F (exact: |sum| < 2^24) and one FMA with
+//    scale * 2^(k-14).  On GB300 this issues about half the instructions of
+//    the magic-float decode with packed FMAs, whose issue cost binds the 4-bit
+//    formats at ntok 3-4 (measured: a register-only model of the inner loop
+//    reaches 27 weights/clk/SM at ntok 4 against 18 with packed FP32).
 //  * FP32 math in packed pairs: per (row, token) a pair of partial sums (even
 //    and odd columns) advanced by fma.rn.f32x2, added and scaled once per
 //    chunk.  On GB300 the packed FMA does not raise the FP32 rate, but it
@@ -197,6 +204,11 @@ __device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
     f2_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
@@ -207,6 +219,12 @@ __device__ __forceinline__ float f2_sum(f2_t a) {
     float x, y;
     asm("mov.b64 {%0,%1}, %2;" : "=f"(x), "=f"(y) : "l"(a));
     return __fadd_rn(x, y);
+}
+// One pair from shared memory.
+__device__ __forceinline__ f2_t lds_f2(uint32_t a) {
+    f2_t p;
+    asm volatile("ld.shared.b64 %0, [%1];" : "=l"(p) : "r"(a));
+    return p;
 }
 // Two consecutive pairs (four floats) from shared memory.
 __device__ __forceinline__ void lds_f2x2(uint32_t a, f2_t& p0, f2_t& p1) {
@@ -235,20 +253,13 @@ template <> struct Fmt<QG_Q8_0> {
     }
 };
 
+// Q4_0 and the affine format run the integer chunk dot (step_idp); their traits give the
+// chunk width and where the scales sit.
 template <> struct Fmt<QG_Q4_0> {
     static constexpr int kW = 32;
     static constexpr int kStepScale = 64;
     static __device__ __forceinline__ uint32_t scale_off(int j) { return 2u * uint32_t(j); }
     static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds16(a); }
-    // (2^23 + q*16^m) - (2^23 + 8*16^m) = (q - 8) * 16^m, exact.
-    static __device__ __forceinline__ void dec(const uint4& q, int i, f2_t& lo, f2_t& hi, uint32_t mg) {
-        const uint32_t w = (i >> 1) == 0 ? q.x : (i >> 1) == 1 ? q.y : (i >> 1) == 2 ? q.z : q.w;
-        const uint32_t h = (i & 1) ? (w >> 16) : w;
-        lo = f2_add(f2_pack(nib<0x000Fu>(h, mg), nib<0x00F0u>(h, mg)),
-                    f2_pack(__float_as_uint(-8388616.0f), __float_as_uint(-8388736.0f)));
-        hi = f2_add(f2_pack(nib<0x0F00u>(h, mg), nib<0xF000u>(h, mg)),
-                    f2_pack(__float_as_uint(-8390656.0f), __float_as_uint(-8421376.0f)));
-    }
 };
 
 template <> struct Fmt<QG_AFFINE4_G64> {
@@ -256,14 +267,6 @@ template <> struct Fmt<QG_AFFINE4_G64> {
     static constexpr int kStepScale = 64;
     static __device__ __forceinline__ uint32_t scale_off(int j) { return 4u * uint32_t(j >> 1); }
     static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds32(a); }
-    // (2^23 + q*16^m) - 2^23 = q * 16^m, exact.
-    static __device__ __forceinline__ void dec(const uint4& q, int i, f2_t& lo, f2_t& hi, uint32_t mg) {
-        const uint32_t w = (i >> 1) == 0 ? q.x : (i >> 1) == 1 ? q.y : (i >> 1) == 2 ? q.z : q.w;
-        const uint32_t h = (i & 1) ? (w >> 16) : w;
-        const f2_t m = f2_const(-8388608.0f);
-        lo = f2_add(f2_pack(nib<0x000Fu>(h, mg), nib<0x00F0u>(h, mg)), m);
-        hi = f2_add(f2_pack(nib<0x0F00u>(h, mg), nib<0xF000u>(h, mg)), m);
-    }
 };
 
 template <> struct Fmt<QG_BF16> {
@@ -312,6 +315,25 @@ template <> struct Fmt<QG_Q5_0> {
     }
 };
 
+// Formats that run the integer chunk dot (x staged as 16-bit integers).
+__host__ __device__ constexpr bool idp_format(int fmt) {
+    return fmt == QG_Q8_0 || fmt == QG_Q4_0 || fmt == QG_AFFINE4_G64;
+}
+template <int FMT> struct IsIdp { static constexpr bool value = idp_format(FMT); };
+
+// 16-byte slots of staged x per chunk and token: the chunk's columns as fp32 (BF16 8,
+// Q5_0 32 columns), or as 16-bit integers for the integer dot (Q8_0 16, Q4_0 and
+// affine 32 columns).
+__host__ __device__ constexpr int x_slots(int fmt) {
+    return fmt == QG_Q8_0 ? 2 : idp_format(fmt) ? 4 : fmt == QG_BF16 ? 2 : 8;
+}
+// Pad slots after a chunk's staged x.  Integer dot: slot 0 holds per token the chunk's
+// scale 2^(k-14), slot 1 per token the starting sum that removes the code offset
+// (Q8_0 -128 * sum(X), Q4_0 -8 * sum(X), int32) or the affine bias's sum(x) (fp32);
+// slot 2 pads the stride to an odd count.  Other formats: one slot (unused but for
+// the odd stride).
+__host__ __device__ constexpr int x_pad_slots(int fmt) { return idp_format(fmt) ? 3 : 1; }
+
 // ------------------------------------------------------------------------------ helpers
 
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
@@ -327,10 +349,10 @@ template <> struct Log2<1> { static constexpr int value = 0; };
 
 // Shared memory layout of one CTA (bytes): staged x, the warps' mbarriers, the
 // warps' rings.  x is stored chunk by chunk: for lane-chunk c, the NTOK*S float4
-// slots of its columns (token-major), then one pad slot that holds the chunk's
-// per-token sums of x (used by the affine format).  The chunk stride of
-// NTOK*S+1 slots is odd, so the 8 lanes of a 128-byte shared-memory phase hit 8
-// distinct 16-byte bank groups, and every load offset is a compile-time constant.
+// slots of its columns (token-major), then the pad slots (x_pad_slots).  The chunk
+// stride of NTOK*S + pad slots is odd, so the 8 lanes of a 128-byte shared-memory
+// phase hit 8 distinct 16-byte bank groups, and every load offset is a
+// compile-time constant.
 struct SmemPlan {
     int x_bytes, bar_off, tbar_off, xch_off, ring_off, total;
 };
@@ -348,12 +370,11 @@ __host__ __device__ constexpr int stage_bytes(int fmt, int rpw) { return (rpw * 
 __host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int rpw, int depth, int warps,
                                               int split) {
     SmemPlan p;
-    const int w = fmt == QG_Q8_0 ? 16 : fmt == QG_BF16 ? 8 : 32;
-    const int slots = w / 4;
+    const int slots = x_slots(fmt);
     const int teams = split > 1 ? warps / split : 0;
     // x holds whole steps of chunks (32 per step), zero past n_in.
     const int codes = fmt == QG_Q8_0 ? n_in : fmt == QG_BF16 ? 2 * n_in : n_in / 2;
-    p.x_bytes = (codes + 511) / 512 * 32 * (ntok * slots + 1) * 16;
+    p.x_bytes = (codes + 511) / 512 * 32 * (ntok * slots + x_pad_slots(fmt)) * 16;
     p.bar_off = (p.x_bytes + 15) / 16 * 16;
     p.tbar_off = p.bar_off + warps * depth * 8;
     p.xch_off = p.tbar_off + teams * 32;
@@ -380,13 +401,83 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
     // NC: x is read-only for the kernel's lifetime (non-coherent loads); otherwise x
     // was written earlier in this kernel by other CTAs (L2 loads).
     auto ld = [](const float4* p) { if constexpr (NC) return __ldg(p); else return __ldcg(p); };
-    constexpr int S = Fmt<FMT>::kW / 4;
-    constexpr int kCS = NTOK * S + 1;
+    constexpr int S = x_slots(FMT);
+    constexpr int kCS = NTOK * S + x_pad_slots(FMT);
     float4* xs = reinterpret_cast<float4*>(smem);
     const int n4 = n_in >> 2;
     const int nchunks = n_in / Fmt<FMT>::kW;
-    constexpr int kXG = NTOK >= 8 ? 1 : 8 / NTOK;   // float4 columns per thread and batch
     const int nt = int(blockDim.x);
+    if constexpr (IsIdp<FMT>::value) {
+        // One (chunk, token) pair per thread and pass: the chunk's values (32 columns, 16
+        // for Q8_0) are loaded at once; with m = max|x| over them and 2^(k-1) <= m < 2^k,
+        // X = rn(x * 2^(14-k)) (|X| <= 2^14) is formed exactly by one FMA with 1.5 * 2^23
+        // (the integer sits in the low bits of the sum, round to nearest even), and stored
+        // as the 16-bit pairs dp2a takes: per word of 8 nibble codes (x0|x2, x4|x6, x1|x3,
+        // x5|x7) against its even and odd codes, per word of 4 byte codes (x0|x1, x2|x3).  A chunk with m < 2^-113 is staged as zero (an
+        // absolute error below 2^-113); one with a NaN or an infinity gets a NaN scale.
+        constexpr int W = Fmt<FMT>::kW;                         // columns per chunk: 16 or 32
+        uint32_t* xu = reinterpret_cast<uint32_t*>(smem);
+        for (int idx = threadIdx.x; idx < live * nchunks; idx += nt) {
+            const int t = int(idx >= nchunks) + int(idx >= 2 * nchunks) + int(idx >= 3 * nchunks);
+            const int c = idx - t * nchunks;
+            const float4* rt = rows[0];
+#pragma unroll
+            for (int u = 1; u < NTOK; ++u) rt = (t == u) ? rows[u] : rt;
+            const float4* src = rt + (W / 4) * c;
+            float v[W];
+#pragma unroll
+            for (int q = 0; q < W / 4; ++q) {
+                const float4 f = ld(src + q);
+                v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
+            }
+            float m = 0.f, sx = 0.f;
+            bool finite = true;
+#pragma unroll
+            for (int i = 0; i < W; ++i) {
+                m = fmaxf(m, fabsf(v[i]));
+                sx = __fadd_rn(sx, v[i]);
+                finite = finite && (fabsf(v[i]) <= 3.402823466e38f);
+            }
+            const int e = int(__float_as_uint(m) >> 23);           // m in [2^(e-127), 2^(e-126))
+            const bool live_chunk = e >= 14;
+            // 2^(14-k) = 2^(140-e) and 2^(k-14) = 2^(e-140), k = e - 126, as float bits
+            const float up = live_chunk ? __uint_as_float(uint32_t(267 - e) << 23) : 0.f;
+            float down = live_chunk ? __uint_as_float(uint32_t(e - 13) << 23) : 0.f;
+            if (!finite) down = __uint_as_float(0x7FC00000u);
+            float y[W];
+            float sX = 0.f;
+#pragma unroll
+            for (int i = 0; i < W; ++i) {
+                y[i] = __fmaf_rn(v[i], up, 12582912.0f);            // 1.5 * 2^23 + X
+                sX = __fadd_rn(sX, __fsub_rn(y[i], 12582912.0f));   // sum of X, exact
+            }
+            uint32_t* dst = xu + (c * kCS + t * S) * 4;
+            if constexpr (FMT == QG_Q8_0) {
+                // byte codes: the pairs in column order, (x0|x1, x2|x3) per word of 4 codes
+#pragma unroll
+                for (int j = 0; j < W / 2; ++j)
+                    dst[j] = __byte_perm(__float_as_uint(y[2 * j]), __float_as_uint(y[2 * j + 1]), 0x5410);
+            } else {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float* yw = y + 8 * w;
+                    dst[4 * w + 0] = __byte_perm(__float_as_uint(yw[0]), __float_as_uint(yw[2]), 0x5410);
+                    dst[4 * w + 1] = __byte_perm(__float_as_uint(yw[4]), __float_as_uint(yw[6]), 0x5410);
+                    dst[4 * w + 2] = __byte_perm(__float_as_uint(yw[1]), __float_as_uint(yw[3]), 0x5410);
+                    dst[4 * w + 3] = __byte_perm(__float_as_uint(yw[5]), __float_as_uint(yw[7]), 0x5410);
+                }
+            }
+            uint32_t* pad = xu + (c * kCS + NTOK * S) * 4;
+            pad[t] = __float_as_uint(down);
+            if constexpr (FMT == QG_Q8_0) pad[4 + t] = uint32_t(-128 * int(sX));
+            else if constexpr (FMT == QG_Q4_0) pad[4 + t] = uint32_t(-8 * int(sX));
+            else pad[4 + t] = __float_as_uint(sx);
+        }
+        for (int i = nchunks * kCS + int(threadIdx.x); i < spr * 32 * kCS; i += int(blockDim.x))
+            xs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    constexpr int kXG = NTOK >= 8 ? 1 : 8 / NTOK;   // float4 columns per thread and batch
     for (int g0 = threadIdx.x; g0 < n4; g0 += kXG * nt) {
         float4 v[kXG][NTOK];
 #pragma unroll
@@ -405,7 +496,7 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
                 for (int t = 0; t < NTOK; ++t) {
                     if (t >= live) break;
                     float4 w = v[j][t];
-                    if constexpr (FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64 || FMT == QG_Q5_0) {
+                    if constexpr (FMT == QG_Q5_0) {
                         // column j is used as q*16^(j%4): store x * 16^-(j%4) (exact)
                         w.y *= 0.0625f;
                         w.z *= 0.00390625f;
@@ -416,33 +507,13 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
             }
         }
     }
-    if constexpr (FMT == QG_AFFINE4_G64) {
-        float* xf = reinterpret_cast<float*>(smem);
-        for (int c = threadIdx.x; c < nchunks; c += blockDim.x) {   // (padding chunks stay 0)
-#pragma unroll 1
-            for (int t = 0; t < live; ++t) {
-                // rows[t] by selects (a rolled loop must not index the array: that
-                // would put it in local memory)
-                const float4* rt = rows[0];
-#pragma unroll
-                for (int u = 1; u < NTOK; ++u) rt = (t == u) ? rows[u] : rt;
-                const float4* src = rt + S * c;
-                float sum = 0.f;
-#pragma unroll
-                for (int q = 0; q < S; ++q) {
-                    const float4 v = ld(src + q);
-                    sum = __fadd_rn(sum, v.x); sum = __fadd_rn(sum, v.y);
-                    sum = __fadd_rn(sum, v.z); sum = __fadd_rn(sum, v.w);
-                }
-                xf[(c * kCS + NTOK * S) * 4 + t] = sum;
-            }
-        }
-    }
     // Chunks past n_in (the lanes past a row's short last step) read as zero.
     for (int i = nchunks * kCS + int(threadIdx.x); i < spr * 32 * kCS; i += int(blockDim.x))
         xs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// A lane's accumulators for one row group: per (row, token) one fp32 sum of scaled
+// chunk sums, or (BF16, no scales) a pair of partial sums over the whole row.
 // A lane's accumulators for one row group: per (row, token) one fp32 sum of scaled
 // chunk sums, or (BF16, no scales) a pair of partial sums over the whole row.
 template <int FMT, int NTOK, int RPW> struct Acc {
@@ -471,11 +542,11 @@ template <int FMT, int NTOK, int RPW> struct Acc {
 // step), the lane's staged x chunk at `xr` (a layout for XT >= NTOK tokens; tokens
 // 0..NTOK-1 are used).  Within the chunk a pair of partial sums (even / odd columns)
 // per (row, token) is advanced by packed FMAs, then added and scaled once.
-template <int FMT, int NTOK, int RPW, int XT = NTOK>
-__device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uint32_t codes, uint32_t scales,
-                                         uint32_t magic) {
+template <int FMT, int NTOK, int RPW, int XT>
+__device__ __forceinline__ void step_fp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uint32_t codes, uint32_t scales,
+                                        uint32_t magic) {
     using F = Fmt<FMT>;
-    constexpr int S = F::kW / 4;
+    constexpr int S = x_slots(FMT);
     constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
     constexpr bool kPairAcc = Acc<FMT, NTOK, RPW>::kPair;
     uint4 qv[RPW];
@@ -512,7 +583,7 @@ __device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
             }
         }
     }
-    if constexpr (FMT == QG_Q8_0 || FMT == QG_Q4_0 || FMT == QG_Q5_0) {
+    if constexpr (FMT == QG_Q8_0 || FMT == QG_Q5_0) {
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             const float d = h2f(sv[r]);
@@ -520,21 +591,117 @@ __device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
             for (int t = 0; t < NTOK; ++t)
                 A.s[r][t] = __fmaf_rn(d, f2_sum(p[r][t]), A.s[r][t]);
         }
-    } else if constexpr (FMT == QG_AFFINE4_G64) {
-        float csv[4];
-        {
-            const uint4 cv = lds128(xr + 16u * uint32_t(XT * S));
-            csv[0] = __uint_as_float(cv.x); csv[1] = __uint_as_float(cv.y);
-            csv[2] = __uint_as_float(cv.z); csv[3] = __uint_as_float(cv.w);
-        }
+    }
+}
+
+// Integer chunk dot (Q8_0, Q4_0, affine).  Q4_0 / affine: the lane's 16-byte chunk of
+// each of the RPW rows is 4 words of 8 codes; a word gives its even codes as 4 bytes
+// (w & 0x0F0F0F0F) and its odd codes (w >> 4 & 0x0F0F0F0F), and per token four dp2a add
+// the 8 products of the word's staged 16-bit x pairs into an int32 (exact).  Q8_0: the
+// chunk is 16 byte codes q + 128, taken by dp2a as they are.  The sums start at
+// -128 * sum(X) (Q8_0) or -8 * sum(X) (Q4_0), which removes the code offset exactly;
+// the chunk then adds (I2F(sum) * 2^(k-14)) * d, and the affine format also
+// b * sum(x).  (|sum| < 2^24 for the 4-bit formats, so the I2F is exact; a Q8_0 chunk
+// sum can reach 2^25 and then rounds to 24 bits.)  The order of additions is fixed per
+// lane and chunk.
+__device__ __forceinline__ int dp2a_lo(uint32_t x, uint32_t q, int c) {
+    int d;
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(q), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t x, uint32_t q, int c) {
+    int d;
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(q), "r"(c));
+    return d;
+}
+
+template <int FMT, int NTOK, int RPW, int XT>
+__device__ __forceinline__ void step_idp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uint32_t codes, uint32_t scales) {
+    using F = Fmt<FMT>;
+    constexpr int S = x_slots(FMT);
+    constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
+    uint4 qv[RPW];
+    uint32_t sv[RPW];
 #pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            const float s = h2f(sv[r] & 0xFFFFu), b = h2f(sv[r] >> 16);
+    for (int r = 0; r < RPW; ++r) {
+        qv[r] = lds128(codes + r * kFullStep);
+        sv[r] = F::scale(scales + r * kFullStep);
+    }
+    const uint4 pk = lds128(xr + 16u * uint32_t(XT * S));         // 2^(k-14) per token
+    const uint4 pb = lds128(xr + 16u * uint32_t(XT * S + 1));     // Q4_0: -8 sum(X); affine: sum(x)
+    const uint32_t pkv[4] = {pk.x, pk.y, pk.z, pk.w};
+    const uint32_t pbv[4] = {pb.x, pb.y, pb.z, pb.w};
+    int acc[RPW][NTOK];
 #pragma unroll
-            for (int t = 0; t < NTOK; ++t)
-                A.s[r][t] = __fmaf_rn(s, f2_sum(p[r][t]), __fmaf_rn(b, csv[t], A.s[r][t]));
+    for (int r = 0; r < RPW; ++r)
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t) acc[r][t] = FMT == QG_AFFINE4_G64 ? 0 : int(pbv[t]);
+    if constexpr (FMT == QG_Q8_0) {
+        // 16 byte codes (q + 128) per row: slot j of staged x holds the pairs of words
+        // 2j and 2j + 1; dp2a.lo takes a word's bytes 0-1, dp2a.hi its bytes 2-3.
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            uint4 xv[NTOK];
+#pragma unroll
+            for (int t = 0; t < NTOK; ++t) xv[t] = lds128(xr + 16u * uint32_t(t * S + j));
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const uint32_t w0 = j == 0 ? qv[r].x : qv[r].z, w1 = j == 0 ? qv[r].y : qv[r].w;
+#pragma unroll
+                for (int t = 0; t < NTOK; ++t) {
+                    int a = acc[r][t];
+                    a = dp2a_lo(xv[t].x, w0, a);
+                    a = dp2a_hi(xv[t].y, w0, a);
+                    a = dp2a_lo(xv[t].z, w1, a);
+                    a = dp2a_hi(xv[t].w, w1, a);
+                    acc[r][t] = a;
+                }
+            }
         }
     }
+#pragma unroll
+    for (int j = 0; j < (FMT == QG_Q8_0 ? 0 : 4); ++j) {
+        uint4 xv[NTOK];
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t) xv[t] = lds128(xr + 16u * uint32_t(t * S + j));
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const uint32_t w = j == 0 ? qv[r].x : j == 1 ? qv[r].y : j == 2 ? qv[r].z : qv[r].w;
+            const uint32_t ev = w & 0x0F0F0F0Fu, od = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+            for (int t = 0; t < NTOK; ++t) {
+                int a = acc[r][t];
+                a = dp2a_lo(xv[t].x, ev, a);
+                a = dp2a_hi(xv[t].y, ev, a);
+                a = dp2a_lo(xv[t].z, od, a);
+                a = dp2a_hi(xv[t].w, od, a);
+                acc[r][t] = a;
+            }
+        }
+    }
+    // Per token: (affine) A += b * sum(x); then A += (I2F(sum) * 2^(k-14)) * scale (the
+    // product with the power of two is exact).
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        const float sc = FMT == QG_AFFINE4_G64 ? h2f(sv[r] & 0xFFFFu) : h2f(sv[r]);
+        if constexpr (FMT == QG_AFFINE4_G64) {
+            const float b = h2f(sv[r] >> 16);
+#pragma unroll
+            for (int t = 0; t < NTOK; ++t) A.s[r][t] = __fmaf_rn(b, __uint_as_float(pbv[t]), A.s[r][t]);
+        }
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t)
+            A.s[r][t] = __fmaf_rn(__fmul_rn(__int2float_rn(acc[r][t]), __uint_as_float(pkv[t])), sc, A.s[r][t]);
+    }
+}
+
+// One ring stage into the accumulators: the integer chunk dot for Q4_0 and the affine
+// format, the magic-float decode with packed FMAs otherwise.
+template <int FMT, int NTOK, int RPW, int XT = NTOK>
+__device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uint32_t codes, uint32_t scales,
+                                         uint32_t magic) {
+    if constexpr (IsIdp<FMT>::value) step_idp<FMT, NTOK, RPW, XT>(A, xr, codes, scales);
+    else step_fp<FMT, NTOK, RPW, XT>(A, xr, codes, scales, magic);
 }
 
 // Transposed warp reduction of the V = RPW * NTOK lane sums (reduce-scatter by
@@ -573,7 +740,7 @@ __device__ __forceinline__ float warp_reduce(const Acc<FMT, NTOK, RPW>& A, int l
 // thread may hold up to 168 registers instead of 128 and the extra rows'
 // accumulators do not spill.  Kernels that fit in 128 keep 16 warps.
 template <int FMT, int NTOK, int RPW> struct MaxThreads {
-    static constexpr bool kFourBit = FMT == QG_Q4_0 || FMT == QG_AFFINE4_G64 || FMT == QG_Q5_0;
+    static constexpr bool kFourBit = FMT == QG_Q5_0;
     static constexpr int value = (RPW * NTOK > 20 || (kFourBit && RPW * NTOK >= 16 && NTOK >= 2)) ? 384 : 512;
 };
 
@@ -618,7 +785,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
     const int GW = gridDim.x * nteams;
     const int ngroups = (a.n_out + RPW - 1) / RPW;
 
-    constexpr int kCS = NTOK * S + 1;               // float4 slots per chunk in staged x
+    constexpr int kCS = NTOK * x_slots(FMT) + x_pad_slots(FMT);   // 16-byte slots per chunk of staged x
     const SmemPlan plan = smem_plan(FMT, NTOK, n_in, RPW, depth, nwarps, P);
     const uint32_t xs_base = smem_addr(smem);
     const uint32_t bars = smem_addr(smem + plan.bar_off) + warp * depth * 8;

@@ -63,20 +63,22 @@ const Entry kTable[] = {
     {QG_Q8_0, 1, 4095, 2560, 0, {2, 2, 12, 1}},
     // Q8_0, n_in 6144, few rows (6144 -> 2560; split 3: 15 warps = 5 teams)
     {QG_Q8_0, 1, 8191, 6144, 0, {4, 2, 16, 1}},
-    // Q4_0 and BF16, 8192 x 2560
-    {QG_Q4_0, 4096, 65535, 2560, 1, {4, 2, 12, 2}},
+    // Q4_0 (integer chunk dot) and BF16, 8192 x 2560
+    {QG_Q4_0, 4096, 65535, 2560, 1, {8, 2, 8, 2}},
     {QG_Q4_0, 4096, 65535, 2560, 2, {8, 2, 6, 2}},
-    {QG_Q4_0, 4096, 65535, 2560, 3, {8, 2, 6, 2}},
+    {QG_Q4_0, 4096, 65535, 2560, 3, {8, 2, 8, 1}},
     {QG_Q4_0, 4096, 65535, 2560, 4, {5, 2, 16, 1}},
     {QG_BF16, 4096, 65535, 2560, 1, {4, 5, 8, 2}},
     {QG_BF16, 4096, 65535, 2560, 2, {4, 5, 8, 2}},
     {QG_BF16, 4096, 65535, 2560, 3, {4, 3, 16, 1}},
     {QG_BF16, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
-    // Q5_0, 8192 x 2560 (measured; ntok 2 and 4 fall through to Q4_0's entries)
+    // Q5_0, 8192 x 2560 (magic-float decode; measured)
     {QG_Q5_0, 4096, 65535, 2560, 1, {2, 3, 16, 1}},
+    {QG_Q5_0, 4096, 65535, 2560, 2, {8, 2, 6, 2}},
     {QG_Q5_0, 4096, 65535, 2560, 3, {2, 3, 16, 1}},
-    // affine 4-bit LM head
-    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {8, 2, 16, 1}},
+    {QG_Q5_0, 4096, 65535, 2560, 4, {5, 2, 12, 1}},
+    // affine 4-bit LM head (integer chunk dot)
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {8, 2, 12, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {8, 2, 12, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 3, {8, 2, 12, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 4, {6, 2, 12, 1}},
@@ -92,9 +94,7 @@ Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
         if (e.ntok && e.ntok != ntok) continue;
         return e.tile;
     }
-    // Q5_0 streams Q4_0's code layout plus 6 bytes per block and decodes the same way
-    // (one more bit per element): where it has no entry of its own it takes Q4_0's.
-    if (fmt == QG_Q5_0) return select_tile(QG_Q4_0, n_out, n_in, ntok);
+
     // Heuristic for unmeasured shapes: many rows stream 4 per warp (8 at ntok 1) in
     // one 12- or 16-warp CTA per SM with a shallow ring; few rows use 2 rows per warp
     // so that the row groups still spread over every SM.

@@ -139,7 +139,8 @@ qg_status qg_pack(qg_fmt fmt, const float* W_host, int64_t n_out, int64_t n_in,
  *   y     device, fp32 [ntok][n_out] row-major, 4-B aligned; fully overwritten.
  *   ntok  1..4.   n_out >= 1.   n_in a positive multiple of the block (as above)
  *         and small enough that ntok*n_in fp32 values fit in one SM's shared
- *         memory (QG_EUNSUPPORTED otherwise; n_in <= 12288 always fits at ntok 4).
+ *         memory (QG_EUNSUPPORTED otherwise; n_in <= 12288 always fits at ntok 4, and
+ *         16384 for Q8_0, Q4_0 and AFFINE4_G64, whose x is staged as 16-bit integers).
  * Each output is an fp32 sum over n_in whose order depends only on the matrix
  * (fmt, n_out, n_in; see the split under tile selection): row t of an ntok=k
  * call is bitwise equal to the ntok=1 call on x[t], for every geometry, grid

@@ -1,12 +1,20 @@
 """The kernels' in-register decode, emulated bit for bit on the CPU (no GPU): for every
-format, the packer's device bytes are turned into fp32 values the way the kernels do
-it — a code placed in the mantissa of the magic float 2^23 (byte permute or nibble
-mask), the offset removed by one fp32 subtraction, Q5_0's fifth bit merged from the
-rotated record word, BF16 widened by a shift — and scaled by the block scale.  Every
-value must equal the oracle's fp64 dequantization exactly: this pins the claim that
-the decode is exact and that the kernels' view of the device layout matches the
-packer's, before any GPU run.  The magic constants are restated here from the
-decode's arithmetic (2^23 = 8388608), not taken from the kernel sources."""
+format, the packer's device bytes are turned into values the way the kernels do it —
+for Q5_0 a code placed in the mantissa of the magic float 2^23 (nibble mask), its fifth
+bit merged from the rotated record word, the offset removed by one fp32 subtraction;
+BF16 widened by a shift; for the integer chunk dot, Q8_0's bytes q + 128 as they are
+(the offset removed through the chunk's starting sum) and a Q4_0 / affine word's even
+and odd codes taken as bytes (one mask, one shift and mask) — and scaled by the block
+scale.  Every value must equal the oracle's fp64
+dequantization exactly: this pins the claim that the decode is exact and that the
+kernels' view of the device layout matches the packer's, before any GPU run.  The
+magic constants are restated here from the decode's arithmetic (2^23 = 8388608), not
+taken from the kernel sources.
+
+The integer chunk dot also rounds x: per 32-column chunk and token, X = rn(x * 2^(14-k))
+with 2^(k-1) <= max|x| < 2^k.  test_x_rounding_bound pins the stated bound of that
+rounding (|X| <= 2^14, |x - X * 2^(k-14)| <= 2^-14 max|x|, the chunk sums of X exact in
+int32 and their I2F exact) on random and adversarial chunks, written from the rule."""
 from __future__ import annotations
 
 import numpy as np
@@ -39,10 +47,14 @@ def emulate_row(fmt, codes, scales, n_in):
         hi = (w & np.uint32(0xFFFF0000)).astype(np.uint32)     # element 2k + 1
         return np.stack([_f32(lo), _f32(hi)], axis=1).reshape(-1).astype(np.float64)
     if fmt == "q8_0":
-        f = _f32(MAGIC | codes.astype(np.uint32)) - (TWO23 + np.float32(128))   # q, exact
-        d = scales.copy().view("<f2").astype(np.float32)
-        return (f.reshape(-1, 32) * d[:, None]).reshape(-1).astype(np.float64)
+        # integer chunk dot: the byte u = q + 128 enters dp2a as it is; the chunk's
+        # starting sum -128 * sum(X) removes the offset, so the code is u - 128, exact
+        q = codes.astype(np.int64) - 128
+        d = scales.copy().view("<f2").astype(np.float64)
+        return (q.reshape(-1, 32) * d[:, None]).reshape(-1).astype(np.float64)
     words = codes.copy().view("<u4").reshape(-1, 4)            # one 16-byte lane chunk per row
+    if fmt in ("q4_0", "affine4_g64"):
+        return emulate_bytes(fmt, words, scales)
     out = np.empty((words.shape[0], 32), dtype=np.float64)
     if fmt == "q5_0":
         rec = scales.reshape(-1, 6)
@@ -67,6 +79,64 @@ def emulate_row(fmt, codes, scales, n_in):
         return (q.reshape(-1, 32) * d5[:, None]).reshape(-1)
     sb = scales.copy().view("<f2").astype(np.float64).reshape(-1, 2)
     return (q.reshape(-1, 64) * sb[:, 0:1] + sb[:, 1:2]).reshape(-1)
+
+
+def emulate_bytes(fmt, words, scales):
+    """Q4_0 / affine: word w of a lane chunk gives its even codes as the 4 bytes of
+    w & 0x0F0F0F0F and its odd codes as those of (w >> 4) & 0x0F0F0F0F; byte b of the
+    even word is element 2b, of the odd word element 2b + 1."""
+    q = np.empty((words.shape[0], 32), dtype=np.float64)
+    for j in range(4):
+        w = words[:, j]
+        ev = w & np.uint32(0x0F0F0F0F)
+        od = (w >> np.uint32(4)) & np.uint32(0x0F0F0F0F)
+        for b in range(4):
+            q[:, 8 * j + 2 * b] = ((ev >> np.uint32(8 * b)) & np.uint32(0xFF)).astype(np.float64)
+            q[:, 8 * j + 2 * b + 1] = ((od >> np.uint32(8 * b)) & np.uint32(0xFF)).astype(np.float64)
+    q = q.reshape(-1)
+    if fmt == "q4_0":
+        d = scales.copy().view("<f2").astype(np.float64)
+        return ((q.reshape(-1, 32) - 8) * d[:, None]).reshape(-1)
+    sb = scales.copy().view("<f2").astype(np.float64).reshape(-1, 2)
+    return (q.reshape(-1, 64) * sb[:, 0:1] + sb[:, 1:2]).reshape(-1)
+
+
+def _round_chunk(x):
+    """The staging rule for one chunk of fp32 x: (X, 2^(k-14)), or zeros for a chunk whose
+    largest |x| is below 2^-113."""
+    x = np.asarray(x, dtype=np.float32)
+    m = np.float32(np.max(np.abs(x)))
+    e = int(m.view(np.uint32) >> 23)
+    if e < 14:
+        return np.zeros(x.shape, dtype=np.int64), 0.0
+    k = e - 126
+    X = np.rint(x.astype(np.float64) * 2.0 ** (14 - k)).astype(np.int64)     # round half even
+    return X, 2.0 ** (k - 14)
+
+
+def test_x_rounding_bound():
+    rng = np.random.default_rng(5)
+    chunks = [rng.standard_normal(32).astype(np.float32) for _ in range(2000)]
+    chunks += [np.float32(2.0) ** rng.integers(-60, 60) * rng.standard_normal(32).astype(np.float32)
+               for _ in range(500)]
+    ch = rng.standard_normal(32).astype(np.float32) * np.float32(1e-3)
+    ch[7] = np.float32(1000.0)                                  # one outlier per chunk
+    chunks.append(ch)
+    chunks.append(np.full(32, np.float32(np.nextafter(np.float32(4.0), np.float32(0)))))   # max just below 2^k
+    chunks.append(np.full(32, np.float32(-4.0)))                                             # max exactly 2^(k-1)
+    chunks.append(np.zeros(32, dtype=np.float32))
+    chunks.append(np.full(32, np.float32(1e-35)))                                            # below 2^-113: zero
+    for x in chunks:
+        X, scale = _round_chunk(x)
+        m = float(np.max(np.abs(x.astype(np.float64))))
+        assert np.all(np.abs(X) <= 2 ** 14)
+        err = np.abs(x.astype(np.float64) - X * scale)
+        assert np.all(err <= 2.0 ** -14 * m + (m if scale == 0.0 else 0.0)), (float(err.max()), m)
+        if scale == 0.0:
+            assert m < 2.0 ** -113
+        # chunk sums against 4-bit codes are exact in int32 and in the I2F to fp32
+        s = int(np.sum(15 * np.abs(X)))
+        assert s < 2 ** 24 and float(np.float32(s)) == s
 
 
 @pytest.mark.parametrize("fmt", ["q8_0", "q4_0", "affine4_g64", "bf16", "q5_0"])

@@ -258,12 +258,21 @@ def test_largest_n_in_and_unsupported():
         canon = ORC.quantize(fmt, W)
         y = gpu_qgemv(fmt, upload(fmt, canon, n_out, n_in), n_out, n_in, x)
         check_close(y, ORC.gemv(fmt, canon, n_out, n_in, x), ORC.gemv_abs(fmt, canon, n_out, n_in, x), fmt)
-    # x for ntok=4 at n_in = 16384 does not fit in shared memory: refused, nothing launched
-    big = torch.zeros(qg.qg_packed_bytes("q8_0", 4, 16384), dtype=torch.uint8, device=dev())
-    xd = torch.zeros((4, 16384), dtype=torch.float32, device=dev())
+    # the integer chunk dot stages x as 16-bit integers: n_in 16384 fits at ntok 4 for
+    # Q8_0, Q4_0 and the affine format
+    for fmt in ("q8_0", "q4_0", "affine4_g64"):
+        n_in = 16384
+        W = workloads.gaussian(13, (n_out, n_in), 0.02)
+        x = workloads.gaussian(14, (4, n_in))
+        canon = ORC.quantize(fmt, W)
+        y = gpu_qgemv(fmt, upload(fmt, canon, n_out, n_in), n_out, n_in, x)
+        check_close(y, ORC.gemv(fmt, canon, n_out, n_in, x), ORC.gemv_abs(fmt, canon, n_out, n_in, x), fmt)
+    # x for ntok=4 at n_in = 32768 does not fit in shared memory: refused, nothing launched
+    big = torch.zeros(qg.qg_packed_bytes("q8_0", 4, 32768), dtype=torch.uint8, device=dev())
+    xd = torch.zeros((4, 32768), dtype=torch.float32, device=dev())
     yd = torch.zeros((4, 4), dtype=torch.float32, device=dev())
     with pytest.raises(qg.QGError) as e:
-        qg.qgemv("q8_0", big, 4, 16384, xd, yd, 4)
+        qg.qgemv("q8_0", big, 4, 32768, xd, yd, 4)
     assert e.value.status == -3
 
 
