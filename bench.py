@@ -12,7 +12,8 @@ covers a real interval.  Also reported, outside the timed region:
 
 * config.per_config: every (head, ntok) launch alone and the 2560->12288
   projection (the largest shapes), with GB/s, the fraction of the measured copy
-  peak and, for the 4-bit head, the fraction of the FP32 FMA pipe's peak;
+  peak and, for the 4-bit head, the products per second against the FMA pipe's
+  128 products per clock per SM;
 * per_workload: every other workload family x ntok, median of 5 graph replays of
   50 launches rotating over weight copies totalling >= 4x L2;
 * e2e: the same step through the public API with host buffers, per call
@@ -51,7 +52,8 @@ LARGEST = HEADS + ["q8_0_12288x2560"]      # the shapes the >= 70% / >= 60% targ
 NTOKS = (1, 2, 3, 4)
 PEAK_FALLBACK_GBS = 6800.0
 MIN_TIMED_S = 1.0                          # timed blocks of K steps are repeated up to this
-FMA_LANES_PER_CLK_SM = 128                 # FP32 FMA pipe, lane-ops per clock per SM (GB300)
+FMA_LANES_PER_CLK_SM = 128                 # products per clock per SM of the FMA pipe on GB300
+                                           # (fma.rn.f32x2 or dp2a: 64 lane-instructions x 2)
 
 
 def parse_args():
@@ -70,6 +72,8 @@ def parse_args():
     p.add_argument("--one", default="", help="fmt,n_out,n_in,ntok[,tile spec]: run one shape 3 times "
                                              "(a small case for ncu) and exit")
     p.add_argument("--one-argmax", default="", help="as --one, through qgemv_argmax (the LM-head call)")
+    p.add_argument("--profile-step", type=int, default=0, help="run the headline step (8 launches) this many "
+                   "times after one warm-up step, eagerly with early start, and exit (for ncu launch lists)")
     p.add_argument("--sweep", default="", help="comma list of workload names: time every tile spec of "
                    "--sweep-specs (';'-separated, qg_set_tile_override grammar; default a grid) at "
                    "--sweep-ntoks, one JSON line per point to --sweep-out, the best per (workload, ntok) "
@@ -464,7 +468,8 @@ def main_gpu(args, rank, world, local_rank):
                 "kernel": "qgemv_kernel (all 8 launches of the step: 2 heads x ntok 1..4)",
                 "algorithmic_bytes_per_launch": round(step_algo / launches_per_step),
                 "avg_launch_us": round(ms_per_step / launches_per_step * 1e3, 3), "peak_kind": peak_kind,
-                "secondary": {"bound": "fp32 fma pipe (4-bit head at ntok 3-4)",
+                "secondary": {"bound": "FMA pipe products (dp2a / fma.rn.f32x2, 128 per clock per SM), "
+                                       "4-bit head at ntok 3-4",
                               "peak_fma_per_s": FMA_LANES_PER_CLK_SM * sms * sm_mhz * 1e6,
                               "fma_frac": {t: aff[t]["fma_frac"] for t in ("3", "4")}}}
 
@@ -895,6 +900,31 @@ def one_shape(spec: str, argmax: bool = False):
     print("ok", qg.qg_describe_tile(fmt, n_out, n_in, ntok))
 
 
+def profile_step(n: int):
+    """The headline step's 8 qgemv_argmax launches (both heads, ntok 1..4), one warm-up
+    step then n steps, eagerly with early start: a bounded case for ncu launch lists
+    and DRAM-traffic captures of the step's kernels."""
+    import torch
+    import block_quantized_token_format_gb300 as qg
+    import __graft_entry__
+    __graft_entry__.build()
+    heads = [workloads.WORKLOADS[n_] for n_ in HEADS]
+    W = {w.name: torch.from_numpy(gen_packed(qg, w)).cuda() for w in heads}
+    X = {w.name: torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).cuda() for w in heads}
+    Y = {w.name: torch.empty((4, w.n_out), device="cuda") for w in heads}
+    am = torch.empty(4, dtype=torch.int32, device="cuda")
+    ws = {w.name: torch.zeros(qg.qgemv_argmax_workspace_bytes(w.n_out, 4), dtype=torch.uint8, device="cuda")
+          for w in heads}
+    qg.qg_set_launch_options(qg.QG_LAUNCH_EARLY_START)
+    for _ in range(1 + n):
+        for ntok in NTOKS:
+            for w in heads:
+                qg.qgemv_argmax(w.fmt, W[w.name], w.n_out, w.n_in, X[w.name], Y[w.name][:ntok], am, ws[w.name], ntok)
+    torch.cuda.synchronize()
+    assert qg.qg_device_status() == 0
+    print("ok", 8 * (1 + n), "launches")
+
+
 def one_experts(spec: str, one_launch: bool = False):
     """Five routed-expert layers (plan, gate/up with the activation and the down
     prefetch, down; or, with one_launch, qgemv_expert_layer) at `ntok` on a 64-expert
@@ -954,6 +984,9 @@ def main():
         return
     if args.one_argmax:
         one_shape(args.one_argmax.replace(";", ","), argmax=True)
+        return
+    if args.profile_step:
+        profile_step(args.profile_step)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

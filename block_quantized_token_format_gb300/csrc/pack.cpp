@@ -154,14 +154,15 @@ void quant_row_bf16(const float* w, int64_t n_in, uint8_t* out) {
 // Canonical row pointers (affine has three planes).
 struct CanonRow { const uint8_t* a; const uint8_t* s; const uint8_t* b; };
 
-// Q5_0 device record: the fifth bit of element e = 4i + m of a block (i = 0..7, m =
-// 0..3) sits at bit (4m + 4 + r_i) mod 32 of the record's word, r_i = i for i < 4 and
-// i + 12 for i >= 4.  Rotating the word right by r_i then puts the fifth bits of
-// elements 4i..4i+3 at bits 4, 8, 12, 16, one place above each element's nibble as
-// the decoder lays them out; the 32 positions are distinct.
+// Q5_0 device record: the fifth bit of element e of a block sits at bit 8b + g of the
+// record's word, where g = 2 * (e / 8) + (e % 2) numbers the block's 8 groups of 4
+// elements (the even or the odd elements of each 8-element code word) and b = (e % 8) / 2
+// is the element's place in its group.  Shifting the word left by 4 - g (right by g - 4)
+// and masking with 0x10101010 puts the group's 4 fifth bits at bit 4 of the 4 bytes that
+// hold the group's codes in the kernels' integer decode; the 32 positions are distinct.
 int q5_fifth_bit_pos(int e) {
-    const int i = e >> 2, m = e & 3;
-    return (4 * m + 4 + (i < 4 ? i : i + 12)) & 31;
+    const int g = 2 * (e >> 3) + (e & 1), b = (e & 7) >> 1;
+    return 8 * b + g;
 }
 
 // The row's codes (device byte / nibble order) followed by all its scales.
@@ -200,7 +201,7 @@ void flat_device_row(int fmt, CanonRow c, int64_t n_in, uint8_t* dst) {
             break;
         case QG_Q5_0:
             // codes: the low nibbles as Q4_0's words; scales: per block its fifth bits
-            // (a uint32 in the rotated order of q5_fifth_bit_pos) and then its fp16 d, 6 bytes.
+            // (a uint32 in the order of q5_fifth_bit_pos) and then its fp16 d, 6 bytes.
             for (int64_t b = 0; b < n_in / 32; ++b) {
                 const uint8_t* blk = c.a + 22 * b;
                 const uint32_t qh = uint32_t(blk[2]) | uint32_t(blk[3]) << 8 | uint32_t(blk[4]) << 16 |

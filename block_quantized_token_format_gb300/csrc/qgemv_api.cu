@@ -338,7 +338,6 @@ qg_status fill_common(KernelArgs& a, const Plan& p, int fmt, const void* W, int6
     a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
     a.drain_limit = std::max<uint32_t>(a.wait_limit, 1u << 16);
     a.test_extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
-    a.fmagic = 0x4B000000u;
     a.stage_tx = uint32_t(p.tile.rpw * full_step_bytes(fmt));
     return QG_OK;
 }

@@ -270,7 +270,6 @@ qg_status qgemv_experts(qg_fmt fmt, const void* W, int64_t n_experts, int64_t n_
     a.wait_limit = wait_limit();
     a.drain_limit = std::max<uint32_t>(a.wait_limit, 1u << 16);
     a.test_extra_tx = test_extra_tx();
-    a.fmagic = 0x4B000000u;
     a.stage_tx = uint32_t(p.tile.rpw * full_step_bytes(fmt));
     a.next_w = static_cast<const unsigned char*>(W_next);
     a.next_bytes = W_next ? (long long)(next_n_out * row_stride(fmt, next_n_in)) : 0;
@@ -337,7 +336,6 @@ qg_status qgemv_expert_layer(qg_fmt fmt, const void* W_gate_up, const void* W_do
         a->wait_limit = wl;
         a->drain_limit = std::max<uint32_t>(wl, 1u << 16);
         a->test_extra_tx = test_extra_tx();
-        a->fmagic = 0x4B000000u;
         a->stage_tx = uint32_t(t.rpw * full_step_bytes(fmt));
     }
     L.gu.x = x;

@@ -71,7 +71,7 @@ struct ExpertArgs {
     unsigned flags;            // kExpertsXBySlot: slot s reads x[s] (else x[slot_token[s]]);
                                // kExpertsPlanReady: the plan is complete when the launch begins
     int depth;
-    uint32_t wait_limit, drain_limit, stage_tx, fmagic;
+    uint32_t wait_limit, drain_limit, stage_tx;
     uint32_t test_extra_tx;    // test hook: bytes added to every warp's first expected transaction
     const unsigned char* next_w;   // optional: a second stack of the same experts whose active
                                    // experts this launch prefetches into L2 (nullptr = none)
@@ -153,7 +153,7 @@ __device__ __forceinline__ void expert_group(const ExpertArgs& a, Ring& R, unsig
             const int codes_k = (kc == R.spr - 1) ? last_codes : 512;
             const uint32_t stage = uint32_t(R.sc) * uint32_t(kStage);
             step_fma<FMT, NE, RPW, XT>(acc, x_lane + uint32_t(kc) * (32u * kCS * 16u), code_lane + stage,
-                                   scale_lane + stage + uint32_t(codes_k), a.fmagic);
+                                   scale_lane + stage + uint32_t(codes_k));
             __syncwarp();                        // every lane has read this stage before it is refilled
             R.issue(&a.wmap, a.stage_tx, a.test_extra_tx, lane);
             if (++R.sc == R.depth) { R.sc = 0; R.phase ^= 1u; }

@@ -21,27 +21,24 @@
 //    read.  The bytes in flight per SM are set by shared memory, not by
 //    registers, and every weight byte is read exactly once.  One flat pipeline
 //    runs across row-group boundaries, so the copies never drain between groups.
-//  * Q8_0, BF16, Q5_0: dequantization in registers without I2F.  A code is
-//    placed in the mantissa of 2^23 (byte permute or mask) and the offset is
-//    removed with an exact packed FADD (add.rn.f32x2); Q5_0's codes at nibble
-//    position 4m come out as q*16^m and x is stored pre-multiplied by 16^-m
-//    (exact).  Block scales are applied once per chunk.
-//  * Q4_0 and affine 4-bit: integer chunk dots.  x is staged per 32-column chunk
-//    and token as 16-bit integers X = rn(x * 2^(14-k)) with 2^(k-1) <= max|x| <
-//    2^k (|X| <= 2^14, error <= 2^-14 of the chunk's largest |x|); a word of 8
-//    codes becomes two words of 4 bytes (one mask, one shift and mask), and
-//    dp2a (16-bit x 8-bit pairs into int32, exact) takes two products per
-//    instruction.  Per chunk one I2F (exact: |sum| < 2^24) and one FMA with
-//    scale * 2^(k-14).  On GB300 this issues about half the instructions of
-//    the magic-float decode with packed FMAs, whose issue cost binds the 4-bit
-//    formats at ntok 3-4 (measured: a register-only model of the inner loop
-//    reaches 27 weights/clk/SM at ntok 4 against 18 with packed FP32).
-//  * FP32 math in packed pairs: per (row, token) a pair of partial sums (even
-//    and odd columns) advanced by fma.rn.f32x2, added and scaled once per
-//    chunk.  On GB300 the packed FMA does not raise the FP32 rate, but it
-//    halves the instructions issued for the multiply-adds.
-//  * The affine bias term b*sum(x) uses per-chunk sums of x computed once per
-//    CTA; the per-chunk fp32 order is fixed.
+//  * Q8_0, Q4_0, Q5_0 and affine 4-bit: integer chunk dots.  x is staged per
+//    chunk (32 columns, 16 for Q8_0) and token as 16-bit integers
+//    X = rn(x * 2^(14-k)) with 2^(k-1) <= max|x| < 2^k (|X| <= 2^14, error
+//    <= 2^-14 of the chunk's largest |x|); codes become bytes (Q8_0's stored
+//    q + 128 as they are; a nibble word's even codes by one mask, its odd codes
+//    by one shift and mask, Q5_0's fifth bits merged from the chunk's record),
+//    and dp2a (16-bit x 8-bit pairs into int32, exact) takes two products per
+//    instruction.  Per chunk one I2F and one FMA with scale * 2^(k-14).  On
+//    GB300 this issues about half the instructions of a magic-float decode
+//    with packed FP32 FMAs, whose issue cost bound the quantized formats at
+//    ntok 3-4 (measured: a register-only model of the 4-bit ntok-4 inner loop
+//    reaches 27 weights/clk/SM against 18 with packed FP32).
+//  * BF16: codes widened to fp32 by shifts and masks.
+//  * BF16 math in packed pairs: per (row, token) a pair of partial sums (even
+//    and odd columns) advanced by fma.rn.f32x2.  On GB300 the packed FMA does
+//    not raise the FP32 rate, but it halves the instructions issued.
+//  * The affine bias term b*sum(x) uses per-chunk fp32 sums of x computed once
+//    per CTA in a fixed order.
 //  * Reduction: per lane, chunks in increasing order; across the warp, a
 //    transposed butterfly (reduce-scatter by halving, then xor steps).  The
 //    order depends only on (fmt, n_in), never on ntok, the tile or the grid, so
@@ -96,9 +93,6 @@ struct KernelArgs {
     uint32_t test_extra_tx;    // test hook: bytes added to the first expected transaction of
                                // every warp, so that wait can never complete (0 = off)
     uint32_t stage_tx;         // bytes one box delivers: RPW x full step (zero fill included)
-    uint32_t fmagic;           // 0x4B000000, the bits of 2^23; passed in so that the nibble
-                               // extraction (h & mask) | magic is one LOP3 with the mask as
-                               // its only immediate
 };
 
 // ------------------------------------------------------------------------------ PTX helpers
@@ -178,15 +172,6 @@ __device__ __forceinline__ float h2f(uint32_t bits) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
 }
 
-// Nibble m (bits 4m..4m+3) of a half-word h, as the bits of the float 2^23 + q*16^m
-// (magic = 0x4B000000, held in a register).
-template <uint32_t MASK>
-__device__ __forceinline__ uint32_t nib(uint32_t h, uint32_t magic) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(h), "n"(MASK), "r"(magic));
-    return d;
-}
-
 // A pair of fp32 values in one 64-bit register pair, as the packed f32x2
 // instructions take them.  Keeping pairs as 64-bit PTX values lets ptxas build
 // each pair in place (no register moves to assemble operands).
@@ -244,13 +229,6 @@ template <> struct Fmt<QG_Q8_0> {
     static constexpr int kStepScale = 32;
     static __device__ __forceinline__ uint32_t scale_off(int j) { return 2u * uint32_t(j >> 1); }
     static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds16(a); }
-    // bytes hold q + 128; 2^23 + (q + 128) - (2^23 + 128) = q, exact.
-    static __device__ __forceinline__ void dec(const uint4& q, int i, f2_t& lo, f2_t& hi, uint32_t mg) {
-        const uint32_t w = i == 0 ? q.x : i == 1 ? q.y : i == 2 ? q.z : q.w;
-        const f2_t m = f2_const(-8388736.0f);
-        lo = f2_add(f2_pack(__byte_perm(w, mg, 0x7440), __byte_perm(w, mg, 0x7441)), m);
-        hi = f2_add(f2_pack(__byte_perm(w, mg, 0x7442), __byte_perm(w, mg, 0x7443)), m);
-    }
 };
 
 // Q4_0 and the affine format run the integer chunk dot (step_idp); their traits give the
@@ -274,7 +252,7 @@ template <> struct Fmt<QG_BF16> {
     static constexpr int kStepScale = 0;
     static __device__ __forceinline__ uint32_t scale_off(int) { return 0u; }
     static __device__ __forceinline__ uint32_t scale(uint32_t) { return 0u; }
-    static __device__ __forceinline__ void dec(const uint4& q, int i, f2_t& lo, f2_t& hi, uint32_t) {
+    static __device__ __forceinline__ void dec(const uint4& q, int i, f2_t& lo, f2_t& hi) {
         const uint32_t w0 = i == 0 ? q.x : q.z;
         const uint32_t w1 = i == 0 ? q.y : q.w;
         lo = f2_pack(w0 << 16, w0 & 0xFFFF0000u);
@@ -282,56 +260,34 @@ template <> struct Fmt<QG_BF16> {
     }
 };
 
-// Q5_0: the Q4_0 nibbles plus a fifth bit per element.  A chunk's scale record (6
-// bytes at 6j after the step's codes) holds its fifth bits (uint32) and then its fp16
-// d.  The packer stores the fifth bit of column 4i + m at bit (4m + 4 + r_i) mod 32,
-// r_i = i (i < 4) or i + 12 (i >= 4), so one funnel rotation by r_i puts the fifth
-// bits of columns 4i..4i+3 at bits 4, 8, 12 and 16: bit 4m + 4 of the magic float,
-// just above nibble m, and one LOP3 per column merges it:
-// (2^23 + q*16^m) - (2^23 + 16*16^m) = (q - 16) * 16^m.
+// Q5_0: the Q4_0 nibbles plus a fifth bit per element.  A chunk's scale record (6 bytes at
+// 6j after the step's codes) holds its fifth bits (uint32, element e at bit 8b + g with
+// g = 2 (e / 8) + e % 2 and b = (e % 8) / 2) and then its fp16 d.
 template <> struct Fmt<QG_Q5_0> {
     static constexpr int kW = 32;
     static constexpr int kStepScale = 192;
     static __device__ __forceinline__ uint32_t scale_off(int j) { return 6u * uint32_t(j); }
     static __device__ __forceinline__ uint32_t scale(uint32_t a) { return lds16(a + 4); }
     static __device__ __forceinline__ uint32_t high(uint32_t a) { return lds16(a) | (lds16(a + 2) << 16); }
-    template <uint32_t BIT>
-    static __device__ __forceinline__ uint32_t merge(uint32_t rot, uint32_t nibble) {
-        uint32_t d;
-        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(rot), "n"(BIT), "r"(nibble));   // (rot & BIT) | nibble
-        return d;
-    }
-    static __device__ __forceinline__ void dec5(const uint4& q, uint32_t qh, int i, f2_t& lo, f2_t& hi,
-                                                uint32_t mg) {
-        const uint32_t w = (i >> 1) == 0 ? q.x : (i >> 1) == 1 ? q.y : (i >> 1) == 2 ? q.z : q.w;
-        const uint32_t h = (i & 1) ? (w >> 16) : w;
-        const uint32_t rot = i == 0 ? qh : __funnelshift_r(qh, qh, i < 4 ? i : i + 12);
-        const uint32_t b0 = merge<0x10u>(rot, nib<0x000Fu>(h, mg));
-        const uint32_t b1 = merge<0x100u>(rot, nib<0x00F0u>(h, mg));
-        const uint32_t b2 = merge<0x1000u>(rot, nib<0x0F00u>(h, mg));
-        const uint32_t b3 = merge<0x10000u>(rot, nib<0xF000u>(h, mg));
-        lo = f2_add(f2_pack(b0, b1), f2_pack(__float_as_uint(-8388624.0f), __float_as_uint(-8388864.0f)));
-        hi = f2_add(f2_pack(b2, b3), f2_pack(__float_as_uint(-8392704.0f), __float_as_uint(-8454144.0f)));
-    }
 };
 
 // Formats that run the integer chunk dot (x staged as 16-bit integers).
 __host__ __device__ constexpr bool idp_format(int fmt) {
-    return fmt == QG_Q8_0 || fmt == QG_Q4_0 || fmt == QG_AFFINE4_G64;
+    return fmt == QG_Q8_0 || fmt == QG_Q4_0 || fmt == QG_AFFINE4_G64 || fmt == QG_Q5_0;
 }
 template <int FMT> struct IsIdp { static constexpr bool value = idp_format(FMT); };
 
-// 16-byte slots of staged x per chunk and token: the chunk's columns as fp32 (BF16 8,
-// Q5_0 32 columns), or as 16-bit integers for the integer dot (Q8_0 16, Q4_0 and
-// affine 32 columns).
+// 16-byte slots of staged x per chunk and token: the chunk's columns as fp32 (BF16, 8
+// columns), or as 16-bit integers for the integer dot (Q8_0 16, the 4- and 5-bit
+// formats 32 columns).
 __host__ __device__ constexpr int x_slots(int fmt) {
-    return fmt == QG_Q8_0 ? 2 : idp_format(fmt) ? 4 : fmt == QG_BF16 ? 2 : 8;
+    return fmt == QG_Q8_0 ? 2 : idp_format(fmt) ? 4 : 2;
 }
 // Pad slots after a chunk's staged x.  Integer dot: slot 0 holds per token the chunk's
 // scale 2^(k-14), slot 1 per token the starting sum that removes the code offset
-// (Q8_0 -128 * sum(X), Q4_0 -8 * sum(X), int32) or the affine bias's sum(x) (fp32);
-// slot 2 pads the stride to an odd count.  Other formats: one slot (unused but for
-// the odd stride).
+// (Q8_0 -128 * sum(X), Q4_0 -8 * sum(X), Q5_0 -16 * sum(X), int32) or the affine
+// bias's sum(x) (fp32); slot 2 pads the stride to an odd count.  BF16: one slot
+// (unused but for the odd stride).
 __host__ __device__ constexpr int x_pad_slots(int fmt) { return idp_format(fmt) ? 3 : 1; }
 
 // ------------------------------------------------------------------------------ helpers
@@ -471,6 +427,7 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
             pad[t] = __float_as_uint(down);
             if constexpr (FMT == QG_Q8_0) pad[4 + t] = uint32_t(-128 * int(sX));
             else if constexpr (FMT == QG_Q4_0) pad[4 + t] = uint32_t(-8 * int(sX));
+            else if constexpr (FMT == QG_Q5_0) pad[4 + t] = uint32_t(-16 * int(sX));
             else pad[4 + t] = __float_as_uint(sx);
         }
         for (int i = nchunks * kCS + int(threadIdx.x); i < spr * 32 * kCS; i += int(blockDim.x))
@@ -495,14 +452,7 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
 #pragma unroll
                 for (int t = 0; t < NTOK; ++t) {
                     if (t >= live) break;
-                    float4 w = v[j][t];
-                    if constexpr (FMT == QG_Q5_0) {
-                        // column j is used as q*16^(j%4): store x * 16^-(j%4) (exact)
-                        w.y *= 0.0625f;
-                        w.z *= 0.00390625f;
-                        w.w *= 0.000244140625f;
-                    }
-                    dst[t * S] = w;
+                    dst[t * S] = v[j][t];
                 }
             }
         }
@@ -543,20 +493,17 @@ template <int FMT, int NTOK, int RPW> struct Acc {
 // 0..NTOK-1 are used).  Within the chunk a pair of partial sums (even / odd columns)
 // per (row, token) is advanced by packed FMAs, then added and scaled once.
 template <int FMT, int NTOK, int RPW, int XT>
-__device__ __forceinline__ void step_fp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uint32_t codes, uint32_t scales,
-                                        uint32_t magic) {
+__device__ __forceinline__ void step_fp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uint32_t codes, uint32_t scales) {
     using F = Fmt<FMT>;
     constexpr int S = x_slots(FMT);
     constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
     constexpr bool kPairAcc = Acc<FMT, NTOK, RPW>::kPair;
     uint4 qv[RPW];
     uint32_t sv[RPW];
-    uint32_t hv[FMT == QG_Q5_0 ? RPW : 1];         // Q5_0: the chunk's fifth bits
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         qv[r] = lds128(codes + r * kFullStep);
         sv[r] = F::scale(scales + r * kFullStep);
-        if constexpr (FMT == QG_Q5_0) hv[r] = F::high(scales + r * kFullStep);
     }
     f2_t p[kPairAcc ? 1 : RPW][kPairAcc ? 1 : NTOK];
 #pragma unroll
@@ -571,8 +518,7 @@ __device__ __forceinline__ void step_fp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uin
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             f2_t wlo, whi;
-            if constexpr (FMT == QG_Q5_0) F::dec5(qv[r], hv[r], i, wlo, whi, magic);
-            else F::dec(qv[r], i, wlo, whi, magic);
+            F::dec(qv[r], i, wlo, whi);
 #pragma unroll
             for (int t = 0; t < NTOK; ++t) {
                 f2_t& pp = [&]() -> f2_t& {
@@ -583,27 +529,19 @@ __device__ __forceinline__ void step_fp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uin
             }
         }
     }
-    if constexpr (FMT == QG_Q8_0 || FMT == QG_Q5_0) {
-#pragma unroll
-        for (int r = 0; r < RPW; ++r) {
-            const float d = h2f(sv[r]);
-#pragma unroll
-            for (int t = 0; t < NTOK; ++t)
-                A.s[r][t] = __fmaf_rn(d, f2_sum(p[r][t]), A.s[r][t]);
-        }
-    }
 }
 
-// Integer chunk dot (Q8_0, Q4_0, affine).  Q4_0 / affine: the lane's 16-byte chunk of
-// each of the RPW rows is 4 words of 8 codes; a word gives its even codes as 4 bytes
-// (w & 0x0F0F0F0F) and its odd codes (w >> 4 & 0x0F0F0F0F), and per token four dp2a add
-// the 8 products of the word's staged 16-bit x pairs into an int32 (exact).  Q8_0: the
-// chunk is 16 byte codes q + 128, taken by dp2a as they are.  The sums start at
-// -128 * sum(X) (Q8_0) or -8 * sum(X) (Q4_0), which removes the code offset exactly;
-// the chunk then adds (I2F(sum) * 2^(k-14)) * d, and the affine format also
-// b * sum(x).  (|sum| < 2^24 for the 4-bit formats, so the I2F is exact; a Q8_0 chunk
-// sum can reach 2^25 and then rounds to 24 bits.)  The order of additions is fixed per
-// lane and chunk.
+// Integer chunk dot (Q8_0, Q4_0, Q5_0, affine).  Q4_0 / Q5_0 / affine: the lane's
+// 16-byte chunk of each of the RPW rows is 4 words of 8 codes; a word gives its even
+// codes as 4 bytes (w & 0x0F0F0F0F) and its odd codes (w >> 4 & 0x0F0F0F0F), Q5_0 ORs
+// in each group's fifth bits (the record word shifted by 4 - g, masked to bit 4 of
+// each byte), and per token four dp2a add the 8 products of the word's staged 16-bit x
+// pairs into an int32 (exact).  Q8_0: the chunk is 16 byte codes q + 128, taken by
+// dp2a as they are.  The sums start at -128 / -8 / -16 * sum(X) (Q8_0 / Q4_0 / Q5_0),
+// which removes the code offset exactly; the chunk then adds (I2F(sum) * 2^(k-14)) * d,
+// and the affine format also b * sum(x).  (|sum| < 2^24 for the 4-bit formats, so the
+// I2F is exact; a Q8_0 or Q5_0 chunk sum can exceed 2^24 and then rounds to 24 bits.)
+// The order of additions is fixed per lane and chunk.
 __device__ __forceinline__ int dp2a_lo(uint32_t x, uint32_t q, int c) {
     int d;
     asm("dp2a.lo.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(x), "r"(q), "r"(c));
@@ -622,10 +560,12 @@ __device__ __forceinline__ void step_idp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
     constexpr int kFullStep = int(kStepCodeBytes) + F::kStepScale;
     uint4 qv[RPW];
     uint32_t sv[RPW];
+    uint32_t hv[FMT == QG_Q5_0 ? RPW : 1];         // Q5_0: the chunk's fifth bits
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         qv[r] = lds128(codes + r * kFullStep);
         sv[r] = F::scale(scales + r * kFullStep);
+        if constexpr (FMT == QG_Q5_0) hv[r] = F::high(scales + r * kFullStep);
     }
     const uint4 pk = lds128(xr + 16u * uint32_t(XT * S));         // 2^(k-14) per token
     const uint4 pb = lds128(xr + 16u * uint32_t(XT * S + 1));     // Q4_0: -8 sum(X); affine: sum(x)
@@ -667,7 +607,16 @@ __device__ __forceinline__ void step_idp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
 #pragma unroll
         for (int r = 0; r < RPW; ++r) {
             const uint32_t w = j == 0 ? qv[r].x : j == 1 ? qv[r].y : j == 2 ? qv[r].z : qv[r].w;
-            const uint32_t ev = w & 0x0F0F0F0Fu, od = (w >> 4) & 0x0F0F0F0Fu;
+            uint32_t ev = w & 0x0F0F0F0Fu, od = (w >> 4) & 0x0F0F0F0Fu;
+            if constexpr (FMT == QG_Q5_0) {
+                // fifth bits of the word's even (group 2j) and odd (group 2j + 1) codes
+                // to bit 4 of their bytes
+                const int ge = 2 * j, go = 2 * j + 1;
+                const uint32_t he = ge <= 4 ? hv[r] << (4 - ge) : hv[r] >> (ge - 4);
+                const uint32_t ho = go <= 4 ? hv[r] << (4 - go) : hv[r] >> (go - 4);
+                ev |= he & 0x10101010u;
+                od |= ho & 0x10101010u;
+            }
 #pragma unroll
             for (int t = 0; t < NTOK; ++t) {
                 int a = acc[r][t];
@@ -695,13 +644,12 @@ __device__ __forceinline__ void step_idp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
     }
 }
 
-// One ring stage into the accumulators: the integer chunk dot for Q4_0 and the affine
-// format, the magic-float decode with packed FMAs otherwise.
+// One ring stage into the accumulators: the integer chunk dot for the quantized formats,
+// packed FP32 FMAs for BF16.
 template <int FMT, int NTOK, int RPW, int XT = NTOK>
-__device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uint32_t codes, uint32_t scales,
-                                         uint32_t magic) {
+__device__ __forceinline__ void step_fma(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uint32_t codes, uint32_t scales) {
     if constexpr (IsIdp<FMT>::value) step_idp<FMT, NTOK, RPW, XT>(A, xr, codes, scales);
-    else step_fp<FMT, NTOK, RPW, XT>(A, xr, codes, scales, magic);
+    else step_fp<FMT, NTOK, RPW, XT>(A, xr, codes, scales);
 }
 
 // Transposed warp reduction of the V = RPW * NTOK lane sums (reduce-scatter by
@@ -735,13 +683,11 @@ __device__ __forceinline__ float warp_reduce(const Acc<FMT, NTOK, RPW>& A, int l
 // ------------------------------------------------------------------------------ kernel
 
 // Threads per CTA a kernel allows: 512 (16 warps), or 384 (12 warps) where a warp
-// keeps more than 20 outputs per row group (8 rows at ntok 3, 6 rows at ntok 4), or
-// 16 with 4-bit codes at ntok >= 2 (whose decode needs more registers), so that each
-// thread may hold up to 168 registers instead of 128 and the extra rows'
+// keeps more than 20 outputs per row group (8 rows at ntok 3, 6 rows at ntok 4), so
+// that each thread may hold up to 168 registers instead of 128 and the extra rows'
 // accumulators do not spill.  Kernels that fit in 128 keep 16 warps.
 template <int FMT, int NTOK, int RPW> struct MaxThreads {
-    static constexpr bool kFourBit = FMT == QG_Q5_0;
-    static constexpr int value = (RPW * NTOK > 20 || (kFourBit && RPW * NTOK >= 16 && NTOK >= 2)) ? 384 : 512;
+    static constexpr int value = RPW * NTOK > 20 ? 384 : 512;
 };
 
 template <int FMT, int NTOK, int RPW, bool ARGMAX, bool SPLIT>
@@ -852,7 +798,6 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
 
     float best_v = -INFINITY;
     int best_i = 0x7FFFFFFF;
-    const uint32_t magic = a.fmagic;
     const uint32_t x_lane = xs_base + uint32_t(lane) * (kCS * 16);          // chunk `lane` of step 0
     const uint32_t code_lane = ring + 16u * uint32_t(lane);
     const uint32_t scale_lane = ring + F::scale_off(lane);
@@ -876,7 +821,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
         {
             const uint32_t stage = uint32_t(sc) * uint32_t(kStage);
             step_fma<FMT, NTOK, RPW>(acc, x_lane + uint32_t(kc) * (32u * kCS * 16u), code_lane + stage,
-                                     scale_lane + stage + uint32_t(codes_k), magic);
+                                     scale_lane + stage + uint32_t(codes_k));
         }
         __syncwarp();          // every lane has read this stage before it is refilled
         issue();

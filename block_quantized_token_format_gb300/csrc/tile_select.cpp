@@ -35,33 +35,28 @@ struct Entry {
 // and CTAs per SM, back-to-back launches with early start; the sweep summary is
 // in profiles/).  First match wins.
 const Entry kTable[] = {
-    // Q8_0, n_in 2560: LM heads
-    {QG_Q8_0, 65536, INT64_MAX, 2560, 1, {4, 3, 16, 1}},
-    {QG_Q8_0, 65536, INT64_MAX, 2560, 2, {8, 2, 16, 1}},
-    {QG_Q8_0, 65536, INT64_MAX, 2560, 3, {8, 2, 12, 1}},
-    {QG_Q8_0, 65536, INT64_MAX, 2560, 4, {4, 2, 16, 1}},
+    // Q8_0 (integer chunk dot), n_in 2560: LM heads
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 1, {8, 2, 12, 1}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 2, {6, 2, 16, 1}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 3, {4, 3, 16, 1}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 4, {5, 2, 16, 1}},
     // Q8_0, n_in 2560: 11264..65535 rows (the 12288 projection)
-    {QG_Q8_0, 11264, 65535, 2560, 1, {4, 2, 12, 2}},
-    {QG_Q8_0, 11264, 65535, 2560, 2, {6, 2, 8, 2}},
-    {QG_Q8_0, 11264, 65535, 2560, 3, {8, 2, 12, 1}},
-    {QG_Q8_0, 11264, 65535, 2560, 0, {4, 2, 12, 1}},
+    {QG_Q8_0, 11264, 65535, 2560, 4, {4, 2, 12, 1}},
+    {QG_Q8_0, 11264, 65535, 2560, 0, {8, 2, 12, 1}},
     // Q8_0, n_in 2560: 9000..11263 rows (the 10240 projection)
-    {QG_Q8_0, 9000, 11263, 2560, 1, {8, 2, 4, 3}},
-    {QG_Q8_0, 9000, 11263, 2560, 2, {6, 2, 12, 1}},
-    {QG_Q8_0, 9000, 11263, 2560, 3, {6, 2, 6, 2}},
-    {QG_Q8_0, 9000, 11263, 2560, 4, {6, 2, 12, 1}},
-    {QG_Q8_0, 9000, 11263, 2560, 0, {4, 2, 12, 1}},
+    {QG_Q8_0, 9000, 11263, 2560, 1, {4, 2, 12, 2}},
+    {QG_Q8_0, 9000, 11263, 2560, 3, {6, 2, 16, 1}},
+    {QG_Q8_0, 9000, 11263, 2560, 0, {6, 2, 12, 1}},
     // Q8_0, n_in 2560: 4096..8999 rows (the 6144 projection)
-    {QG_Q8_0, 4096, 8999, 2560, 1, {4, 2, 12, 1}},
-    {QG_Q8_0, 4096, 8999, 2560, 3, {6, 2, 6, 2}},
-    {QG_Q8_0, 4096, 8999, 2560, 4, {4, 2, 16, 1}},
+    {QG_Q8_0, 4096, 8999, 2560, 1, {4, 2, 8, 2}},
+    {QG_Q8_0, 4096, 8999, 2560, 3, {4, 2, 16, 1}},
     {QG_Q8_0, 4096, 8999, 2560, 0, {4, 2, 12, 1}},
     // Q8_0, n_in 2560: up to 4095 rows (2560 x 2560)
     {QG_Q8_0, 1, 4095, 2560, 1, {2, 5, 12, 2}},
-    {QG_Q8_0, 1, 4095, 2560, 2, {2, 5, 12, 2}},
-    {QG_Q8_0, 1, 4095, 2560, 4, {5, 2, 12, 1}},
-    {QG_Q8_0, 1, 4095, 2560, 0, {2, 2, 12, 1}},
+    {QG_Q8_0, 1, 4095, 2560, 4, {2, 3, 16, 1}},
+    {QG_Q8_0, 1, 4095, 2560, 0, {4, 3, 16, 1}},
     // Q8_0, n_in 6144, few rows (6144 -> 2560; split 3: 15 warps = 5 teams)
+    {QG_Q8_0, 1, 8191, 6144, 1, {4, 3, 16, 1}},
     {QG_Q8_0, 1, 8191, 6144, 0, {4, 2, 16, 1}},
     // Q4_0 (integer chunk dot) and BF16, 8192 x 2560
     {QG_Q4_0, 4096, 65535, 2560, 1, {8, 2, 8, 2}},
@@ -79,9 +74,9 @@ const Entry kTable[] = {
     {QG_Q5_0, 4096, 65535, 2560, 4, {5, 2, 12, 1}},
     // affine 4-bit LM head (integer chunk dot)
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {8, 2, 12, 1}},
-    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {8, 2, 12, 1}},
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {6, 2, 16, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 3, {8, 2, 12, 1}},
-    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 4, {6, 2, 12, 1}},
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 4, {5, 2, 16, 1}},
 };
 
 }  // namespace

@@ -92,10 +92,10 @@ int qg_abi_version(void);
  *           words of 8 consecutive elements (element k at bits [4k,4k+4)); BF16 raw.
  *   scales: Q8_0 / Q4_0 one fp16 d per 32 weights; AFFINE4_G64 one (fp16 s,
  *           fp16 b) pair per 64 weights; Q5_0 one (uint32 fifth bits, fp16 d)
- *           record of 6 bytes per 32 weights, the fifth bit of block element
- *           e = 4i + m (m < 4) at bit (4m + 4 + r) mod 32 of the uint32, r = i for
- *           i < 4 and i + 12 otherwise (rotating the word right by r lines up the
- *           fifth bits of elements 4i..4i+3 one place above their nibbles).
+ *           record of 6 bytes per 32 weights, the fifth bit of block element e at
+ *           bit 8b + g of the uint32, g = 2*(e/8) + e%2 and b = (e%8)/2 (shifting
+ *           the word by 4 - g and masking 0x10101010 puts a group's fifth bits at
+ *           bit 4 of its code bytes).
  * Sizes return 0 for invalid arguments. */
 size_t  qg_canonical_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);
 size_t  qg_packed_bytes(qg_fmt fmt, int64_t n_out, int64_t n_in);

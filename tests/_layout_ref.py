@@ -7,8 +7,8 @@ Device layout: rows one after the other; a row is a run of steps, each step
 Codes: Q8_0 q+128; Q4_0 / Q5_0 (low nibbles) / affine uint32 words of 8
 consecutive elements (element k at bits 4k); BF16 raw.  Scales: Q8_0 / Q4_0 fp16 d
 per 32 weights; affine (fp16 s, fp16 b) per 64 weights; Q5_0 (uint32 fifth bits,
-fp16 d) per 32 weights, the fifth bit of element 4i + m at bit (4m + 4 + r_i) mod 32
-with r_i = i (i < 4) or i + 12 (i >= 4).
+fp16 d) per 32 weights, the fifth bit of element e at bit 8b + g with
+g = 2 (e // 8) + e % 2 and b = (e % 8) // 2.
 """
 from __future__ import annotations
 
@@ -69,9 +69,9 @@ def decode_device(fmt: str, packed: np.ndarray, n_out: int, n_in: int) -> np.nda
                 rec = scales.reshape(-1, 6)
                 qh = rec[:, :4].copy().view("<u4").reshape(-1)
                 d = rec[:, 4:].copy().view("<f2").astype(np.float64).reshape(-1)
-                # fifth bit of element e = 4i + m at bit (4m + 4 + r_i) mod 32, r_i = i or i + 12
+                # fifth bit of element e at bit 8b + g, g = 2 (e // 8) + e % 2, b = (e % 8) // 2
                 e = np.arange(32)
-                pos = (4 * (e & 3) + 4 + np.where(e >> 2 < 4, e >> 2, (e >> 2) + 12)) % 32
+                pos = 8 * ((e & 7) >> 1) + 2 * (e >> 3) + (e & 1)
                 hb = (qh[:, None] >> pos.astype(np.uint32)) & np.uint32(1)
                 q5 = (q.reshape(-1, 32) | (hb << np.uint32(4))).astype(np.float64)
                 out[r] = ((q5 - 16) * d[:, None]).reshape(-1)

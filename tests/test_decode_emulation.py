@@ -1,15 +1,12 @@
 """The kernels' in-register decode, emulated bit for bit on the CPU (no GPU): for every
 format, the packer's device bytes are turned into values the way the kernels do it —
-for Q5_0 a code placed in the mantissa of the magic float 2^23 (nibble mask), its fifth
-bit merged from the rotated record word, the offset removed by one fp32 subtraction;
 BF16 widened by a shift; for the integer chunk dot, Q8_0's bytes q + 128 as they are
-(the offset removed through the chunk's starting sum) and a Q4_0 / affine word's even
-and odd codes taken as bytes (one mask, one shift and mask) — and scaled by the block
-scale.  Every value must equal the oracle's fp64
+(the offset removed through the chunk's starting sum) and a Q4_0 / Q5_0 / affine word's
+even and odd codes taken as bytes (one mask, one shift and mask, Q5_0's fifth bits
+merged from its record) — and scaled by the block scale.  Every value must equal the oracle's fp64
 dequantization exactly: this pins the claim that the decode is exact and that the
 kernels' view of the device layout matches the packer's, before any GPU run.  The
-magic constants are restated here from the decode's arithmetic (2^23 = 8388608), not
-taken from the kernel sources.
+rule is restated here from the layout description, not taken from the kernel sources.
 
 The integer chunk dot also rounds x: per 32-column chunk and token, X = rn(x * 2^(14-k))
 with 2^(k-1) <= max|x| < 2^k.  test_x_rounding_bound pins the stated bound of that
@@ -25,18 +22,8 @@ import workloads
 import block_quantized_token_format_gb300 as qg
 from _layout_ref import split_row, row_stride
 
-MAGIC = np.uint32(0x4B000000)          # bits of 2^23
-TWO23 = np.float32(8388608.0)
-
-
 def _f32(bits):
     return np.asarray(bits, dtype=np.uint32).view(np.float32)
-
-
-def _rotr(v, s):
-    v = v.astype(np.uint64)
-    return (((v >> np.uint64(s)) | (v << np.uint64(32 - s))) & np.uint64(0xFFFFFFFF)).astype(np.uint32) if s else \
-        v.astype(np.uint32)
 
 
 def emulate_row(fmt, codes, scales, n_in):
@@ -53,43 +40,34 @@ def emulate_row(fmt, codes, scales, n_in):
         d = scales.copy().view("<f2").astype(np.float64)
         return (q.reshape(-1, 32) * d[:, None]).reshape(-1).astype(np.float64)
     words = codes.copy().view("<u4").reshape(-1, 4)            # one 16-byte lane chunk per row
-    if fmt in ("q4_0", "affine4_g64"):
+    if fmt in ("q4_0", "affine4_g64", "q5_0"):
         return emulate_bytes(fmt, words, scales)
-    out = np.empty((words.shape[0], 32), dtype=np.float64)
-    if fmt == "q5_0":
-        rec = scales.reshape(-1, 6)
-        qh = rec[:, :4].copy().view("<u4").reshape(-1)
-        d5 = rec[:, 4:].copy().view("<f2").astype(np.float64).reshape(-1)
-    for i in range(8):                                         # 4 columns per step of i
-        w = words[:, i >> 1]
-        h = (w >> np.uint32(16)) if (i & 1) else w
-        rot = _rotr(qh, i if i < 4 else i + 12) if fmt == "q5_0" else None
-        for m in range(4):
-            bits = (h & np.uint32(0xF << (4 * m))) | MAGIC     # 2^23 + nibble * 16^m
-            if fmt == "q5_0":
-                bits = bits | (rot & np.uint32(0x10 << (4 * m)))
-            off = {"q4_0": 8, "q5_0": 16, "affine4_g64": 0}[fmt]
-            f = _f32(bits) - np.float32(8388608.0 + off * 16.0 ** m)   # (q - off) * 16^m, exact
-            out[:, 4 * i + m] = f.astype(np.float64) / 16.0 ** m       # the kernel pre-scales x by 16^-m
-    q = out.reshape(-1)
-    if fmt == "q4_0":
-        d = scales.copy().view("<f2").astype(np.float64)
-        return (q.reshape(-1, 32) * d[:, None]).reshape(-1)
-    if fmt == "q5_0":
-        return (q.reshape(-1, 32) * d5[:, None]).reshape(-1)
-    sb = scales.copy().view("<f2").astype(np.float64).reshape(-1, 2)
-    return (q.reshape(-1, 64) * sb[:, 0:1] + sb[:, 1:2]).reshape(-1)
+    raise ValueError(fmt)
+
+
+def _shift(v, s):
+    """v << s for s >= 0, v >> -s otherwise (uint32)."""
+    v = v.astype(np.uint64)
+    r = (v << np.uint64(s)) if s >= 0 else (v >> np.uint64(-s))
+    return (r & np.uint64(0xFFFFFFFF)).astype(np.uint32)
 
 
 def emulate_bytes(fmt, words, scales):
-    """Q4_0 / affine: word w of a lane chunk gives its even codes as the 4 bytes of
-    w & 0x0F0F0F0F and its odd codes as those of (w >> 4) & 0x0F0F0F0F; byte b of the
-    even word is element 2b, of the odd word element 2b + 1."""
+    """Q4_0 / Q5_0 / affine: word w of a lane chunk gives its even codes as the 4 bytes of
+    w & 0x0F0F0F0F and its odd codes as those of (w >> 4) & 0x0F0F0F0F; Q5_0 ORs in the
+    fifth bits of group g = 2j (even) or 2j + 1 (odd) as (record << (4 - g)) & 0x10101010;
+    byte b of the even word is element 2b, of the odd word element 2b + 1."""
     q = np.empty((words.shape[0], 32), dtype=np.float64)
+    if fmt == "q5_0":
+        rec = scales.reshape(-1, 6)
+        qh = rec[:, :4].copy().view("<u4").reshape(-1)
     for j in range(4):
         w = words[:, j]
         ev = w & np.uint32(0x0F0F0F0F)
         od = (w >> np.uint32(4)) & np.uint32(0x0F0F0F0F)
+        if fmt == "q5_0":
+            ev = ev | (_shift(qh, 4 - 2 * j) & np.uint32(0x10101010))
+            od = od | (_shift(qh, 4 - (2 * j + 1)) & np.uint32(0x10101010))
         for b in range(4):
             q[:, 8 * j + 2 * b] = ((ev >> np.uint32(8 * b)) & np.uint32(0xFF)).astype(np.float64)
             q[:, 8 * j + 2 * b + 1] = ((od >> np.uint32(8 * b)) & np.uint32(0xFF)).astype(np.float64)
@@ -97,6 +75,9 @@ def emulate_bytes(fmt, words, scales):
     if fmt == "q4_0":
         d = scales.copy().view("<f2").astype(np.float64)
         return ((q.reshape(-1, 32) - 8) * d[:, None]).reshape(-1)
+    if fmt == "q5_0":
+        d5 = scales.reshape(-1, 6)[:, 4:].copy().view("<f2").astype(np.float64).reshape(-1)
+        return ((q.reshape(-1, 32) - 16) * d5[:, None]).reshape(-1)
     sb = scales.copy().view("<f2").astype(np.float64).reshape(-1, 2)
     return (q.reshape(-1, 64) * sb[:, 0:1] + sb[:, 1:2]).reshape(-1)
 
@@ -157,9 +138,12 @@ def test_kernel_decode_is_exact(fmt, n_in):
         assert np.array_equal(got, ref[r]), (fmt, n_in, r, int(np.argmax(got != ref[r])))
 
 
-def test_q5_0_rotation_covers_every_bit_once():
-    """The rotated record places the 32 fifth bits at 32 distinct positions."""
+def test_q5_0_record_order_covers_every_bit_once():
+    """The record places the 32 fifth bits at 32 distinct positions, and group g's bits
+    land at bit 4 of its 4 code bytes after the shift by 4 - g."""
     e = np.arange(32)
-    i, m = e >> 2, e & 3
-    pos = (4 * m + 4 + np.where(i < 4, i, i + 12)) % 32
+    g = 2 * (e >> 3) + (e & 1)
+    b = (e & 7) >> 1
+    pos = 8 * b + g
     assert sorted(pos.tolist()) == list(range(32))
+    assert np.all(pos + (4 - g) == 8 * b + 4)
