@@ -373,19 +373,18 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
         // absolute error below 2^-113); one with a NaN or an infinity gets a NaN scale.
         constexpr int W = Fmt<FMT>::kW;                         // columns per chunk: 16 or 32
         uint32_t* xu = reinterpret_cast<uint32_t*>(smem);
-        for (int idx = threadIdx.x; idx < live * nchunks; idx += nt) {
-            const int t = int(idx >= nchunks) + int(idx >= 2 * nchunks) + int(idx >= 3 * nchunks);
-            const int c = idx - t * nchunks;
+        const int npairs = live * nchunks;
+        // The (chunk, token) pair's row of x and its first float4.
+        auto src_of = [&](int idx, int& t, int& c) {
+            t = int(idx >= nchunks) + int(idx >= 2 * nchunks) + int(idx >= 3 * nchunks);
+            c = idx - t * nchunks;
             const float4* rt = rows[0];
 #pragma unroll
             for (int u = 1; u < NTOK; ++u) rt = (t == u) ? rows[u] : rt;
-            const float4* src = rt + (W / 4) * c;
-            float v[W];
-#pragma unroll
-            for (int q = 0; q < W / 4; ++q) {
-                const float4 f = ld(src + q);
-                v[4 * q] = f.x; v[4 * q + 1] = f.y; v[4 * q + 2] = f.z; v[4 * q + 3] = f.w;
-            }
+            return rt + (W / 4) * c;
+        };
+        // Round, pack and store one pair's values.
+        auto put = [&](const float (&v)[W], int t, int c) {
             float m = 0.f, sx = 0.f;
             bool finite = true;
 #pragma unroll
@@ -429,6 +428,27 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
             else if constexpr (FMT == QG_Q4_0) pad[4 + t] = uint32_t(-8 * int(sX));
             else if constexpr (FMT == QG_Q5_0) pad[4 + t] = uint32_t(-16 * int(sX));
             else pad[4 + t] = __float_as_uint(sx);
+        };
+        // Two pairs per thread and pass, both pairs' loads issued before either is
+        // rounded (one L2 round trip where a CTA has up to twice as many pairs as threads).
+        for (int i0 = threadIdx.x; i0 < npairs; i0 += 2 * nt) {
+            const int i1 = i0 + nt;
+            int t0, c0, t1 = 0, c1 = 0;
+            const float4* s0 = src_of(i0, t0, c0);
+            const float4* s1 = i1 < npairs ? src_of(i1, t1, c1) : s0;
+            float v0[W], v1[W];
+#pragma unroll
+            for (int q = 0; q < W / 4; ++q) {
+                const float4 f = ld(s0 + q);
+                v0[4 * q] = f.x; v0[4 * q + 1] = f.y; v0[4 * q + 2] = f.z; v0[4 * q + 3] = f.w;
+            }
+#pragma unroll
+            for (int q = 0; q < W / 4; ++q) {
+                const float4 f = ld(s1 + q);
+                v1[4 * q] = f.x; v1[4 * q + 1] = f.y; v1[4 * q + 2] = f.z; v1[4 * q + 3] = f.w;
+            }
+            put(v0, t0, c0);
+            if (i1 < npairs) put(v1, t1, c1);
         }
         for (int i = nchunks * kCS + int(threadIdx.x); i < spr * 32 * kCS; i += int(blockDim.x))
             xs[i] = make_float4(0.f, 0.f, 0.f, 0.f);
