@@ -81,6 +81,8 @@ def parse_args():
     p.add_argument("--sweep-specs", default="")
     p.add_argument("--sweep-ntoks", default="1,2,3,4")
     p.add_argument("--sweep-out", default="tile_sweep.jsonl")
+    p.add_argument("--sweep-experts", default="", help="';'-separated tile specs: time the routed-expert "
+                   "layer (plan + gate/up + down) under each, one JSON line per spec")
     p.add_argument("--cpu-worker", default="", help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -871,6 +873,27 @@ def tile_sweep(args):
     qg.qg_set_tile_override(None)
 
 
+def sweep_experts(args):
+    """The routed-expert layer (the bench's 512-expert Q8_0 layer, share 0.65) under each
+    tile override spec: plan, gate/up and down times per ntok."""
+    import torch
+    import block_quantized_token_format_gb300 as qg
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda:0")
+    peak, _ = peaks()
+    qg.qg_set_launch_options(qg.QG_LAUNCH_EARLY_START)
+    layer = workloads.EXPERT_LAYERS["q8_0_experts_512x2560x640_top10"]
+    for spec in args.sweep_experts.split(";"):
+        qg.qg_set_tile_override(spec or None)
+        r = experts_detail(qg, torch, dev, peak, layer, routings=32)
+        print(json.dumps({"spec": spec, "tile": r["tile"],
+                          "ntok": {t: {k: v[k]["us"] for k in ("gate_up", "down", "layer")}
+                                   for t, v in r["ntok"].items()}}), flush=True)
+        torch.cuda.empty_cache()
+    qg.qg_set_tile_override(None)
+
+
 # ----------------------------------------------------------------------------- entry
 
 def one_shape(spec: str, argmax: bool = False):
@@ -978,6 +1001,9 @@ def main():
         return
     if args.sweep:
         tile_sweep(args)
+        return
+    if args.sweep_experts:
+        sweep_experts(args)
         return
     if args.one:
         one_shape(args.one.replace(";", ","))

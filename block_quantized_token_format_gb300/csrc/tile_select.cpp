@@ -110,17 +110,18 @@ Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok) {
 }
 
 // Measured on GB300 for the routed-expert layer (gate/up 1280x2560, down 2560x640,
-// Q8_0, 10-21 active experts): 4 rows per warp, 12 warps, a 2-stage ring beat 2 rows
-// x 16 warps by 8-12% and deeper rings (3-7 stages) by 1-10%.  CTA shares weighted
-// 4 + tokens per group (a 4-token group gets 1.6x the CTAs of a 1-token group) cut
-// the layer at ntok 3-4 by 7-10% against equal shares (2 + tokens: 5-8%).
+// Q8_0, 10-21 active experts, integer chunk dot): 4 rows per warp, 12 warps and a
+// 3-stage ring; 2 rows x 16 warps is 14% slower, 8 warps 10-20% slower, a 2-stage
+// ring 1-1.5% slower.  CTA shares weighted 4 + tokens per group (a 4-token group gets
+// 1.6x the CTAs of a 1-token group) cut the layer at ntok 3-4 by 7-10% against equal
+// shares (2 + tokens: 3% slower at ntok 4 than 4 + tokens, 8 + tokens 1.5% slower).
 Tile select_expert_tile(int fmt, int64_t n_out, int64_t n_in) {
     (void)fmt;
     (void)n_out;
     (void)n_in;
     Tile t;
     t.rpw = 4;
-    t.depth = 2;
+    t.depth = 3;
     t.warps = 12;
     t.ctas = 1;
     t.gw = 4;
