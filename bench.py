@@ -83,6 +83,9 @@ def parse_args():
     p.add_argument("--sweep-out", default="tile_sweep.jsonl")
     p.add_argument("--sweep-experts", default="", help="';'-separated tile specs: time the routed-expert "
                    "layer (plan + gate/up + down) under each, one JSON line per spec")
+    p.add_argument("--phases", default="", help="comma list of workload names: per-CTA phase timestamps "
+                   "(qg_set_phase_record) of 20 back-to-back launches in a graph, with and without early "
+                   "start, at --sweep-ntoks; one JSON line per (workload, ntok, launch mode)")
     p.add_argument("--cpu-worker", default="", help=argparse.SUPPRESS)
     return p.parse_args()
 
@@ -821,7 +824,7 @@ def reference_arm(args, rank, world):
 
 def tile_sweep(args):
     """GB/s per (workload, ntok, tile spec): each point is the median of 3 replays of a
-    20-launch graph rotating over weight copies totalling >= 4x L2 (set
+    graph of at least 20 launches rotating over weight copies totalling >= 4x L2 (set
     QGEMV_EARLY_START=1 to sweep with early-start launches).  The table in
     csrc/tile_select.cpp was filled from such sweeps."""
     import itertools
@@ -860,7 +863,7 @@ def tile_sweep(args):
                         qg.qgemv_argmax(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y[:ntok], am, ws, ntok)
                     else:
                         qg.qgemv(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y[:ntok], ntok)
-                us = time_graph(torch, call, n=20, reps=3)
+                us = time_graph(torch, call, n=max(20, copies), reps=3)
                 rec = {"name": name, "ntok": ntok, "spec": spec, "desc": desc, "us": round(us, 3),
                        "gbs": round(wb / us / 1e3, 1)}
                 out.write(json.dumps(rec) + "\n")
@@ -871,6 +874,101 @@ def tile_sweep(args):
         del pool, base
         torch.cuda.empty_cache()
     qg.qg_set_tile_override(None)
+
+
+def phase_times(args):
+    """Where a launch's time goes: each launch of a 20-launch graph (rotating over weight
+    copies totalling >= 4x L2) records per CTA the global time at entry and exit and the SM
+    cycles to warp 0's first copies issued, to the end of the wait for the previous kernel,
+    to x staged, to warp 0's first ring stage, to warp 0's last row group, to the CTA's
+    end, and to the landing of each of warp 0's first ring stages, polled before the wait
+    (recording only).  Reported per (workload,
+    ntok, launch mode): medians over the launches of the per-launch medians over CTAs (in
+    ns, cycles converted with the clock each CTA saw), the launch span (first entry to last
+    exit), the overlap with the previous launch and the period (exit to exit)."""
+    import torch
+    import block_quantized_token_format_gb300 as qg
+    import __graft_entry__
+    __graft_entry__.build()
+    ntoks = [int(v) for v in args.sweep_ntoks.split(",")]
+    dev = torch.device("cuda:0")
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    med = statistics.median
+    for name in args.phases.split(","):
+        w = workloads.WORKLOADS[name]
+        base = torch.from_numpy(gen_packed(qg, w)).to(dev)
+        copies = max(1, math.ceil(4 * l2 / base.numel()))
+        pool = [base] + [base.clone() for _ in range(copies - 1)]
+        n = max(20, copies)                 # one replay reads >= 4x L2 of weights
+        buf = torch.zeros(n * qg.QG_PHASE_SLOT_WORDS, dtype=torch.int64, device=dev)
+        x = torch.from_numpy(workloads.activations(w.seed, w.n_in, 4)).to(dev)
+        y = torch.empty((4, w.n_out), dtype=torch.float32, device=dev)
+        am = torch.empty(4, dtype=torch.int32, device=dev)
+        ws = torch.zeros(qg.qgemv_argmax_workspace_bytes(w.n_out, 4), dtype=torch.uint8, device=dev)
+        wb = workloads_bytes(w.fmt, w.n_out, w.n_in)
+        for ntok in ntoks:
+            desc = qg.qg_describe_tile(w.fmt, w.n_out, w.n_in, ntok)
+            grid = int(desc.split("grid=")[1])
+
+            def call(i, ntok=ntok):
+                if w.argmax:
+                    qg.qgemv_argmax(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y[:ntok], am, ws, ntok)
+                else:
+                    qg.qgemv(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y[:ntok], ntok)
+            for mode, flags in (("early_start", qg.QG_LAUNCH_EARLY_START), ("plain", 0)):
+                qg.qg_set_launch_options(flags)
+                us = time_graph(torch, call, n=n, reps=3)
+                # the captured launches take slots 0..n-1 in launch order
+                qg.qg_set_phase_record(buf, n)
+                try:
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                        for i in range(n):
+                            call(i)
+                finally:
+                    qg.qg_set_phase_record(None)
+                g.replay()
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                ev[0].record()
+                g.replay()
+                ev[1].record()
+                torch.cuda.synchronize()
+                us_rec = ev[0].elapsed_time(ev[1]) / n * 1e3
+                del g
+                rec = buf.view(n, -1)[:, :grid * qg.QG_PHASE_WORDS].reshape(n, grid, qg.QG_PHASE_WORDS).cpu().numpy()
+                rec = rec.astype(np.float64)
+                t_in, t_out, sm, cyc = rec[:, :, 0], rec[:, :, 1], rec[:, :, 2], rec[:, :, 3:16]
+                mhz = cyc[:, :, 5] / np.maximum(t_out - t_in, 1.0) * 1e3
+                ns = cyc / np.maximum(mhz[:, :, None], 1.0) * 1e3
+                start, end = t_in.min(axis=1), t_out.max(axis=1)
+                out = {"name": name, "ntok": ntok, "mode": mode, "tile": desc, "us_per_launch": round(us, 3),
+                       "us_per_launch_recording": round(us_rec, 3), "gbs": round(wb / us / 1e3, 1),
+                       "sm_mhz": round(float(np.median(mhz)), 1)}
+                out["span_ns"] = round(float(med(list(end - start))), 1)
+                out["overlap_prev_ns"] = round(float(med(list(end[:-1] - start[1:]))), 1)
+                out["period_ns"] = round(float(med(list(end[1:] - end[:-1]))), 1)
+                out["cta_entry_spread_ns"] = round(float(med(list(t_in.max(axis=1) - start))), 1)
+                out["cta_exit_spread_ns"] = round(float(med(list(end - t_out.min(axis=1)))), 1)
+                # per SM: first entry of launch i minus last exit of launch i-1 on the same SM
+                # (negative: the two launches' CTAs were resident on that SM together)
+                hand = []
+                for i in range(1, n):
+                    for smv in np.unique(sm[i]):
+                        prev = t_out[i - 1][sm[i - 1] == smv]
+                        if prev.size:
+                            hand.append(float(t_in[i][sm[i] == smv].min() - prev.max()))
+                out["sm_handoff_ns"] = round(float(med(hand)), 1) if hand else None
+                keys = ["copies_issued", "wait_done", "x_staged", "first_stage", "warp0_done", "cta_done"]
+                keys += [f"stage{k}_landed" for k in range(7)]
+                for j, key in enumerate(keys):
+                    if not np.any(cyc[:, :, j]):
+                        continue
+                    out[key + "_ns"] = round(float(med([med(list(ns[i, :, j])) for i in range(n)])), 1)
+                    out[key + "_ns_max"] = round(float(med([float(ns[i, :, j].max()) for i in range(n)])), 1)
+                print(json.dumps(out), flush=True)
+        del pool, base, buf
+        torch.cuda.empty_cache()
+    qg.qg_set_launch_options(0)
 
 
 def sweep_experts(args):
@@ -1004,6 +1102,9 @@ def main():
         return
     if args.sweep_experts:
         sweep_experts(args)
+        return
+    if args.phases:
+        phase_times(args)
         return
     if args.one:
         one_shape(args.one.replace(";", ","))

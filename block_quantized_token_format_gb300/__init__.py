@@ -25,6 +25,7 @@ __all__ = [
     "QG_DEVICE_BAD_ROW_ID", "qg_expert_plan_ints", "qg_expert_plan", "qgemv_experts", "qg_describe_expert_tile",
     "QG_DEVICE_BAD_PLAN", "QG_EXPERTS_X_BY_SLOT", "QG_EXPERTS_PLAN_READY",
     "QG_EXPERTS_SWIGLU", "qgemv_expert_layer", "qgemv_expert_layer_workspace_bytes",
+    "qg_set_phase_record", "QG_PHASE_WORDS", "QG_PHASE_SLOT_WORDS",
 ]
 
 QG_Q8_0, QG_Q4_0, QG_AFFINE4_G64, QG_BF16, QG_Q5_0 = 0, 1, 2, 3, 4
@@ -78,6 +79,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         "qg_set_wait_limit": (i32, [ctypes.c_uint, ctypes.c_uint]),
         "qgemv_argmax_noalloc": (i32, [i32, vp, i64, i64, vp, vp, vp, i32, vp]),
         "qg_set_launch_options": (i32, [ctypes.c_uint]),
+        "qg_set_phase_record": (i32, [vp, i64]),
         "qg_gather_rows": (i32, [i32, vp, i64, i64, vp, i64, vp, vp]),
         "qgemv_argmax_ids": (i32, [i32, vp, i64, i64, vp, vp, vp, i32, vp, vp, sz, vp]),
         "qg_expert_plan_ints": (sz, [i64]),
@@ -331,6 +333,19 @@ def qg_set_wait_limit(polls: int = 0, extra_tx_bytes: int = 0) -> None:
 
 QG_DEVICE_WAIT_TIMEOUT = 1
 QG_LAUNCH_EARLY_START = 1
+QG_PHASE_WORDS = 16
+QG_PHASE_SLOT_WORDS = 4096 * QG_PHASE_WORDS
+
+
+def qg_set_phase_record(buf, slots: int = 0) -> None:
+    """Profiling hook: per-CTA phase stamps of every later mat-vec launch into `buf`
+    (a CUDA uint64/int64 tensor of slots * QG_PHASE_SLOT_WORDS words; None turns it off)."""
+    if buf is None:
+        _check(load_library().qg_set_phase_record(None, 0), "qg_set_phase_record")
+        return
+    if buf.numel() < slots * QG_PHASE_SLOT_WORDS or buf.element_size() != 8:
+        raise ValueError("qg_set_phase_record: buffer smaller than slots * QG_PHASE_SLOT_WORDS 8-byte words")
+    _check(load_library().qg_set_phase_record(_ptr(buf), int(slots)), "qg_set_phase_record")
 
 
 def qg_set_launch_options(flags: int) -> None:

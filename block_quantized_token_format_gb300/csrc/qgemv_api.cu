@@ -52,6 +52,11 @@ DevInfo g_dev[kMaxDevices];
 std::atomic<uint32_t> g_wait_limit{kWaitLimit};
 std::atomic<uint32_t> g_test_extra_tx{0};
 
+// Profiling hook (qg_set_phase_record): the buffer, its slot count, the launch counter.
+std::mutex g_phase_mu;
+unsigned long long* g_phase_buf = nullptr;
+int64_t g_phase_slots = 0, g_phase_next = 0;
+
 // Tile override: QGEMV_TILE at first use, or qg_set_tile_override.
 std::mutex g_override_mu;
 std::atomic<uint64_t> g_override_gen{1};   // bumped whenever the override changes (plan cache key)
@@ -339,6 +344,14 @@ qg_status fill_common(KernelArgs& a, const Plan& p, int fmt, const void* W, int6
     a.drain_limit = std::max<uint32_t>(a.wait_limit, 1u << 16);
     a.test_extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
     a.stage_tx = uint32_t(p.tile.rpw * full_step_bytes(fmt));
+    a.phase = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_phase_mu);
+        if (g_phase_buf) {
+            a.phase = g_phase_buf + size_t(g_phase_next) * QG_PHASE_SLOT_WORDS;
+            g_phase_next = (g_phase_next + 1) % g_phase_slots;
+        }
+    }
     return QG_OK;
 }
 
@@ -545,6 +558,16 @@ qg_status qg_set_launch_options(unsigned int flags) {
 qg_status qg_set_wait_limit(uint32_t polls, uint32_t extra_tx_bytes) {
     g_wait_limit.store(polls == 0 ? kWaitLimit : polls, std::memory_order_relaxed);
     g_test_extra_tx.store(extra_tx_bytes, std::memory_order_relaxed);
+    return QG_OK;
+}
+
+qg_status qg_set_phase_record(unsigned long long* buf, int64_t slots) {
+    if (buf && slots < 1) return QG_EINVAL;
+    if (buf && !aligned(buf, 8)) return QG_EALIGN;
+    std::lock_guard<std::mutex> lk(g_phase_mu);
+    g_phase_buf = buf;
+    g_phase_slots = buf ? slots : 0;
+    g_phase_next = 0;
     return QG_OK;
 }
 

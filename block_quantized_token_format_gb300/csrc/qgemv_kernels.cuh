@@ -23,12 +23,13 @@
 //    runs across row-group boundaries, so the copies never drain between groups.
 //  * Q8_0, Q4_0, Q5_0 and affine 4-bit: integer chunk dots.  x is staged per
 //    chunk (32 columns, 16 for Q8_0) and token as 16-bit integers
-//    X = rn(x * 2^(14-k)) with 2^(k-1) <= max|x| < 2^k (|X| <= 2^14, error
-//    <= 2^-14 of the chunk's largest |x|); codes become bytes (Q8_0's stored
+//    X = rn(x * 2^(15-k)) capped at 32767, with 2^(k-1) <= max|x| < 2^k (error
+//    <= 2^-14 of the chunk's largest |x|, 2^-15 where the cap does not act);
+//    codes become bytes (Q8_0's stored
 //    q + 128 as they are; a nibble word's even codes by one mask, its odd codes
 //    by one shift and mask, Q5_0's fifth bits merged from the chunk's record),
 //    and dp2a (16-bit x 8-bit pairs into int32, exact) takes two products per
-//    instruction.  Per chunk one I2F and one FMA with scale * 2^(k-14).  On
+//    instruction.  Per chunk one I2F and one FMA with scale * 2^(k-15).  On
 //    GB300 this issues about half the instructions of a magic-float decode
 //    with packed FP32 FMAs, whose issue cost bound the quantized formats at
 //    ntok 3-4 (measured: a register-only model of the 4-bit ntok-4 inner loop
@@ -93,9 +94,21 @@ struct KernelArgs {
     uint32_t test_extra_tx;    // test hook: bytes added to the first expected transaction of
                                // every warp, so that wait can never complete (0 = off)
     uint32_t stage_tx;         // bytes one box delivers: RPW x full step (zero fill included)
+    unsigned long long* phase; // profiling: this launch's slot of per-CTA phase stamps, or null
 };
 
 // ------------------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned int sm_id() {
+    unsigned int v;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+    return v;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -284,7 +297,7 @@ __host__ __device__ constexpr int x_slots(int fmt) {
     return fmt == QG_Q8_0 ? 2 : idp_format(fmt) ? 4 : 2;
 }
 // Pad slots after a chunk's staged x.  Integer dot: slot 0 holds per token the chunk's
-// scale 2^(k-14), slot 1 per token the starting sum that removes the code offset
+// scale 2^(k-15), slot 1 per token the starting sum that removes the code offset
 // (Q8_0 -128 * sum(X), Q4_0 -8 * sum(X), Q5_0 -16 * sum(X), int32) or the affine
 // bias's sum(x) (fp32); slot 2 pads the stride to an odd count.  BF16: one slot
 // (unused but for the odd stride).
@@ -366,11 +379,14 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
     if constexpr (IsIdp<FMT>::value) {
         // One (chunk, token) pair per thread and pass: the chunk's values (32 columns, 16
         // for Q8_0) are loaded at once; with m = max|x| over them and 2^(k-1) <= m < 2^k,
-        // X = rn(x * 2^(14-k)) (|X| <= 2^14) is formed exactly by one FMA with 1.5 * 2^23
-        // (the integer sits in the low bits of the sum, round to nearest even), and stored
-        // as the 16-bit pairs dp2a takes: per word of 8 nibble codes (x0|x2, x4|x6, x1|x3,
-        // x5|x7) against its even and odd codes, per word of 4 byte codes (x0|x1, x2|x3).  A chunk with m < 2^-113 is staged as zero (an
-        // absolute error below 2^-113); one with a NaN or an infinity gets a NaN scale.
+        // X = rn(x * 2^(15-k)) is formed exactly by one FMA with 1.5 * 2^23 (the integer
+        // sits in the low bits of the sum, round to nearest even) and capped at 32767 (a
+        // value within 2^-16 m of 2^k rounds to 2^15, which int16 cannot hold), so
+        // -2^15 <= X < 2^15 and |x - X 2^(k-15)| <= 2^(k-15) <= 2^-14 m (half that where
+        // the cap does not act).  X is stored as the 16-bit pairs dp2a takes: per word of 8
+        // nibble codes (x0|x2, x4|x6, x1|x3, x5|x7) against its even and odd codes, per
+        // word of 4 byte codes (x0|x1, x2|x3).  A chunk with m < 2^-112 is staged as zero
+        // (an absolute error below 2^-112); one with a NaN or an infinity gets a NaN scale.
         constexpr int W = Fmt<FMT>::kW;                         // columns per chunk: 16 or 32
         uint32_t* xu = reinterpret_cast<uint32_t*>(smem);
         const int npairs = live * nchunks;
@@ -394,17 +410,17 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
                 finite = finite && (fabsf(v[i]) <= 3.402823466e38f);
             }
             const int e = int(__float_as_uint(m) >> 23);           // m in [2^(e-127), 2^(e-126))
-            const bool live_chunk = e >= 14;
-            // 2^(14-k) = 2^(140-e) and 2^(k-14) = 2^(e-140), k = e - 126, as float bits
-            const float up = live_chunk ? __uint_as_float(uint32_t(267 - e) << 23) : 0.f;
-            float down = live_chunk ? __uint_as_float(uint32_t(e - 13) << 23) : 0.f;
+            const bool live_chunk = e >= 15;
+            // 2^(15-k) = 2^(141-e) and 2^(k-15) = 2^(e-141), k = e - 126, as float bits
+            const float up = live_chunk ? __uint_as_float(uint32_t(268 - e) << 23) : 0.f;
+            float down = live_chunk ? __uint_as_float(uint32_t(e - 14) << 23) : 0.f;
             if (!finite) down = __uint_as_float(0x7FC00000u);
             float y[W];
             float sX = 0.f;
 #pragma unroll
             for (int i = 0; i < W; ++i) {
-                y[i] = __fmaf_rn(v[i], up, 12582912.0f);            // 1.5 * 2^23 + X
-                sX = __fadd_rn(sX, __fsub_rn(y[i], 12582912.0f));   // sum of X, exact
+                y[i] = fminf(__fmaf_rn(v[i], up, 12582912.0f), 12615679.0f);   // 1.5 * 2^23 + X, X <= 32767
+                sX = __fadd_rn(sX, __fsub_rn(y[i], 12582912.0f));              // sum of X, exact
             }
             uint32_t* dst = xu + (c * kCS + t * S) * 4;
             if constexpr (FMT == QG_Q8_0) {
@@ -558,9 +574,9 @@ __device__ __forceinline__ void step_fp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, uin
 // each byte), and per token four dp2a add the 8 products of the word's staged 16-bit x
 // pairs into an int32 (exact).  Q8_0: the chunk is 16 byte codes q + 128, taken by
 // dp2a as they are.  The sums start at -128 / -8 / -16 * sum(X) (Q8_0 / Q4_0 / Q5_0),
-// which removes the code offset exactly; the chunk then adds (I2F(sum) * 2^(k-14)) * d,
-// and the affine format also b * sum(x).  (|sum| < 2^24 for the 4-bit formats, so the
-// I2F is exact; a Q8_0 or Q5_0 chunk sum can exceed 2^24 and then rounds to 24 bits.)
+// which removes the code offset exactly; the chunk then adds (I2F(sum) * 2^(k-15)) * d,
+// and the affine format also b * sum(x).  (|sum| <= 2^24 for the 4- and 5-bit formats,
+// so the I2F is exact; a Q8_0 chunk sum can reach 2^26 and then rounds to 24 bits.)
 // The order of additions is fixed per lane and chunk.
 __device__ __forceinline__ int dp2a_lo(uint32_t x, uint32_t q, int c) {
     int d;
@@ -587,7 +603,7 @@ __device__ __forceinline__ void step_idp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
         sv[r] = F::scale(scales + r * kFullStep);
         if constexpr (FMT == QG_Q5_0) hv[r] = F::high(scales + r * kFullStep);
     }
-    const uint4 pk = lds128(xr + 16u * uint32_t(XT * S));         // 2^(k-14) per token
+    const uint4 pk = lds128(xr + 16u * uint32_t(XT * S));         // 2^(k-15) per token
     const uint4 pb = lds128(xr + 16u * uint32_t(XT * S + 1));     // Q4_0: -8 sum(X); affine: sum(x)
     const uint32_t pkv[4] = {pk.x, pk.y, pk.z, pk.w};
     const uint32_t pbv[4] = {pb.x, pb.y, pb.z, pb.w};
@@ -648,7 +664,7 @@ __device__ __forceinline__ void step_idp(Acc<FMT, NTOK, RPW>& A, uint32_t xr, ui
             }
         }
     }
-    // Per token: (affine) A += b * sum(x); then A += (I2F(sum) * 2^(k-14)) * scale (the
+    // Per token: (affine) A += b * sum(x); then A += (I2F(sum) * 2^(k-15)) * scale (the
     // product with the power of two is exact).
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
@@ -781,6 +797,13 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
         if (++si == depth) si = 0;
     };
 
+    // Profiling stamps (thread 0, only when a phase slot is given): entry, then
+    // SM cycles since entry at each phase.
+    unsigned long long* const ph = a.phase ? a.phase + size_t(blockIdx.x) * QG_PHASE_WORDS : nullptr;
+    const long long clk0 = clock64();
+    if (ph && threadIdx.x == 0) { ph[0] = global_ns(); ph[2] = sm_id(); }
+    auto stamp = [&](int k) { if (ph && threadIdx.x == 0) ph[k] = (unsigned long long)(clock64() - clk0); };
+
     // Programmatic dependent launch: let the next kernel in the stream start its
     // own weight copies as soon as SMs free up (a no-op without that launch mode).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -801,10 +824,16 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
     // The first copies read only W, which no earlier kernel writes (the caller's
     // promise when it enables the early start), so they go before the wait.
     for (int s = 0; s < depth; ++s) issue();
+    stamp(3);
+    // (profiling only) when warp 0's first stages land, seen before the wait below
+    if (ph && threadIdx.x == 0)
+        for (uint32_t s = 0; s < issued && s < 7u; ++s)
+            if (mbar_wait(bars + s * 8, 0u, limit)) stamp(9 + int(s));
 
     // Everything below may depend on the previous kernel in the stream (x, y, the
     // argmax workspace): wait for it to complete (a no-op without the early start).
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    stamp(4);
 
     // ---- stage x (overlaps the first copies)
     {
@@ -815,6 +844,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
         stage_x<FMT, NTOK>(smem, rows, n_in, spr);
     }
     __syncthreads();
+    stamp(5);
 
     float best_v = -INFINITY;
     int best_i = 0x7FFFFFFF;
@@ -834,6 +864,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
             failed = true;
             break;
         }
+        if (consumed == 0) stamp(6);
         ++consumed;
         // In a row's short last step the lanes past its codes read zero-filled or
         // scale bytes with a zero scale, against zero-padded x: they add exact zeros.
@@ -900,6 +931,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
             if (++sc == depth) { sc = 0; phase ^= 1u; }
         }
     }
+    stamp(7);
 
     if constexpr (ARGMAX) {
         // ---- per-token argmax: warp -> CTA partial -> last CTA reduces all partials
@@ -951,6 +983,10 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
             }
             if (threadIdx.x == 0) *a.ticket = 0u;   // ready for the next call on this workspace
         }
+    }
+    if (ph) {                  // uniform over the CTA
+        __syncthreads();
+        if (threadIdx.x == 0) { ph[8] = (unsigned long long)(clock64() - clk0); ph[1] = global_ns(); }
     }
 }
 

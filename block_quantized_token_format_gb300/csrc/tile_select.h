@@ -31,7 +31,7 @@ struct TileOverride {
 // added: every ntok and every tile of one matrix then give bitwise the same rows.
 int select_split(int fmt, int64_t n_out, int64_t n_in);
 
-constexpr int kMaxSplit = 4;
+constexpr int kMaxSplit = 8;
 
 // The geometry for a call, before the override and the occupancy cap.
 Tile select_tile(int fmt, int64_t n_out, int64_t n_in, int ntok);

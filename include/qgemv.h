@@ -352,7 +352,7 @@ qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t
  * with a heuristic fallback (the Track 2 audit's per-shape, per-ntok tile
  * rules are the prior art).  The reduction order never depends on this choice.
  *
- * The split P (1..4) is chosen per (fmt, n_out, n_in) only: a row's steps are
+ * The split P (1..8) is chosen per (fmt, n_out, n_in) only: a row's steps are
  * cut into P segments, one per warp of a team, and the segments' sums are added
  * in segment order.  P fixes the reduction order, so it never depends on ntok
  * or the geometry: for a given matrix every ntok and every geometry give
@@ -365,7 +365,7 @@ qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t
  * 3 and 5 for ntok 4 (QG_EUNSUPPORTED otherwise); where rpw * ntok > 20 (or
  * >= 16 with 4-bit codes at ntok >= 2) a CTA has at most 12 warps; depth in
  * {2..16}, warps in {1..16}, ctas in
- * {1..8}, split in {1..4}, gw in {0..64}: the expert calls' group weighting).  The
+ * {1..8}, split in {1..8}, gw in {0..64}: the expert calls' group weighting).  The
  * split is capped at one segment per step and
  * lowered until one team fits in shared memory at ntok = 4 (so it stays the
  * same for every ntok); warps are rounded to whole teams; the ring depth, then
@@ -415,6 +415,26 @@ qg_status qg_device_status(int clear, unsigned int* status);
  * the first expected transaction of every warp, so that wait can never
  * complete and the timeout path runs.  Process-wide; for tests only. */
 qg_status qg_set_wait_limit(uint32_t polls, uint32_t extra_tx_bytes);
+
+/* Profiling hook: per-CTA phase timestamps of the mat-vec kernel.  With `buf`
+ * non-null (device memory of `slots` * QG_PHASE_SLOT_WORDS uint64, 8-byte aligned,
+ * owned by the caller), every later qgemv / qgemv_argmax launch on this process
+ * takes the next slot (a process-wide counter modulo `slots`, advanced at launch
+ * time, so the launches of a captured graph keep distinct slots) and thread 0 of
+ * CTA b writes the QG_PHASE_WORDS words at slot * QG_PHASE_SLOT_WORDS +
+ * b * QG_PHASE_WORDS: [0] %globaltimer (ns) at entry, [1] %globaltimer when the
+ * CTA's warps are done, [2] %smid, [3..8] SM cycles (%clock64) since entry when
+ * warp 0 has issued its first copies, after the wait for the previous kernel,
+ * after x is staged, when warp 0's first ring stage has arrived, when warp 0 has
+ * finished its row groups, and when every warp is done; [9..15] SM cycles since
+ * entry when warp 0's ring stages 0..6 have landed, polled in order before the
+ * wait for the previous kernel (0 for stages warp 0 did not fill).  The
+ * launch then also ends with a CTA barrier.  `buf` = NULL turns the hook off
+ * (the default); the results are unchanged either way.  QG_EINVAL if slots < 1
+ * with a non-null buf.  For profiling only; the expert calls do not record. */
+#define QG_PHASE_WORDS 16
+#define QG_PHASE_SLOT_WORDS (4096 * QG_PHASE_WORDS)
+qg_status qg_set_phase_record(unsigned long long* buf, int64_t slots);
 
 #ifdef __cplusplus
 }

@@ -8,10 +8,11 @@ dequantization exactly: this pins the claim that the decode is exact and that th
 kernels' view of the device layout matches the packer's, before any GPU run.  The
 rule is restated here from the layout description, not taken from the kernel sources.
 
-The integer chunk dot also rounds x: per 32-column chunk and token, X = rn(x * 2^(14-k))
-with 2^(k-1) <= max|x| < 2^k.  test_x_rounding_bound pins the stated bound of that
-rounding (|X| <= 2^14, |x - X * 2^(k-14)| <= 2^-14 max|x|, the chunk sums of X exact in
-int32 and their I2F exact) on random and adversarial chunks, written from the rule."""
+The integer chunk dot also rounds x: per 32-column chunk and token, X = rn(x * 2^(15-k))
+capped at 32767, with 2^(k-1) <= max|x| < 2^k.  test_x_rounding_bound pins the stated bound
+of that rounding (X fits int16, |x - X * 2^(k-15)| <= 2^-14 max|x|, the chunk sums of X
+against 4-bit codes exact in int32 and in their I2F) on random and adversarial chunks,
+written from the rule."""
 from __future__ import annotations
 
 import numpy as np
@@ -83,16 +84,16 @@ def emulate_bytes(fmt, words, scales):
 
 
 def _round_chunk(x):
-    """The staging rule for one chunk of fp32 x: (X, 2^(k-14)), or zeros for a chunk whose
-    largest |x| is below 2^-113."""
+    """The staging rule for one chunk of fp32 x: (X, 2^(k-15)), or zeros for a chunk whose
+    largest |x| is below 2^-112."""
     x = np.asarray(x, dtype=np.float32)
     m = np.float32(np.max(np.abs(x)))
     e = int(m.view(np.uint32) >> 23)
-    if e < 14:
+    if e < 15:
         return np.zeros(x.shape, dtype=np.int64), 0.0
     k = e - 126
-    X = np.rint(x.astype(np.float64) * 2.0 ** (14 - k)).astype(np.int64)     # round half even
-    return X, 2.0 ** (k - 14)
+    X = np.rint(x.astype(np.float64) * 2.0 ** (15 - k)).astype(np.int64)     # round half even
+    return np.minimum(X, 32767), 2.0 ** (k - 15)
 
 
 def test_x_rounding_bound():
@@ -106,15 +107,18 @@ def test_x_rounding_bound():
     chunks.append(np.full(32, np.float32(np.nextafter(np.float32(4.0), np.float32(0)))))   # max just below 2^k
     chunks.append(np.full(32, np.float32(-4.0)))                                             # max exactly 2^(k-1)
     chunks.append(np.zeros(32, dtype=np.float32))
-    chunks.append(np.full(32, np.float32(1e-35)))                                            # below 2^-113: zero
+    chunks.append(np.full(32, np.float32(1e-35)))                                            # below 2^-112: zero
+    chunks.append(np.full(32, np.float32(2.0 ** -112)))                                       # the smallest live max
+    top = np.float32(np.nextafter(np.float32(8.0), np.float32(0)))
+    chunks.append(np.array([top, -top] * 16, dtype=np.float32))                              # rounds to +-2^15: capped
     for x in chunks:
         X, scale = _round_chunk(x)
         m = float(np.max(np.abs(x.astype(np.float64))))
-        assert np.all(np.abs(X) <= 2 ** 14)
+        assert np.all(X >= -2 ** 15) and np.all(X <= 2 ** 15 - 1)
         err = np.abs(x.astype(np.float64) - X * scale)
         assert np.all(err <= 2.0 ** -14 * m + (m if scale == 0.0 else 0.0)), (float(err.max()), m)
         if scale == 0.0:
-            assert m < 2.0 ** -113
+            assert m < 2.0 ** -112
         # chunk sums against 4-bit codes are exact in int32 and in the I2F to fp32
         s = int(np.sum(15 * np.abs(X)))
         assert s < 2 ** 24 and float(np.float32(s)) == s

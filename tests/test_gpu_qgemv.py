@@ -105,6 +105,66 @@ def test_workload_full(name):
     print(f"{name}: max normalised error {worst:.3g}")
 
 
+# ----------------------------------------------------------------------------- activations with outliers
+
+IDP_FMTS = ["q8_0", "q4_0", "affine4_g64", "q5_0"]      # x staged as 16-bit integers per chunk
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_outlier_activations(fmt):
+    """x shaped like a transformer hidden state: three massive channels (300..3000 against
+    N(0,1)) and eight moderate ones (10..40), at 1e-3 like every other case."""
+    n_out, n_in = 3000, n_in_for(fmt, 2560 if fmt != "affine4_g64" else 5120)
+    W = workloads.gaussian(71, (n_out, n_in), 0.02)
+    canon = ORC.quantize(fmt, W)
+    packed = upload(fmt, canon, n_out, n_in)
+    worst = 0.0
+    for seed in (72, 73, 74):
+        x = workloads.activations_with_outliers(seed, n_in, 4)
+        ref = ORC.gemv(fmt, canon, n_out, n_in, x)
+        den = ORC.gemv_abs(fmt, canon, n_out, n_in, x)
+        for ntok in (1, 4):
+            y = gpu_qgemv(fmt, packed, n_out, n_in, x[:ntok])
+            worst = max(worst, check_close(y, ref[:ntok], den[:ntok], f"{fmt} outliers seed={seed} ntok={ntok}"))
+    print(f"{fmt}: max normalised error with outlier channels {worst:.3g}")
+
+
+def x_rounding_bound(fmt, canon, n_out, n_in, x):
+    """The stated bound of the integer chunk dot's x rounding, per output: the sum over
+    chunks c (32 columns, 16 for Q8_0) of 2^-14 * max_c |x| * sum_c |w|."""
+    w = np.abs(ORC.dequantize(fmt, canon, n_out, n_in))
+    cw = 16 if fmt == "q8_0" else 32
+    m = np.abs(x.astype(np.float64)).reshape(x.shape[0], -1, cw).max(axis=2)      # [ntok, chunks]
+    sw = w.reshape(n_out, -1, cw).sum(axis=2)                                      # [n_out, chunks]
+    return 2.0 ** -14 * (m @ sw.T)
+
+
+@pytest.mark.parametrize("fmt", IDP_FMTS)
+def test_x_rounding_error_within_stated_bound(fmt):
+    """Where the weight mass sits far below a chunk's largest |x| (one entry 1e4, the rest
+    about 1e-2, the weights of the large entries zero), the x rounding can exceed 1e-3 of
+    sum|w x|.  The error must still respect the stated bound: the x-rounding term plus
+    2e-4 of sum|w x| for fp32 rounding."""
+    n_out, n_in = 500, n_in_for(fmt, 2560)
+    cw = 16 if fmt == "q8_0" else 32
+    W = workloads.gaussian(81, (n_out, n_in), 0.02)
+    big = np.arange(0, n_in, cw) + 5                  # one large entry per chunk
+    W[:, big] = 0.0
+    x = workloads.gaussian(82, (4, n_in), 1e-2)
+    x[:, big] = np.float32(1e4)
+    x[1, big] = np.float32(-7.5e3)
+    canon = ORC.quantize(fmt, W)
+    packed = upload(fmt, canon, n_out, n_in)
+    ref = ORC.gemv(fmt, canon, n_out, n_in, x)
+    den = ORC.gemv_abs(fmt, canon, n_out, n_in, x)
+    bound = x_rounding_bound(fmt, canon, n_out, n_in, x) + 2e-4 * den
+    y = gpu_qgemv(fmt, packed, n_out, n_in, x).astype(np.float64)
+    err = np.abs(y - ref)
+    assert np.all(err <= bound), (fmt, float((err / bound).max()))
+    print(f"{fmt}: adversarial x, max normalised error {float((err / np.maximum(den, 1e-300)).max()):.3g}, "
+          f"max error / bound {float((err / bound).max()):.3g}")
+
+
 # ----------------------------------------------------------------------------- invariances
 
 @pytest.mark.parametrize("fmt", FMTS)

@@ -12,7 +12,7 @@ ALLOWED = {
     "depth": set(range(2, 17)),
     "warps": set(range(1, 17)),
     "ctas": set(range(1, 9)),
-    "split": {1, 2, 3, 4},
+    "split": set(range(1, 9)),
     "gw": set(range(0, 65)),
 }
 

@@ -140,6 +140,22 @@ def activations(seed: int, n_in: int, ntok: int) -> np.ndarray:
     return np.ascontiguousarray(g.standard_normal((MAX_NTOK, n_in), dtype=np.float32)[:ntok])
 
 
+def activations_with_outliers(seed: int, n_in: int, ntok: int, n_massive: int = 3, massive=(300.0, 3000.0),
+                              n_moderate: int = 8, moderate=(10.0, 40.0)) -> np.ndarray:
+    """x as fp32 ``[ntok, n_in]`` shaped like a transformer's hidden state: N(0,1) per token
+    with a per-token scale in [0.5, 2], plus a few fixed "massive" channels (magnitude drawn
+    log-uniformly in `massive`, random sign per token) and some moderate outlier channels
+    (`moderate`), the channel indices shared by all tokens."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    x = g.standard_normal((ntok, n_in)).astype(np.float64) * g.uniform(0.5, 2.0, (ntok, 1))
+    ch = g.choice(n_in, n_massive + n_moderate, replace=False)
+    for j, c in enumerate(ch):
+        lo, hi = massive if j < n_massive else moderate
+        mag = np.exp(g.uniform(np.log(lo), np.log(hi), ntok))
+        x[:, c] = mag * np.where(g.random(ntok) < 0.5, -1.0, 1.0)
+    return np.ascontiguousarray(x.astype(np.float32))
+
+
 def gaussian(seed: int, shape, scale: float = 1.0) -> np.ndarray:
     """A generic seeded fp32 normal array for small test cases."""
     g = np.random.Generator(np.random.PCG64(seed))
