@@ -880,9 +880,8 @@ def phase_times(args):
     """Where a launch's time goes: each launch of a 20-launch graph (rotating over weight
     copies totalling >= 4x L2) records per CTA the global time at entry and exit and the SM
     cycles to warp 0's first copies issued, to the end of the wait for the previous kernel,
-    to x staged, to warp 0's first ring stage, to warp 0's last row group, to the CTA's
-    end, and to the landing of each of warp 0's first ring stages, polled before the wait
-    (recording only).  Reported per (workload,
+    to x staged, to warp 0's last row group, to the CTA's end, and to the landing of each
+    of warp 0's first ring stages, polled before the wait (recording only).  Reported per (workload,
     ntok, launch mode): medians over the launches of the per-launch medians over CTAs (in
     ns, cycles converted with the clock each CTA saw), the launch span (first entry to last
     exit), the overlap with the previous launch and the period (exit to exit)."""
@@ -919,6 +918,7 @@ def phase_times(args):
                 qg.qg_set_launch_options(flags)
                 us = time_graph(torch, call, n=n, reps=3)
                 # the captured launches take slots 0..n-1 in launch order
+                buf.zero_()
                 qg.qg_set_phase_record(buf, n)
                 try:
                     g = torch.cuda.CUDAGraph()
@@ -937,7 +937,11 @@ def phase_times(args):
                 del g
                 rec = buf.view(n, -1)[:, :grid * qg.QG_PHASE_WORDS].reshape(n, grid, qg.QG_PHASE_WORDS).cpu().numpy()
                 rec = rec.astype(np.float64)
-                t_in, t_out, sm, cyc = rec[:, :, 0], rec[:, :, 1], rec[:, :, 2], rec[:, :, 3:16]
+                t_in, t_out, sm = rec[:, :, 0], rec[:, :, 1], rec[:, :, 2]
+                raw = rec[:, :, 3:16].astype(np.int64)
+                # SM clock (32 bits) at each phase, relative to the entry clock in word 6
+                cyc = np.where(raw != 0, (raw - raw[:, :, 3:4]) % (1 << 32), 0).astype(np.float64)
+                cyc[:, :, 3] = 0.0
                 mhz = cyc[:, :, 5] / np.maximum(t_out - t_in, 1.0) * 1e3
                 ns = cyc / np.maximum(mhz[:, :, None], 1.0) * 1e3
                 start, end = t_in.min(axis=1), t_out.max(axis=1)

@@ -416,12 +416,13 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
             float down = live_chunk ? __uint_as_float(uint32_t(e - 14) << 23) : 0.f;
             if (!finite) down = __uint_as_float(0x7FC00000u);
             float y[W];
-            float sX = 0.f;
+            float sXf = 0.f;
 #pragma unroll
             for (int i = 0; i < W; ++i) {
                 y[i] = fminf(__fmaf_rn(v[i], up, 12582912.0f), 12615679.0f);   // 1.5 * 2^23 + X, X <= 32767
-                sX = __fadd_rn(sX, __fsub_rn(y[i], 12582912.0f));              // sum of X, exact
+                sXf = __fadd_rn(sXf, __fsub_rn(y[i], 12582912.0f));            // sum of X, exact
             }
+            const uint32_t sX = uint32_t(int(sXf));
             uint32_t* dst = xu + (c * kCS + t * S) * 4;
             if constexpr (FMT == QG_Q8_0) {
                 // byte codes: the pairs in column order, (x0|x1, x2|x3) per word of 4 codes
@@ -440,9 +441,9 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
             }
             uint32_t* pad = xu + (c * kCS + NTOK * S) * 4;
             pad[t] = __float_as_uint(down);
-            if constexpr (FMT == QG_Q8_0) pad[4 + t] = uint32_t(-128 * int(sX));
-            else if constexpr (FMT == QG_Q4_0) pad[4 + t] = uint32_t(-8 * int(sX));
-            else if constexpr (FMT == QG_Q5_0) pad[4 + t] = uint32_t(-16 * int(sX));
+            if constexpr (FMT == QG_Q8_0) pad[4 + t] = sX * uint32_t(-128);
+            else if constexpr (FMT == QG_Q4_0) pad[4 + t] = sX * uint32_t(-8);
+            else if constexpr (FMT == QG_Q5_0) pad[4 + t] = sX * uint32_t(-16);
             else pad[4 + t] = __float_as_uint(sx);
         };
         // Two pairs per thread and pass, both pairs' loads issued before either is
@@ -797,12 +798,16 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
         if (++si == depth) si = 0;
     };
 
-    // Profiling stamps (thread 0, only when a phase slot is given): entry, then
-    // SM cycles since entry at each phase.
-    unsigned long long* const ph = a.phase ? a.phase + size_t(blockIdx.x) * QG_PHASE_WORDS : nullptr;
-    const long long clk0 = clock64();
-    if (ph && threadIdx.x == 0) { ph[0] = global_ns(); ph[2] = sm_id(); }
-    auto stamp = [&](int k) { if (ph && threadIdx.x == 0) ph[k] = (unsigned long long)(clock64() - clk0); };
+    // Profiling stamps (thread 0, only when a phase slot is given): the SM clock at
+    // each phase (none inside the step loop; nothing stays live in registers).
+    auto stamp = [&](int k) {
+        if (a.phase && threadIdx.x == 0) a.phase[size_t(blockIdx.x) * QG_PHASE_WORDS + k] = uint32_t(clock());
+    };
+    stamp(6);
+    if (a.phase && threadIdx.x == 0) {
+        a.phase[size_t(blockIdx.x) * QG_PHASE_WORDS] = global_ns();
+        a.phase[size_t(blockIdx.x) * QG_PHASE_WORDS + 2] = sm_id();
+    }
 
     // Programmatic dependent launch: let the next kernel in the stream start its
     // own weight copies as soon as SMs free up (a no-op without that launch mode).
@@ -826,7 +831,7 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
     for (int s = 0; s < depth; ++s) issue();
     stamp(3);
     // (profiling only) when warp 0's first stages land, seen before the wait below
-    if (ph && threadIdx.x == 0)
+    if (a.phase && threadIdx.x == 0)
         for (uint32_t s = 0; s < issued && s < 7u; ++s)
             if (mbar_wait(bars + s * 8, 0u, limit)) stamp(9 + int(s));
 
@@ -864,7 +869,6 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
             failed = true;
             break;
         }
-        if (consumed == 0) stamp(6);
         ++consumed;
         // In a row's short last step the lanes past its codes read zero-filled or
         // scale bytes with a zero scale, against zero-padded x: they add exact zeros.
@@ -984,9 +988,10 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
             if (threadIdx.x == 0) *a.ticket = 0u;   // ready for the next call on this workspace
         }
     }
-    if (ph) {                  // uniform over the CTA
+    if (a.phase) {             // uniform over the CTA
         __syncthreads();
-        if (threadIdx.x == 0) { ph[8] = (unsigned long long)(clock64() - clk0); ph[1] = global_ns(); }
+        stamp(8);
+        if (threadIdx.x == 0) a.phase[size_t(blockIdx.x) * QG_PHASE_WORDS + 1] = global_ns();
     }
 }
 

@@ -423,12 +423,12 @@ qg_status qg_set_wait_limit(uint32_t polls, uint32_t extra_tx_bytes);
  * time, so the launches of a captured graph keep distinct slots) and thread 0 of
  * CTA b writes the QG_PHASE_WORDS words at slot * QG_PHASE_SLOT_WORDS +
  * b * QG_PHASE_WORDS: [0] %globaltimer (ns) at entry, [1] %globaltimer when the
- * CTA's warps are done, [2] %smid, [3..8] SM cycles (%clock64) since entry when
- * warp 0 has issued its first copies, after the wait for the previous kernel,
- * after x is staged, when warp 0's first ring stage has arrived, when warp 0 has
- * finished its row groups, and when every warp is done; [9..15] SM cycles since
- * entry when warp 0's ring stages 0..6 have landed, polled in order before the
- * wait for the previous kernel (0 for stages warp 0 did not fill).  The
+ * CTA's warps are done, [2] %smid; then the SM clock (%clock, 32 bits): [6] at
+ * entry, [3] when warp 0 has issued its first copies, [4] after the wait for the
+ * previous kernel, [5] after x is staged, [7] when warp 0 has finished its row
+ * groups, [8] when every warp is done, and [9..15] when warp 0's ring stages 0..6
+ * have landed, polled in order before the wait for the previous kernel (0 for
+ * stages warp 0 did not fill).  The
  * launch then also ends with a CTA barrier.  `buf` = NULL turns the hook off
  * (the default); the results are unchanged either way.  QG_EINVAL if slots < 1
  * with a non-null buf.  For profiling only; the expert calls do not record. */

@@ -156,6 +156,18 @@ def test_tile_override_grammar():
     assert lib.qg_set_tile_override(None) == 0
 
 
+def test_phase_record_arguments():
+    """The profiling hook validates on the host: a buffer needs at least one slot and 8-byte
+    alignment; NULL turns it off.  (No launch here: the buffers are never dereferenced.)"""
+    lib = qg.load_library()
+    lib.qg_set_phase_record.argtypes = [ctypes.c_void_p, ctypes.c_int64]
+    assert lib.qg_set_phase_record(None, 0) == 0
+    assert lib.qg_set_phase_record(0x10000, 0) == -1
+    assert lib.qg_set_phase_record(0x10004, 1) == -2
+    assert lib.qg_set_phase_record(None, 5) == 0
+    assert qg.QG_PHASE_WORDS == 16 and qg.QG_PHASE_SLOT_WORDS == 4096 * 16
+
+
 def test_launch_options():
     lib = qg.load_library()
     assert lib.qg_set_launch_options(1) == 0
