@@ -131,7 +131,8 @@ Tile select_expert_tile(int fmt, int64_t n_out, int64_t n_in) {
 int select_split(int fmt, int64_t n_out, int64_t n_in) {
     // Matrices with 8192 rows or more have row groups for every warp of the GPU
     // (at 4 rows per warp) and short rows gain nothing from a team (measured on
-    // GB300: a split of 2-3 costs 5-20% on 6144-12288 x 2560).  Few long rows
+    // GB300: splits of 2, 3 or 5 cost 5-15% at ntok 1 and 13-25% at ntok 4 on
+    // 10240-12288 x 2560, and gain at most 1-3% on 2560 x 2560).  Few long rows
     // (2560 x 6144: 12 steps a row, 640 groups for 2280 warps) leave most warps
     // idle while each active one walks its steps alone; a team of about one warp
     // per 4 steps gains ~20% there (split 3 on 2560 x 6144).

@@ -430,8 +430,11 @@ qg_status qg_set_wait_limit(uint32_t polls, uint32_t extra_tx_bytes);
  * have landed, polled in order before the wait for the previous kernel (0 for
  * stages warp 0 did not fill).  The
  * launch then also ends with a CTA barrier.  `buf` = NULL turns the hook off
- * (the default); the results are unchanged either way.  QG_EINVAL if slots < 1
- * with a non-null buf.  For profiling only; the expert calls do not record. */
+ * (the default); the results are unchanged either way.  The buffer must stay
+ * allocated until the hook is off and every launch that recorded into it has
+ * completed; launches captured into a CUDA graph while it is on keep their slots
+ * and record on every replay.  QG_EINVAL if slots < 1 with a non-null buf, QG_EALIGN if buf is not
+ * 8-byte aligned.  For profiling only; the expert calls do not record. */
 #define QG_PHASE_WORDS 16
 #define QG_PHASE_SLOT_WORDS (4096 * QG_PHASE_WORDS)
 qg_status qg_set_phase_record(unsigned long long* buf, int64_t slots);
