@@ -14,8 +14,9 @@ covers a real interval.  Also reported, outside the timed region:
   projection (the largest shapes), with GB/s, the fraction of the measured copy
   peak and, for the 4-bit head, the products per second against the FMA pipe's
   128 products per clock per SM;
-* per_workload: every other workload family x ntok, median of 5 graph replays of
-  50 launches rotating over weight copies totalling >= 4x L2;
+* per_workload: every other workload family x ntok, median of 7 graph replays (after 2
+  untimed ones) of max(200, copies) launches rotating over weight copies totalling
+  >= 4x L2;
 * e2e: the same step through the public API with host buffers, per call
   (pinned x uploaded, logits and argmax read back, host synchronized every step);
 * roofline of the dominant kernel, cpu_baseline (the fp64 oracle on the host's
@@ -225,8 +226,9 @@ def gen_packed(qg, w: workloads.Workload, threads: int = 16) -> np.ndarray:
     return out
 
 
-def time_graph(torch, call, n, reps=5):
-    """Median per-call microseconds of a graph of n calls (call(i), i < n), over reps replays."""
+def time_graph(torch, call, n, reps=5, warm=2):
+    """Median per-call microseconds of a graph of n calls (call(i), i < n), over reps replays
+    after `warm` untimed ones (a replay right after an idle host gap runs 5-10% slower)."""
     for i in range(3):
         call(i)
     torch.cuda.synchronize()
@@ -234,7 +236,8 @@ def time_graph(torch, call, n, reps=5):
     with torch.cuda.graph(g, capture_error_mode="thread_local"):
         for i in range(n):
             call(i)
-    g.replay()
+    for _ in range(max(1, warm)):
+        g.replay()
     times = []
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -449,7 +452,7 @@ def main_gpu(args, rank, world, local_rank):
     row = {}
     for ntok in NTOKS:
         us = time_graph(torch, lambda i, ntok=ntok: qg.qgemv(proj.fmt, pool[i % copies], proj.n_out, proj.n_in,
-                                                             px, py[:ntok], ntok), n=50)
+                                                             px, py[:ntok], ntok), n=200, reps=7)
         gbs = workloads_bytes(proj.fmt, proj.n_out, proj.n_in) / (us * 1e-6) / 1e9
         row[str(ntok)] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                           "frac_nominal_7900": round(gbs / 7900.0, 4)}
@@ -559,7 +562,8 @@ def main_gpu(args, rank, world, local_rank):
 
 def detail_table(args, qg, torch, dev, l2, peak, have=None):
     """Every workload x ntok except the headline heads (timed in config.per_config): median of
-    5 replays of a 50-launch graph over rotating copies.  `have`: packed matrices already on
+    7 replays of a graph of max(200, copies) launches over rotating copies (after 2 untimed
+    replays).  `have`: packed matrices already on
     the device, by workload name (the drafted-vocabulary variants reuse the full Q8_0 head)."""
     if args.detail_only:
         names = args.detail_only.split(",")
@@ -598,28 +602,12 @@ def detail_table(args, qg, torch, dev, l2, peak, have=None):
                     qg.qgemv_argmax(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y, am, wsp, ntok)
                 else:
                     qg.qgemv(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y, ntok)
-            n = 50
-            for i in range(copies + 2):
+            for i in range(copies + 2):        # every copy touched once before the capture
                 call(i)
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, capture_error_mode="thread_local"):
-                for i in range(n):
-                    call(i)
-            g.replay()
-            times = []
-            for _ in range(5):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                g.replay()
-                b.record()
-                torch.cuda.synchronize()
-                times.append(a.elapsed_time(b) / n * 1e3)
-            us = statistics.median(times)
+            us = time_graph(torch, call, n=max(200, copies), reps=7)
             gbs = wbytes / (us * 1e-6) / 1e9
             row[str(ntok)] = {"us": round(us, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                               "tile": qg.qg_describe_tile(w.fmt, w.n_out, w.n_in, ntok)}
-            del g
         table[name] = {"fmt": w.fmt, "n_out": w.n_out, "n_in": w.n_in, "weight_bytes": wbytes,
                        "call": "qgemv_argmax" if w.argmax else "qgemv", "copies": copies, "ntok": row}
         del pool
