@@ -131,8 +131,17 @@ def test_outlier_activations(fmt):
 
 def x_rounding_bound(fmt, canon, n_out, n_in, x):
     """The stated bound of the integer chunk dot's x rounding, per output: the sum over
-    chunks c (32 columns, 16 for Q8_0) of 2^-14 * max_c |x| * sum_c |w|."""
-    w = np.abs(ORC.dequantize(fmt, canon, n_out, n_in))
+    chunks c (32 columns, 16 for Q8_0) of 2^-14 * max_c |x| * sum_c |v|, where v is the
+    weight (Q8_0, Q4_0, Q5_0) or, for the affine format w = s q + b, the code part s q
+    (the bias multiplies the exact fp32 sum of x), bounded here by 15 |s|.  Affine
+    canonical bytes: n_out * n_in / 8 uint32 code words, then the fp16 scales s, then
+    the fp16 biases b, one per 64 weights."""
+    if fmt == "affine4_g64":
+        nw, ng = n_out * n_in // 8, n_out * n_in // 64
+        sc = np.asarray(canon, dtype=np.uint8)[nw * 4: nw * 4 + ng * 2].view("<f2").astype(np.float64)
+        w = np.repeat(15.0 * np.abs(sc).reshape(n_out, n_in // 64), 64, axis=1)
+    else:
+        w = np.abs(ORC.dequantize(fmt, canon, n_out, n_in))
     cw = 16 if fmt == "q8_0" else 32
     m = np.abs(x.astype(np.float64)).reshape(x.shape[0], -1, cw).max(axis=2)      # [ntok, chunks]
     sw = w.reshape(n_out, -1, cw).sum(axis=2)                                      # [n_out, chunks]
