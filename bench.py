@@ -864,6 +864,56 @@ def tile_sweep(args):
     qg.qg_set_tile_override(None)
 
 
+PHASE_KEYS = ["copies_issued", "wait_done", "x_staged", "first_stage", "warp0_done", "cta_done"] + \
+    [f"stage{k}_landed" for k in range(7)]
+
+
+def summarize_phases(rec) -> dict:
+    """Summary of the phase stamps of n launches x grid CTAs (rec: int64 [n, grid, 16], the
+    qg_set_phase_record layout: [0] entry and [1] exit globaltimer ns, [2] SM id, [6] the
+    entry SM clock, [3..5, 7..15] the SM clock at each phase, 32 bits, 0 = not reached).
+    Global times are taken relative to the first entry in integers (as float64, raw
+    globaltimer values would keep only ~256 ns).  Per CTA the SM clock rate is its cycles
+    from entry to its end over its global duration; phases are converted with it.  Medians
+    over launches of per-launch medians (and of per-launch maxima for *_max)."""
+    med = statistics.median
+    rec = np.asarray(rec, dtype=np.int64)
+    n = rec.shape[0]
+    base = int(rec[:, :, 0].min())
+    t_in = (rec[:, :, 0] - base).astype(np.float64)
+    t_out = (rec[:, :, 1] - base).astype(np.float64)
+    sm = rec[:, :, 2]
+    raw = rec[:, :, 3:16] & 0xFFFFFFFF
+    # SM clock (32 bits) at each phase, relative to the entry clock in word 6 (index 3 here)
+    cyc = np.where(raw != 0, (raw - raw[:, :, 3:4]) % (1 << 32), 0).astype(np.float64)
+    cyc[:, :, 3] = 0.0
+    mhz = cyc[:, :, 5] / np.maximum(t_out - t_in, 1.0) * 1e3
+    ns = cyc / np.maximum(mhz[:, :, None], 1.0) * 1e3
+    start, end = t_in.min(axis=1), t_out.max(axis=1)
+    out = {"sm_mhz": round(float(np.median(mhz)), 1)}
+    out["span_ns"] = round(float(med(list(end - start))), 1)
+    if n > 1:
+        out["overlap_prev_ns"] = round(float(med(list(end[:-1] - start[1:]))), 1)
+        out["period_ns"] = round(float(med(list(end[1:] - end[:-1]))), 1)
+    out["cta_entry_spread_ns"] = round(float(med(list(t_in.max(axis=1) - start))), 1)
+    out["cta_exit_spread_ns"] = round(float(med(list(end - t_out.min(axis=1)))), 1)
+    # per SM: first entry of launch i minus last exit of launch i-1 on the same SM
+    # (negative: the two launches' CTAs were resident on that SM together)
+    hand = []
+    for i in range(1, n):
+        for smv in np.unique(sm[i]):
+            prev = t_out[i - 1][sm[i - 1] == smv]
+            if prev.size:
+                hand.append(float(t_in[i][sm[i] == smv].min() - prev.max()))
+    out["sm_handoff_ns"] = round(float(med(hand)), 1) if hand else None
+    for j, key in enumerate(PHASE_KEYS):
+        if not np.any(cyc[:, :, j]):
+            continue
+        out[key + "_ns"] = round(float(med([med(list(ns[i, :, j])) for i in range(n)])), 1)
+        out[key + "_ns_max"] = round(float(med([float(ns[i, :, j].max()) for i in range(n)])), 1)
+    return out
+
+
 def phase_times(args):
     """Where a launch's time goes: each launch of a 20-launch graph (rotating over weight
     copies totalling >= 4x L2) records per CTA the global time at entry and exit and the SM
@@ -880,7 +930,6 @@ def phase_times(args):
     ntoks = [int(v) for v in args.sweep_ntoks.split(",")]
     dev = torch.device("cuda:0")
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    med = statistics.median
     for name in args.phases.split(","):
         w = workloads.WORKLOADS[name]
         base = torch.from_numpy(gen_packed(qg, w)).to(dev)
@@ -924,39 +973,9 @@ def phase_times(args):
                 us_rec = ev[0].elapsed_time(ev[1]) / n * 1e3
                 del g
                 rec = buf.view(n, -1)[:, :grid * qg.QG_PHASE_WORDS].reshape(n, grid, qg.QG_PHASE_WORDS).cpu().numpy()
-                rec = rec.astype(np.float64)
-                t_in, t_out, sm = rec[:, :, 0], rec[:, :, 1], rec[:, :, 2]
-                raw = rec[:, :, 3:16].astype(np.int64)
-                # SM clock (32 bits) at each phase, relative to the entry clock in word 6
-                cyc = np.where(raw != 0, (raw - raw[:, :, 3:4]) % (1 << 32), 0).astype(np.float64)
-                cyc[:, :, 3] = 0.0
-                mhz = cyc[:, :, 5] / np.maximum(t_out - t_in, 1.0) * 1e3
-                ns = cyc / np.maximum(mhz[:, :, None], 1.0) * 1e3
-                start, end = t_in.min(axis=1), t_out.max(axis=1)
                 out = {"name": name, "ntok": ntok, "mode": mode, "tile": desc, "us_per_launch": round(us, 3),
-                       "us_per_launch_recording": round(us_rec, 3), "gbs": round(wb / us / 1e3, 1),
-                       "sm_mhz": round(float(np.median(mhz)), 1)}
-                out["span_ns"] = round(float(med(list(end - start))), 1)
-                out["overlap_prev_ns"] = round(float(med(list(end[:-1] - start[1:]))), 1)
-                out["period_ns"] = round(float(med(list(end[1:] - end[:-1]))), 1)
-                out["cta_entry_spread_ns"] = round(float(med(list(t_in.max(axis=1) - start))), 1)
-                out["cta_exit_spread_ns"] = round(float(med(list(end - t_out.min(axis=1)))), 1)
-                # per SM: first entry of launch i minus last exit of launch i-1 on the same SM
-                # (negative: the two launches' CTAs were resident on that SM together)
-                hand = []
-                for i in range(1, n):
-                    for smv in np.unique(sm[i]):
-                        prev = t_out[i - 1][sm[i - 1] == smv]
-                        if prev.size:
-                            hand.append(float(t_in[i][sm[i] == smv].min() - prev.max()))
-                out["sm_handoff_ns"] = round(float(med(hand)), 1) if hand else None
-                keys = ["copies_issued", "wait_done", "x_staged", "first_stage", "warp0_done", "cta_done"]
-                keys += [f"stage{k}_landed" for k in range(7)]
-                for j, key in enumerate(keys):
-                    if not np.any(cyc[:, :, j]):
-                        continue
-                    out[key + "_ns"] = round(float(med([med(list(ns[i, :, j])) for i in range(n)])), 1)
-                    out[key + "_ns_max"] = round(float(med([float(ns[i, :, j].max()) for i in range(n)])), 1)
+                       "us_per_launch_recording": round(us_rec, 3), "gbs": round(wb / us / 1e3, 1)}
+                out.update(summarize_phases(rec))
                 print(json.dumps(out), flush=True)
         del pool, base, buf
         torch.cuda.empty_cache()
