@@ -231,6 +231,7 @@ qg_status plan_launch(int fmt, int64_t n_out, int64_t n_in, int ntok, bool argma
     plan->fn = fn;
     plan->tile = t;
     plan->tile.ctas = std::min(t.ctas, occ);
+    plan->tile.pre = t.pre <= 0 ? 1 : std::min(t.pre, t.depth);
     plan->grid = int(grid);
     plan->threads = threads;
     plan->smem = smem;
@@ -344,6 +345,7 @@ qg_status fill_common(KernelArgs& a, const Plan& p, int fmt, const void* W, int6
     a.drain_limit = std::max<uint32_t>(a.wait_limit, 1u << 16);
     a.test_extra_tx = g_test_extra_tx.load(std::memory_order_relaxed);
     a.stage_tx = uint32_t(p.tile.rpw * full_step_bytes(fmt));
+    a.pre = p.tile.pre;
     a.phase = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_phase_mu);

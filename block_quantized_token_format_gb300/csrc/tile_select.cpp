@@ -33,7 +33,11 @@ struct Entry {
 
 // Measured on GB300 (tile sweeps over rows per warp, ring depth, warps per CTA
 // and CTAs per SM, back-to-back launches with early start; the sweep summary is
-// in profiles/).  First match wins.
+// in profiles/).  First match wins.  The fifth value, where given, is `pre`: the ring
+// stages requested before the wait for the previous kernel (default one): the
+// 7 MB matrix gains 3-6% from requesting its whole ring at once, the BF16 matrix
+// ~10% from three of its five stages; elsewhere one stage is best or within 1% (the
+// affine head at ntok 2 and 4 keeps both stages: 0.2-0.3% ahead in a same-box A/B).
 const Entry kTable[] = {
     // Q8_0 (integer chunk dot), n_in 2560: LM heads
     {QG_Q8_0, 65536, INT64_MAX, 2560, 1, {8, 2, 12, 1}},
@@ -48,13 +52,13 @@ const Entry kTable[] = {
     {QG_Q8_0, 9000, 11263, 2560, 3, {6, 2, 16, 1}},
     {QG_Q8_0, 9000, 11263, 2560, 0, {6, 2, 12, 1}},
     // Q8_0, n_in 2560: 4096..8999 rows (the 6144 projection)
-    {QG_Q8_0, 4096, 8999, 2560, 1, {4, 2, 8, 2}},
+    {QG_Q8_0, 4096, 8999, 2560, 1, {4, 2, 8, 2, 2}},
     {QG_Q8_0, 4096, 8999, 2560, 3, {4, 2, 16, 1}},
     {QG_Q8_0, 4096, 8999, 2560, 0, {4, 2, 12, 1}},
     // Q8_0, n_in 2560: up to 4095 rows (2560 x 2560)
-    {QG_Q8_0, 1, 4095, 2560, 1, {2, 5, 12, 2}},
-    {QG_Q8_0, 1, 4095, 2560, 4, {2, 3, 16, 1}},
-    {QG_Q8_0, 1, 4095, 2560, 0, {4, 3, 16, 1}},
+    {QG_Q8_0, 1, 4095, 2560, 1, {2, 5, 12, 2, 5}},
+    {QG_Q8_0, 1, 4095, 2560, 4, {2, 3, 16, 1, 3}},
+    {QG_Q8_0, 1, 4095, 2560, 0, {4, 3, 16, 1, 3}},
     // Q8_0, n_in 6144, few rows (6144 -> 2560; split 3: 15 warps = 5 teams)
     {QG_Q8_0, 1, 8191, 6144, 1, {4, 3, 16, 1}},
     {QG_Q8_0, 1, 8191, 6144, 0, {4, 2, 16, 1}},
@@ -63,20 +67,20 @@ const Entry kTable[] = {
     {QG_Q4_0, 4096, 65535, 2560, 2, {8, 2, 6, 2}},
     {QG_Q4_0, 4096, 65535, 2560, 3, {8, 2, 8, 1}},
     {QG_Q4_0, 4096, 65535, 2560, 4, {5, 2, 16, 1}},
-    {QG_BF16, 4096, 65535, 2560, 1, {4, 5, 8, 2}},
-    {QG_BF16, 4096, 65535, 2560, 2, {4, 5, 8, 2}},
+    {QG_BF16, 4096, 65535, 2560, 1, {4, 5, 8, 2, 3}},
+    {QG_BF16, 4096, 65535, 2560, 2, {4, 5, 8, 2, 3}},
     {QG_BF16, 4096, 65535, 2560, 3, {4, 3, 16, 1}},
     {QG_BF16, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
     // Q5_0, 8192 x 2560 (magic-float decode; measured)
-    {QG_Q5_0, 4096, 65535, 2560, 1, {2, 3, 16, 1}},
+    {QG_Q5_0, 4096, 65535, 2560, 1, {2, 3, 16, 1, 3}},
     {QG_Q5_0, 4096, 65535, 2560, 2, {8, 2, 6, 2}},
     {QG_Q5_0, 4096, 65535, 2560, 3, {2, 3, 16, 1}},
     {QG_Q5_0, 4096, 65535, 2560, 4, {5, 2, 12, 1}},
     // affine 4-bit LM head (integer chunk dot)
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {8, 2, 12, 1}},
-    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {6, 2, 16, 1}},
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {6, 2, 16, 1, 2}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 3, {8, 2, 12, 1}},
-    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 4, {5, 2, 16, 1}},
+    {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 4, {5, 2, 16, 1, 2}},
 };
 
 }  // namespace
@@ -148,6 +152,7 @@ Tile apply_override(Tile t, const TileOverride& o) {
     if (o.depth > 0) t.depth = o.depth;
     if (o.warps > 0) t.warps = o.warps;
     if (o.ctas > 0) t.ctas = o.ctas;
+    if (o.pre > 0) t.pre = o.pre;
     if (o.split > 0) t.split = o.split;
     if (o.gw >= 0) t.gw = o.gw;
     return t;
@@ -174,6 +179,7 @@ bool parse_tile_spec(const char* spec, TileOverride* out) {
         else if (key == "depth") { if (!depth_ok(v)) return false; o.depth = v; }
         else if (key == "warps") { if (v < 1 || v > 16) return false; o.warps = v; }
         else if (key == "ctas") { if (v < 1 || v > 8) return false; o.ctas = v; }
+        else if (key == "pre") { if (!depth_ok(v) && v != 1) return false; o.pre = v; }
         else if (key == "split") { if (v < 1 || v > kMaxSplit) return false; o.split = v; }
         else if (key == "gw") { if (v > 64) return false; o.gw = v; }
         else return false;
@@ -184,8 +190,8 @@ bool parse_tile_spec(const char* spec, TileOverride* out) {
 
 std::string tile_to_string(const Tile& t) {
     char b[96];
-    std::snprintf(b, sizeof b, "rpw=%d,depth=%d,warps=%d,ctas=%d,split=%d", t.rpw, t.depth, t.warps, t.ctas,
-                  t.split);
+    std::snprintf(b, sizeof b, "rpw=%d,depth=%d,warps=%d,ctas=%d,pre=%d,split=%d", t.rpw, t.depth, t.warps,
+                  t.ctas, t.pre, t.split);
     return b;
 }
 

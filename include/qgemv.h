@@ -360,12 +360,14 @@ qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t
  * few row groups per warp use about one segment per three steps.)
  *
  * qg_set_tile_override: force a geometry for later calls, e.g.
- * "rpw=4,depth=4,warps=8,ctas=2,split=2,gw=4" (any subset of the keys; rpw in
+ * "rpw=4,depth=4,warps=8,ctas=2,pre=1,split=2,gw=4" (any subset of the keys; rpw in
  * {1,2,3,4,5,6,8}: 1, 2, 4 for every ntok, 8 for ntok <= 3, 6 for ntok 2-4,
  * 3 and 5 for ntok 4 (QG_EUNSUPPORTED otherwise); where rpw * ntok > 20 (or
  * >= 16 with 4-bit codes at ntok >= 2) a CTA has at most 12 warps; depth in
- * {2..16}, warps in {1..16}, ctas in
- * {1..8}, split in {1..8}, gw in {0..64}: the expert calls' group weighting).  The
+ * {2..16}, warps in {1..16}, ctas in {1..8}, pre in {1..16}: the ring stages each
+ * warp requests before the wait for the previous kernel, the rest once x is
+ * staged (capped at depth), split in {1..8}, gw in {0..64}: the expert calls'
+ * group weighting).  The
  * split is capped at one segment per step and
  * lowered until one team fits in shared memory at ntok = 4 (so it stays the
  * same for every ntok); warps are rounded to whole teams; the ring depth, then
@@ -377,7 +379,7 @@ qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t
  * (the override is unchanged).
  *
  * qg_describe_tile: writes the geometry a call would use into buf as
- * "rpw=..,depth=..,warps=..,ctas=..,split=..,grid=.." (NUL-terminated,
+ * "rpw=..,depth=..,warps=..,ctas=..,pre=..,split=..,grid=.." (NUL-terminated,
  * truncated to len). */
 qg_status qg_set_tile_override(const char* spec);
 qg_status qg_describe_tile(qg_fmt fmt, int64_t n_out, int64_t n_in, int ntok,

@@ -148,10 +148,10 @@ def test_expert_layer_rejects_before_launch():
 
 def test_tile_override_grammar():
     lib = qg.load_library()
-    for good in (b"rpw=4", b"depth=2,rpw=1", b"rpw=2,depth=4,warps=8,ctas=2", b"", None, b"rpw=1,", b"rpw=8", b"split=3,rpw=2", b"split=5", b"split=8", b"rpw=3", b"rpw=5", b"rpw=6", b"gw=0", b"gw=4,rpw=2", b"gw=64"):
+    for good in (b"rpw=4", b"depth=2,rpw=1", b"rpw=2,depth=4,warps=8,ctas=2", b"", None, b"rpw=1,", b"rpw=8", b"split=3,rpw=2", b"split=5", b"split=8", b"pre=1", b"pre=16,depth=16", b"rpw=3", b"rpw=5", b"rpw=6", b"gw=0", b"gw=4,rpw=2", b"gw=64"):
         assert lib.qg_set_tile_override(good) == 0, good
     for bad in (b"rpw=7", b"rpw=9", b"rpw=0", b"depth=1", b"depth=17", b"warps=0", b"warps=17", b"ctas=0", b"foo=1", b"rpw", b"rpw=x",
-                b"rpw=-1", b"pf=2", b"split=0", b"split=9", b"gw=65", b"gw=-1"):
+                b"rpw=-1", b"pf=2", b"split=0", b"split=9", b"pre=0", b"pre=17", b"gw=65", b"gw=-1"):
         assert lib.qg_set_tile_override(bad) == -1, bad
     assert lib.qg_set_tile_override(None) == 0
 

@@ -12,6 +12,7 @@ ALLOWED = {
     "depth": set(range(2, 17)),
     "warps": set(range(1, 17)),
     "ctas": set(range(1, 9)),
+    "pre": set(range(1, 17)),
     "split": set(range(1, 9)),
     "gw": set(range(0, 65)),
 }
