@@ -832,8 +832,8 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
     // promise when it enables the early start), so they go before the wait.  Only the
     // first `pre` stages do: the rest of the ring is requested once x is staged, so that
     // the loads of x after the wait do not queue behind the whole initial burst of
-    // weights (measured on GB300: 2-7% faster on 10-33 MB matrices with pre = 1, while
-    // matrices of a few MB gain from requesting their whole share at once).
+    // weights (measured on GB300: 1.5-5% faster on 7-33 MB projections at ntok 2-4 with
+    // pre = 1; the tile table keeps the whole ring where that was ahead).
     for (int s = 0; s < a.pre; ++s) issue();
     stamp(3);
     // (profiling only) when warp 0's first stages land, seen before the wait below
@@ -854,9 +854,9 @@ __global__ void __launch_bounds__(MaxThreads<FMT, NTOK, RPW>::value, 1) qgemv_ke
         for (int t = 0; t < NTOK; ++t) rows[t] = x4 + t * n4;
         stage_x<FMT, NTOK>(smem, rows, n_in, spr);
     }
-    for (int s = a.pre; s < depth; ++s) issue();
     __syncthreads();
     stamp(5);
+    for (int s = a.pre; s < depth; ++s) issue();
 
     float best_v = -INFINITY;
     int best_i = 0x7FFFFFFF;

@@ -35,20 +35,22 @@ struct Entry {
 // and CTAs per SM, back-to-back launches with early start; the sweep summary is
 // in profiles/).  First match wins.  The fifth value, where given, is `pre`: the ring
 // stages requested before the wait for the previous kernel (default one): the
-// 7 MB matrix gains 3-6% from requesting its whole ring at once, the BF16 matrix
-// ~10% from three of its five stages; elsewhere one stage is best or within 1% (the
-// affine head at ntok 2 and 4 keeps both stages: 0.2-0.3% ahead in a same-box A/B).
+// Q8_0 / Q4_0 / Q5_0 / BF16 projections at ntok 2-4 gain 1.5-5% from one stage (same-box
+// A/B against the whole ring); the 2560 x 2560 matrix, the 10240 / 12288-row ones at
+// ntok 1, BF16 at ntok 1 and the heads at ntok 2-4 keep more (the whole ring was 1-3%
+// ahead there).
 const Entry kTable[] = {
     // Q8_0 (integer chunk dot), n_in 2560: LM heads
     {QG_Q8_0, 65536, INT64_MAX, 2560, 1, {8, 2, 12, 1}},
     {QG_Q8_0, 65536, INT64_MAX, 2560, 2, {6, 2, 16, 1}},
-    {QG_Q8_0, 65536, INT64_MAX, 2560, 3, {4, 3, 16, 1}},
+    {QG_Q8_0, 65536, INT64_MAX, 2560, 3, {4, 3, 16, 1, 3}},
     {QG_Q8_0, 65536, INT64_MAX, 2560, 4, {5, 2, 16, 1}},
     // Q8_0, n_in 2560: 11264..65535 rows (the 12288 projection)
     {QG_Q8_0, 11264, 65535, 2560, 4, {4, 2, 12, 1}},
+    {QG_Q8_0, 11264, 65535, 2560, 1, {8, 2, 12, 1, 2}},
     {QG_Q8_0, 11264, 65535, 2560, 0, {8, 2, 12, 1}},
     // Q8_0, n_in 2560: 9000..11263 rows (the 10240 projection)
-    {QG_Q8_0, 9000, 11263, 2560, 1, {4, 2, 12, 2}},
+    {QG_Q8_0, 9000, 11263, 2560, 1, {4, 2, 12, 2, 2}},
     {QG_Q8_0, 9000, 11263, 2560, 3, {6, 2, 16, 1}},
     {QG_Q8_0, 9000, 11263, 2560, 0, {6, 2, 12, 1}},
     // Q8_0, n_in 2560: 4096..8999 rows (the 6144 projection)
@@ -67,11 +69,11 @@ const Entry kTable[] = {
     {QG_Q4_0, 4096, 65535, 2560, 2, {8, 2, 6, 2}},
     {QG_Q4_0, 4096, 65535, 2560, 3, {8, 2, 8, 1}},
     {QG_Q4_0, 4096, 65535, 2560, 4, {5, 2, 16, 1}},
-    {QG_BF16, 4096, 65535, 2560, 1, {4, 5, 8, 2, 3}},
+    {QG_BF16, 4096, 65535, 2560, 1, {4, 5, 8, 2, 5}},
     {QG_BF16, 4096, 65535, 2560, 2, {4, 5, 8, 2, 3}},
     {QG_BF16, 4096, 65535, 2560, 3, {4, 3, 16, 1}},
     {QG_BF16, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
-    // Q5_0, 8192 x 2560 (magic-float decode; measured)
+    // Q5_0, 8192 x 2560 (integer chunk dot; measured)
     {QG_Q5_0, 4096, 65535, 2560, 1, {2, 3, 16, 1, 3}},
     {QG_Q5_0, 4096, 65535, 2560, 2, {8, 2, 6, 2}},
     {QG_Q5_0, 4096, 65535, 2560, 3, {2, 3, 16, 1}},
