@@ -142,6 +142,7 @@ qg_status plan_experts(int fmt, int64_t n_out, int64_t n_in, Plan* plan) {
     plan->fn = fn;
     plan->tile = t;
     plan->tile.ctas = std::min(t.ctas, occ);
+    plan->tile.pre = t.depth;    // the expert kernels request a group's whole ring at once
     plan->grid = int(grid);
     plan->threads = threads;
     plan->smem = smem;
