@@ -811,8 +811,9 @@ def reference_arm(args, rank, world):
 
 
 def tile_sweep(args):
-    """GB/s per (workload, ntok, tile spec): each point is the median of 3 replays of a
-    graph of at least 20 launches rotating over weight copies totalling >= 4x L2 (set
+    """GB/s per (workload, ntok, tile spec): each point is the median of 3 replays (after 2
+    untimed ones) of a graph of at least 100 launches rotating over weight copies
+    totalling >= 4x L2 (set
     QGEMV_EARLY_START=1 to sweep with early-start launches).  The table in
     csrc/tile_select.cpp was filled from such sweeps."""
     import itertools
@@ -851,7 +852,7 @@ def tile_sweep(args):
                         qg.qgemv_argmax(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y[:ntok], am, ws, ntok)
                     else:
                         qg.qgemv(w.fmt, pool[i % copies], w.n_out, w.n_in, x, y[:ntok], ntok)
-                us = time_graph(torch, call, n=max(20, copies), reps=3)
+                us = time_graph(torch, call, n=max(100, copies), reps=3)
                 rec = {"name": name, "ntok": ntok, "spec": spec, "desc": desc, "us": round(us, 3),
                        "gbs": round(wb / us / 1e3, 1)}
                 out.write(json.dumps(rec) + "\n")

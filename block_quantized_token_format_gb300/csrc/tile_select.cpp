@@ -47,14 +47,14 @@ const Entry kTable[] = {
     {QG_Q8_0, 65536, INT64_MAX, 2560, 4, {5, 2, 16, 1}},
     // Q8_0, n_in 2560: 11264..65535 rows (the 12288 projection)
     {QG_Q8_0, 11264, 65535, 2560, 4, {4, 2, 12, 1}},
-    {QG_Q8_0, 11264, 65535, 2560, 1, {8, 2, 12, 1, 2}},
+    {QG_Q8_0, 11264, 65535, 2560, 1, {8, 3, 12, 1, 1}},
     {QG_Q8_0, 11264, 65535, 2560, 0, {8, 2, 12, 1}},
     // Q8_0, n_in 2560: 9000..11263 rows (the 10240 projection)
-    {QG_Q8_0, 9000, 11263, 2560, 1, {4, 2, 12, 2, 2}},
+    {QG_Q8_0, 9000, 11263, 2560, 1, {8, 3, 12, 1, 1}},
     {QG_Q8_0, 9000, 11263, 2560, 3, {6, 2, 16, 1}},
     {QG_Q8_0, 9000, 11263, 2560, 0, {6, 2, 12, 1}},
     // Q8_0, n_in 2560: 4096..8999 rows (the 6144 projection)
-    {QG_Q8_0, 4096, 8999, 2560, 1, {4, 2, 8, 2, 2}},
+    {QG_Q8_0, 4096, 8999, 2560, 1, {4, 2, 12, 1, 1}},
     {QG_Q8_0, 4096, 8999, 2560, 3, {4, 2, 16, 1}},
     {QG_Q8_0, 4096, 8999, 2560, 0, {4, 2, 12, 1}},
     // Q8_0, n_in 2560: up to 4095 rows (2560 x 2560)
@@ -65,8 +65,8 @@ const Entry kTable[] = {
     {QG_Q8_0, 1, 8191, 6144, 1, {4, 3, 16, 1}},
     {QG_Q8_0, 1, 8191, 6144, 0, {4, 2, 16, 1}},
     // Q4_0 (integer chunk dot) and BF16, 8192 x 2560
-    {QG_Q4_0, 4096, 65535, 2560, 1, {8, 2, 8, 2}},
-    {QG_Q4_0, 4096, 65535, 2560, 2, {8, 2, 6, 2}},
+    {QG_Q4_0, 4096, 65535, 2560, 1, {4, 2, 16, 1}},
+    {QG_Q4_0, 4096, 65535, 2560, 2, {8, 2, 12, 1}},
     {QG_Q4_0, 4096, 65535, 2560, 3, {8, 2, 8, 1}},
     {QG_Q4_0, 4096, 65535, 2560, 4, {5, 2, 16, 1}},
     {QG_BF16, 4096, 65535, 2560, 1, {4, 5, 8, 2, 5}},
