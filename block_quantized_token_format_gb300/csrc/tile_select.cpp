@@ -58,9 +58,10 @@ const Entry kTable[] = {
     {QG_Q8_0, 4096, 8999, 2560, 3, {4, 2, 16, 1}},
     {QG_Q8_0, 4096, 8999, 2560, 0, {4, 2, 12, 1}},
     // Q8_0, n_in 2560: up to 4095 rows (2560 x 2560)
-    {QG_Q8_0, 1, 4095, 2560, 1, {2, 5, 12, 2, 5}},
+    {QG_Q8_0, 1, 4095, 2560, 1, {4, 4, 12, 1, 4}},
+    {QG_Q8_0, 1, 4095, 2560, 2, {2, 4, 12, 1, 4}},
+    {QG_Q8_0, 1, 4095, 2560, 3, {2, 4, 16, 1, 4}},
     {QG_Q8_0, 1, 4095, 2560, 4, {2, 3, 16, 1, 3}},
-    {QG_Q8_0, 1, 4095, 2560, 0, {4, 3, 16, 1, 3}},
     // Q8_0, n_in 6144, few rows (6144 -> 2560; split 3: 15 warps = 5 teams)
     {QG_Q8_0, 1, 8191, 6144, 1, {4, 3, 16, 1}},
     {QG_Q8_0, 1, 8191, 6144, 0, {4, 2, 16, 1}},
@@ -74,10 +75,10 @@ const Entry kTable[] = {
     {QG_BF16, 4096, 65535, 2560, 3, {4, 3, 16, 1}},
     {QG_BF16, 4096, 65535, 2560, 4, {4, 2, 16, 1}},
     // Q5_0, 8192 x 2560 (integer chunk dot; measured)
-    {QG_Q5_0, 4096, 65535, 2560, 1, {2, 3, 16, 1, 3}},
-    {QG_Q5_0, 4096, 65535, 2560, 2, {8, 2, 6, 2}},
-    {QG_Q5_0, 4096, 65535, 2560, 3, {2, 3, 16, 1}},
-    {QG_Q5_0, 4096, 65535, 2560, 4, {5, 2, 12, 1}},
+    {QG_Q5_0, 4096, 65535, 2560, 1, {8, 2, 12, 1}},
+    {QG_Q5_0, 4096, 65535, 2560, 2, {8, 2, 12, 1}},
+    {QG_Q5_0, 4096, 65535, 2560, 3, {4, 3, 16, 1}},
+    {QG_Q5_0, 4096, 65535, 2560, 4, {4, 3, 16, 1}},
     // affine 4-bit LM head (integer chunk dot)
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 1, {8, 2, 12, 1}},
     {QG_AFFINE4_G64, 65536, INT64_MAX, 0, 2, {6, 2, 16, 1, 2}},
