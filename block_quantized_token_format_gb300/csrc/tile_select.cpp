@@ -35,10 +35,10 @@ struct Entry {
 // and CTAs per SM, back-to-back launches with early start; the sweep summary is
 // in profiles/).  First match wins.  The fifth value, where given, is `pre`: the ring
 // stages requested before the wait for the previous kernel (default one): the
-// Q8_0 / Q4_0 / Q5_0 / BF16 projections at ntok 2-4 gain 1.5-5% from one stage (same-box
-// A/B against the whole ring); the 2560 x 2560 matrix, the 10240 / 12288-row ones at
-// ntok 1, BF16 at ntok 1 and the heads at ntok 2-4 keep more (the whole ring was 1-3%
-// ahead there).
+// Q8_0 / Q4_0 / Q5_0 / BF16 projections gain 1.5-12% from one stage (same-box A/B
+// against the whole ring, after retuning the geometry for it); the 2560 x 2560 matrix,
+// BF16 at ntok 1-2 and the heads at ntok 2-4 keep more (the whole ring was 1-5% ahead
+// there).
 const Entry kTable[] = {
     // Q8_0 (integer chunk dot), n_in 2560: LM heads
     {QG_Q8_0, 65536, INT64_MAX, 2560, 1, {8, 2, 12, 1}},
