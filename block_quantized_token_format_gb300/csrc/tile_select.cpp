@@ -146,7 +146,7 @@ int select_split(int fmt, int64_t n_out, int64_t n_in) {
     const int64_t spr = steps_per_row(fmt, n_in);
     if (n_out >= 8192 || spr <= 6) return 1;
     int64_t p = (spr + 3) / 4;
-    if (p > kMaxSplit) p = kMaxSplit;
+    if (p > 4) p = 4;          // measured up to 4; larger splits only through the override
     return int(p);
 }
 
