@@ -359,6 +359,40 @@ __host__ __device__ inline SmemPlan smem_plan(int fmt, int ntok, int n_in, int r
 // ------------------------------------------------------------------------------ kernel pieces
 // Shared by the mat-vec kernel and the expert-grouped kernel.
 
+// The rounding of one (chunk, token) pair of x for the integer chunk dot: with
+// m = max|v| over the chunk's W values and 2^(k-1) <= m < 2^k, y[i] = 1.5 * 2^23 + X_i
+// where X_i = rn(v_i * 2^(15-k)) capped at 32767 (formed exactly by one FMA: the integer
+// sits in the low bits of the sum, round to nearest even; a value within 2^-16 m of 2^k
+// rounds to 2^15, which int16 cannot hold), so -2^15 <= X_i < 2^15 and
+// |v_i - X_i 2^(k-15)| <= 2^(k-15) <= 2^-14 m (half that where the cap does not act).
+// down = 2^(k-15) (0 for a chunk with m < 2^-112, staged as zero; NaN where a value is
+// not finite), sx = the fp32 sum of v in column order, sXf = the sum of X (exact).
+template <int W>
+__device__ __forceinline__ void round_chunk(const float (&v)[W], float (&y)[W], float& down, float& sx,
+                                            float& sXf) {
+    float m = 0.f;
+    sx = 0.f;
+    bool finite = true;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        m = fmaxf(m, fabsf(v[i]));
+        sx = __fadd_rn(sx, v[i]);
+        finite = finite && (fabsf(v[i]) <= 3.402823466e38f);
+    }
+    const int e = int(__float_as_uint(m) >> 23);           // m in [2^(e-127), 2^(e-126))
+    const bool live_chunk = e >= 15;
+    // 2^(15-k) = 2^(141-e) and 2^(k-15) = 2^(e-141), k = e - 126, as float bits
+    const float up = live_chunk ? __uint_as_float(uint32_t(268 - e) << 23) : 0.f;
+    down = live_chunk ? __uint_as_float(uint32_t(e - 14) << 23) : 0.f;
+    if (!finite) down = __uint_as_float(0x7FC00000u);
+    sXf = 0.f;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        y[i] = fminf(__fmaf_rn(v[i], up, 12582912.0f), 12615679.0f);   // 1.5 * 2^23 + X, X <= 32767
+        sXf = __fadd_rn(sXf, __fsub_rn(y[i], 12582912.0f));            // sum of X, exact
+    }
+}
+
 // Stage x rows[0..live-1] (each n_in fp32, 16-byte aligned) into the chunk-interleaved
 // layout for NTOK tokens at `smem` (see SmemPlan), zero past n_in up to whole steps;
 // the slots of tokens live..NTOK-1 are left as they are.  Each thread issues all its
@@ -380,15 +414,11 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
     const int nt = int(blockDim.x);
     if constexpr (IsIdp<FMT>::value) {
         // One (chunk, token) pair per thread and pass: the chunk's values (32 columns, 16
-        // for Q8_0) are loaded at once; with m = max|x| over them and 2^(k-1) <= m < 2^k,
-        // X = rn(x * 2^(15-k)) is formed exactly by one FMA with 1.5 * 2^23 (the integer
-        // sits in the low bits of the sum, round to nearest even) and capped at 32767 (a
-        // value within 2^-16 m of 2^k rounds to 2^15, which int16 cannot hold), so
-        // -2^15 <= X < 2^15 and |x - X 2^(k-15)| <= 2^(k-15) <= 2^-14 m (half that where
-        // the cap does not act).  X is stored as the 16-bit pairs dp2a takes: per word of 8
-        // nibble codes (x0|x2, x4|x6, x1|x3, x5|x7) against its even and odd codes, per
-        // word of 4 byte codes (x0|x1, x2|x3).  A chunk with m < 2^-112 is staged as zero
-        // (an absolute error below 2^-112); one with a NaN or an infinity gets a NaN scale.
+        // for Q8_0) are loaded at once and rounded to 16-bit integers X (round_chunk).  X
+        // is stored as the 16-bit pairs dp2a takes: per word of 8 nibble codes (x0|x2,
+        // x4|x6, x1|x3, x5|x7) against its even and odd codes, per word of 4 byte codes
+        // (x0|x1, x2|x3).  A chunk with m < 2^-112 is staged as zero (an absolute error
+        // below 2^-112); one with a NaN or an infinity gets a NaN scale.
         constexpr int W = Fmt<FMT>::kW;                         // columns per chunk: 16 or 32
         uint32_t* xu = reinterpret_cast<uint32_t*>(smem);
         const int npairs = live * nchunks;
@@ -403,27 +433,9 @@ __device__ __forceinline__ void stage_x(unsigned char* smem, const float4* const
         };
         // Round, pack and store one pair's values.
         auto put = [&](const float (&v)[W], int t, int c) {
-            float m = 0.f, sx = 0.f;
-            bool finite = true;
-#pragma unroll
-            for (int i = 0; i < W; ++i) {
-                m = fmaxf(m, fabsf(v[i]));
-                sx = __fadd_rn(sx, v[i]);
-                finite = finite && (fabsf(v[i]) <= 3.402823466e38f);
-            }
-            const int e = int(__float_as_uint(m) >> 23);           // m in [2^(e-127), 2^(e-126))
-            const bool live_chunk = e >= 15;
-            // 2^(15-k) = 2^(141-e) and 2^(k-15) = 2^(e-141), k = e - 126, as float bits
-            const float up = live_chunk ? __uint_as_float(uint32_t(268 - e) << 23) : 0.f;
-            float down = live_chunk ? __uint_as_float(uint32_t(e - 14) << 23) : 0.f;
-            if (!finite) down = __uint_as_float(0x7FC00000u);
             float y[W];
-            float sXf = 0.f;
-#pragma unroll
-            for (int i = 0; i < W; ++i) {
-                y[i] = fminf(__fmaf_rn(v[i], up, 12582912.0f), 12615679.0f);   // 1.5 * 2^23 + X, X <= 32767
-                sXf = __fadd_rn(sXf, __fsub_rn(y[i], 12582912.0f));            // sum of X, exact
-            }
+            float down, sx, sXf;
+            round_chunk<W>(v, y, down, sx, sXf);
             const uint32_t sX = uint32_t(int(sXf));
             uint32_t* dst = xu + (c * kCS + t * S) * 4;
             if constexpr (FMT == QG_Q8_0) {
