@@ -7,9 +7,10 @@
 // table: effective bandwidth = weight bytes / time).  The Metal tiles on those
 // pages were made for Apple GPUs; this is a GB300 design:
 //
-//  * Persistent grid (a few CTAs per SM).  Each CTA stages x once, in fp32,
-//    in shared memory with an XOR swizzle that makes the lanes' reads
-//    conflict-free, so x never costs HBM traffic after the first read.
+//  * Persistent grid (a few CTAs per SM).  Each CTA stages x once in shared
+//    memory (16-bit integers for the integer chunk dot, fp32 for BF16), chunk by
+//    chunk with an odd chunk stride that makes the lanes' loads conflict-free,
+//    so x never costs HBM traffic after the first read.
 //  * Weights move HBM -> shared memory by TMA tensor copies
 //    (cp.async.bulk.tensor.2d, completion counted on an mbarrier), never
 //    through registers: each warp owns a ring of `depth` stages, a stage holds
@@ -41,10 +42,11 @@
 //  * The affine bias term b*sum(x) uses per-chunk fp32 sums of x computed once
 //    per CTA in a fixed order.
 //  * Reduction: per lane, chunks in increasing order; across the warp, a
-//    transposed butterfly (reduce-scatter by halving, then xor steps).  The
-//    order depends only on (fmt, n_in), never on ntok, the tile or the grid, so
-//    a token's outputs are bitwise identical for every ntok (the opus-mtp-turbo
-//    Track 1 report, item 3, relies on exactly this property).
+//    transposed butterfly (reduce-scatter by halving, then xor steps); where a
+//    row's steps are split over a team of warps, the segments' sums in segment
+//    order.  The order depends only on (fmt, n_out, n_in), never on ntok, the
+//    tile or the grid, so a token's outputs are bitwise identical for every ntok
+//    (the opus-mtp-turbo Track 1 report, item 3, relies on exactly this property).
 //  * The fused argmax (perf(speculative): cut the MTP drafter's per-step
 //    cost, Phase 2 item 2a) keeps a running (max, lowest index) per lane,
 //    reduces it per CTA into the workspace, and the last CTA to take a ticket
@@ -196,19 +198,6 @@ __device__ __forceinline__ f2_t f2_pack(uint32_t lo, uint32_t hi) {
     asm("mov.b64 %0, {%1,%2};" : "=l"(d) : "r"(lo), "r"(hi));
     return d;
 }
-__device__ __forceinline__ f2_t f2_const(float v) {
-    return f2_pack(__float_as_uint(v), __float_as_uint(v));
-}
-__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
-    f2_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
-    f2_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 __device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
     f2_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
@@ -219,12 +208,6 @@ __device__ __forceinline__ float f2_sum(f2_t a) {
     float x, y;
     asm("mov.b64 {%0,%1}, %2;" : "=f"(x), "=f"(y) : "l"(a));
     return __fadd_rn(x, y);
-}
-// One pair from shared memory.
-__device__ __forceinline__ f2_t lds_f2(uint32_t a) {
-    f2_t p;
-    asm volatile("ld.shared.b64 %0, [%1];" : "=l"(p) : "r"(a));
-    return p;
 }
 // Two consecutive pairs (four floats) from shared memory.
 __device__ __forceinline__ void lds_f2x2(uint32_t a, f2_t& p0, f2_t& p1) {
