@@ -356,14 +356,14 @@ qg_status qgemv_argmax_noalloc(qg_fmt fmt, const void* W, int64_t n_out, int64_t
  * cut into P segments, one per warp of a team, and the segments' sums are added
  * in segment order.  P fixes the reduction order, so it never depends on ntok
  * or the geometry: for a given matrix every ntok and every geometry give
- * bitwise the same rows.  (Vocabulary-sized heads use P = 1; projections with a
- * few row groups per warp use about one segment per three steps.)
+ * bitwise the same rows.  (P = 1 for n_out >= 8192 or at most 6 steps of 512
+ * code bytes per row; otherwise one segment per four steps, at most 4.)
  *
  * qg_set_tile_override: force a geometry for later calls, e.g.
  * "rpw=4,depth=4,warps=8,ctas=2,pre=1,split=2,gw=4" (any subset of the keys; rpw in
  * {1,2,3,4,5,6,8}: 1, 2, 4 for every ntok, 8 for ntok <= 3, 6 for ntok 2-4,
- * 3 and 5 for ntok 4 (QG_EUNSUPPORTED otherwise); where rpw * ntok > 20 (or
- * >= 16 with 4-bit codes at ntok >= 2) a CTA has at most 12 warps; depth in
+ * 3 and 5 for ntok 4 (QG_EUNSUPPORTED otherwise); where rpw * ntok > 20 a CTA
+ * has at most 12 warps; depth in
  * {2..16}, warps in {1..16}, ctas in {1..8}, pre in {1..16}: the ring stages each
  * warp requests before the wait for the previous kernel, the rest once x is
  * staged (capped at depth), split in {1..8}, gw in {0..64}: the expert calls'
